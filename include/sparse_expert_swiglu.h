@@ -1,0 +1,199 @@
+/*
+ * sparse_expert_swiglu.h -- C ABI of the GB300 (sm_103a) decode-time MoE library
+ * with contextually sparse SwiGLU experts.
+ *
+ * What it computes (page title, section):
+ *   - "FloE: On-the-Fly MoE Inference on Memory-constrained GPU", sec. 三
+ *     "MoE 专家前向计算": a SwiGLU expert a_E(x) = (SiLU(x W^gate) (.) x W^up) W^down;
+ *     "混合压缩策略": W^up stored INT2, W^gate / W^down sparsified by activation;
+ *     "系统协同优化", Algorithm 1 "Efficient Sparse Kernel":
+ *        v = x W^up;  mask = |v| > t_ij;  x' = SiLU(x W^gate[:, mask]) (.) v[mask];
+ *        out = x' W^down[mask, :]
+ *     with W^down stored transposed (one contiguous d-vector per intermediate
+ *     column), only selected columns loaded, SiLU fused with the product.
+ *   - "MoE-Lightning: High-Throughput MoE Inference on Memory-constrained GPUs",
+ *     sec. 三 "MoE 模型架构": a gating network chooses the top-k experts of each
+ *     token; "MOE-INFINITY ...", sec. A3 background: Mixtral-8x7B has 8 experts
+ *     and routes each token to 2 of them.
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, unless the
+ *     comment says "host".  The library allocates nothing and keeps no global
+ *     mutable state; all scratch lives in the caller's workspace.
+ *   - fp16 tensors are IEEE binary16 bit patterns passed as uint16_t.  All
+ *     arrays are dense, row-major, and start on a 16-byte boundary.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on it and returns without
+ *     synchronising, except moe_get_status().
+ *   - Return value: MOE_OK (0) or a negative moe_status_t.  Argument errors
+ *     are detected on the host before anything is enqueued.  Errors found on
+ *     the device (a bounded wait that ran out) are recorded in the workspace
+ *     and reported by moe_get_status().
+ *   - Thread safety: calls may be made from several host threads as long as
+ *     concurrent calls use different workspaces.
+ */
+#ifndef SPARSE_EXPERT_SWIGLU_H
+#define SPARSE_EXPERT_SWIGLU_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int moe_status_t;
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,        /* NULL where a pointer is required, negative size, k > E ... */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2,  /* see "Shape limits" below */
+  MOE_ERR_ALIGNMENT = -3,          /* a pointer is not 16-byte aligned (workspace: 256-byte) */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -4,
+  MOE_ERR_CUDA = -5,               /* a CUDA runtime call or a launch failed */
+  MOE_ERR_TIMEOUT = -6,            /* a bounded device-side wait ran out (moe_get_status) */
+  MOE_ERR_OOM = -7
+};
+
+/*
+ * Shape limits (MOE_ERR_UNSUPPORTED_SHAPE otherwise):
+ *   hidden size d: multiple of 256, 256 <= d <= 7936
+ *   intermediate size f (per expert): multiple of 16, 16 <= f <= 65536
+ *   routed experts E: 1..256; top-k: 1 <= k <= min(E, 8); shared experts: 0..8
+ *   tokens per call B (or n): 0..1024 (0 is a no-op that returns MOE_OK)
+ */
+
+/* One stack of equally shaped experts of one layer. */
+typedef struct {
+  int32_t E;                 /* number of experts in the stack */
+  int32_t d;                 /* hidden size */
+  int32_t f;                 /* intermediate size of one expert */
+  const void* up_packed;     /* [E][expert_int2_up_packed_bytes(d, f)] from expert_pack_int2_up */
+  const uint16_t* gate_t;    /* fp16 [E][f][d]: row i = column i of W^gate */
+  const uint16_t* down;      /* fp16 [E][f][d]: row i = row i of W^down (the transposed,
+                                column-major W^down of FloE's kernel optimisation list) */
+  const float* thr;          /* fp32 [E]: threshold t_ij of Algorithm 1, one per expert */
+} moe_experts_t;
+
+/* One MoE layer. */
+typedef struct {
+  int32_t k;                 /* experts per token */
+  int32_t renorm;            /* 1: weights = softmax over the k chosen logits;
+                                0: full softmax over E, read at the chosen experts */
+  const uint16_t* w_router;  /* fp16 [d][E] router (gating network) weight */
+  moe_experts_t routed;      /* routed experts */
+  moe_experts_t shared;      /* always-on shared experts, weight 1 (E = 0: none);
+                                same d and f as `routed` */
+} moe_layer_t;
+
+/* Optional outputs of moe_layer_decode / moe_expert_sparse_swiglu for tests and
+ * inspection.  Any member may be NULL.  S = k + shared.E (1 for the single-expert
+ * call); slot j < k is the token's j-th routed expert, slot k + s shared expert s. */
+typedef struct {
+  int32_t* topk_idx;   /* [B][k] chosen experts, by logit descending, ties to the lower index */
+  float* topk_w;       /* [B][k] combine weights */
+  uint32_t* mask;      /* [B][S][ceil(f/32)] bit i%32 of word i/32 = (|v_i| > t) */
+  float* v;            /* [B][S][f] fp32 v = x W~^up (step 1 of Algorithm 1) */
+} moe_debug_t;
+
+/* ---------------- INT2 up projection ---------------- */
+
+/* Bytes of one packed expert: (f/16) * ceil(d/512) * 2560.  0 for unsupported shapes. */
+size_t expert_int2_up_packed_bytes(int32_t d, int32_t f);
+
+/*
+ * expert_pack_int2_up -- quantise one W^up to INT2 (FloE "混合压缩策略": Q(.) on the
+ * up projection) and store it in the layout the expert kernels read.
+ *   w_up      fp16 [d][f] (x . W^up gives the f intermediate values); finite values
+ *   up_packed out, expert_int2_up_packed_bytes(d, f) bytes
+ * Scheme (the pages name only "INT2"): one fp16 (scale, zero) per 64-row group and
+ * column, computed with fp32 IEEE operations:
+ *   scale = fp16((max - min) / 3), replaced by 1 if it rounds to 0;
+ *   zero  = fp16(clamp(-min / scale, +-65504));  q = clamp(rint(w / scale + zero), 0, 3)
+ * and W~^up = scale * (q - zero).  Deterministic: the same input gives the same bytes.
+ */
+moe_status_t expert_pack_int2_up(const uint16_t* w_up, int32_t d, int32_t f, void* up_packed,
+                                 void* stream);
+
+/*
+ * expert_unpack_int2_up -- inverse of the storage step of expert_pack_int2_up, for
+ * tests and inspection: writes the codes q uint8 [d][f] (values 0..3), scale and
+ * zero fp16 [d/64][f].  Any of the three outputs may be NULL.
+ */
+moe_status_t expert_unpack_int2_up(const void* up_packed, int32_t d, int32_t f, uint8_t* q,
+                                   uint16_t* scale, uint16_t* zero, void* stream);
+
+/* ---------------- routing ---------------- */
+
+/*
+ * moe_route_topk -- router GEMV and softmax top-k of every token (MoE-Lightning
+ * sec. 三 "MoE 模型架构"; MOE-INFINITY sec. A3).
+ *   x        fp16 [B][d];  w_router fp16 [d][E]
+ *   topk_idx out int32 [B][k]: experts by logit descending, equal logits to the lower index
+ *   topk_w   out fp32 [B][k]: renorm ? softmax over the k chosen logits
+ *                                   : full softmax over E at the chosen experts
+ *   expert_count out int32 [E] or NULL: tokens routed to each expert (one row of
+ *            MOE-INFINITY's iteration-level expert activation matrix)
+ *   ws / ws_bytes: workspace of at least moe_route_workspace_bytes(B, E, k) bytes,
+ *            256-byte aligned, zero-filled once before its first use (moe_workspace_init).
+ */
+size_t moe_route_workspace_bytes(int32_t B, int32_t E, int32_t k);
+moe_status_t moe_route_topk(const uint16_t* x, int32_t B, int32_t d, const uint16_t* w_router,
+                            int32_t E, int32_t k, int32_t renorm, int32_t* topk_idx, float* topk_w,
+                            int32_t* expert_count, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------- one expert ---------------- */
+
+/*
+ * moe_expert_sparse_swiglu -- Algorithm 1 of FloE for one expert of `experts` on n
+ * tokens, weight 1:  y[b] = sum over i with |v_bi| > thr[e] of
+ *                           SiLU(x_b . gate_t[e][i]) * v_bi * down[e][i][:]
+ * with v = x . W~^up (dequantised INT2).  Only the gate and down rows of kept
+ * columns are read.  fp32 accumulation; y is rounded to fp16 once.
+ *   x  fp16 [n][d];  y out fp16 [n][d];  dbg: optional (topk members unused; S = 1)
+ *   ws / ws_bytes: at least moe_expert_workspace_bytes(n, d, f) bytes, 256-byte
+ *   aligned, zero-filled once before its first use (moe_workspace_init).
+ */
+size_t moe_expert_workspace_bytes(int32_t n, int32_t d, int32_t f);
+moe_status_t moe_expert_sparse_swiglu(const uint16_t* x, int32_t n, const moe_experts_t* experts,
+                                      int32_t expert, uint16_t* y, const moe_debug_t* dbg, void* ws,
+                                      size_t ws_bytes, void* stream);
+
+/* ---------------- one layer ---------------- */
+
+/*
+ * moe_layer_decode -- one MoE decode layer on B tokens:
+ *   y[b] = sum_j topk_w[b][j] * E_{topk_idx[b][j]}(x[b]) + sum_s E^shared_s(x[b])
+ * where every expert is the sparse SwiGLU expert above (routed and shared experts
+ * use their own thresholds).  With rmsnorm_out = 1 the result is replaced by
+ * y / sqrt(mean(y^2) + 1e-6) (unit weight) before the fp16 rounding: the hidden
+ * state handed to the next layer of a stack.  Routing stays on the device.
+ *   x fp16 [B][d];  y out fp16 [B][d] (may not alias x);  layer: host pointer to the
+ *   description (its tensor members are device pointers);  dbg: optional.
+ *   ws / ws_bytes: at least moe_layer_workspace_bytes(layer, B) bytes, 256-byte
+ *   aligned, zero-filled once before its first use (moe_workspace_init).
+ */
+size_t moe_layer_workspace_bytes(const moe_layer_t* layer, int32_t B);
+moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* layer, uint16_t* y,
+                              int32_t rmsnorm_out, const moe_debug_t* dbg, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* ---------------- workspace and status ---------------- */
+
+/* Zero-fills `ws` on `stream` (required once after allocating a workspace). */
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the first device-side error
+ * recorded in `ws` since the last call (MOE_OK if none; MOE_ERR_CUDA if the
+ * synchronisation itself failed).
+ */
+moe_status_t moe_get_status(void* ws, void* stream);
+
+/* Static string for a status code. */
+const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_EXPERT_SWIGLU_H */

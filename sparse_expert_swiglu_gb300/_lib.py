@@ -1,0 +1,320 @@
+"""ctypes binding of the C ABI in include/sparse_expert_swiglu.h.
+
+Argument marshalling only: every step of the MoE path runs in the CUDA library.
+torch provides device memory and the current stream.  There is no fallback: if
+the library is missing, `lib()` raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+_STATUS = {
+    0: "ok", -1: "invalid argument", -2: "unsupported shape", -3: "misaligned pointer",
+    -4: "workspace too small", -5: "CUDA error", -6: "device-side wait timed out",
+    -7: "out of memory",
+}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {_STATUS.get(status, status)} ({status})")
+        self.status = status
+
+
+class _Experts(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int32), ("d", ctypes.c_int32), ("f", ctypes.c_int32),
+                ("up_packed", ctypes.c_void_p), ("gate_t", ctypes.c_void_p),
+                ("down", ctypes.c_void_p), ("thr", ctypes.c_void_p)]
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_int32), ("renorm", ctypes.c_int32), ("w_router", ctypes.c_void_p),
+                ("routed", _Experts), ("shared", _Experts)]
+
+
+class _Debug(ctypes.Structure):
+    _fields_ = [("topk_idx", ctypes.c_void_p), ("topk_w", ctypes.c_void_p),
+                ("mask", ctypes.c_void_p), ("v", ctypes.c_void_p)]
+
+
+_LIB = None
+_SIGS = {
+    "expert_int2_up_packed_bytes": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32]),
+    "expert_pack_int2_up": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_void_p, ctypes.c_void_p]),
+    "expert_unpack_int2_up": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p]),
+    "moe_route_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32] * 3),
+    "moe_route_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                      ctypes.c_void_p]),
+    "moe_expert_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32] * 3),
+    "moe_expert_sparse_swiglu": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
+                                                ctypes.POINTER(_Experts), ctypes.c_int32,
+                                                ctypes.c_void_p, ctypes.POINTER(_Debug),
+                                                ctypes.c_void_p, ctypes.c_size_t,
+                                                ctypes.c_void_p]),
+    "moe_layer_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(_Layer), ctypes.c_int32]),
+    "moe_layer_decode": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(_Layer),
+                                        ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(_Debug),
+                                        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_workspace_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_get_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+EXPORTED = tuple(_SIGS)
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built ({path}); run __graft_entry__.build()")
+        handle = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = handle
+    return _LIB
+
+
+def _check(fn: str, status: int) -> None:
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def _stream() -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+# ---------------------------------------------------------------------------
+# workspace
+# ---------------------------------------------------------------------------
+
+class Workspace:
+    """A zero-initialised device workspace (256-byte aligned torch allocation)."""
+
+    def __init__(self, nbytes: int, device=None):
+        self.nbytes = int(nbytes)
+        self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device or "cuda")
+        _check("moe_workspace_init", lib().moe_workspace_init(_ptr(self.buf), self.buf.numel(), _stream()))
+
+    def ptr(self):
+        return _ptr(self.buf)
+
+    def status(self) -> int:
+        """Synchronise and return (and clear) the first device-side error."""
+        return lib().moe_get_status(self.ptr(), _stream())
+
+
+# ---------------------------------------------------------------------------
+# INT2 up projection
+# ---------------------------------------------------------------------------
+
+def packed_bytes(d: int, f: int) -> int:
+    return int(lib().expert_int2_up_packed_bytes(d, f))
+
+
+def pack_int2_up(w_up: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """W^up fp16 [d, f] -> packed INT2 bytes (uint8 [packed_bytes(d, f)])."""
+    _need(w_up, torch.float16, "w_up")
+    d, f = w_up.shape
+    if out is None:
+        out = torch.empty(packed_bytes(d, f), dtype=torch.uint8, device=w_up.device)
+    _check("expert_pack_int2_up", lib().expert_pack_int2_up(_ptr(w_up), d, f, _ptr(out), _stream()))
+    return out
+
+
+def unpack_int2_up(packed: torch.Tensor, d: int, f: int):
+    """Packed bytes -> (q uint8 [d, f], scale fp16 [d/64, f], zero fp16 [d/64, f])."""
+    _need(packed, torch.uint8, "packed")
+    q = torch.empty((d, f), dtype=torch.uint8, device=packed.device)
+    s = torch.empty((d // 64, f), dtype=torch.float16, device=packed.device)
+    z = torch.empty((d // 64, f), dtype=torch.float16, device=packed.device)
+    _check("expert_unpack_int2_up",
+           lib().expert_unpack_int2_up(_ptr(packed), d, f, _ptr(q), _ptr(s), _ptr(z), _stream()))
+    return q, s, z
+
+
+# ---------------------------------------------------------------------------
+# experts and layers
+# ---------------------------------------------------------------------------
+
+@dataclass
+class Experts:
+    """A stack of E equally shaped experts (device tensors).
+
+    up_packed uint8 [E, packed_bytes(d, f)]; gate_t fp16 [E, f, d] (row i = column i
+    of W^gate); down fp16 [E, f, d] (row i = row i of W^down); thr fp32 [E]."""
+    up_packed: torch.Tensor
+    gate_t: torch.Tensor
+    down: torch.Tensor
+    thr: torch.Tensor
+
+    @property
+    def E(self):
+        return self.gate_t.shape[0]
+
+    @property
+    def f(self):
+        return self.gate_t.shape[1]
+
+    @property
+    def d(self):
+        return self.gate_t.shape[2]
+
+    def c_struct(self) -> _Experts:
+        _need(self.up_packed, torch.uint8, "up_packed")
+        _need(self.gate_t, torch.float16, "gate_t")
+        _need(self.down, torch.float16, "down")
+        _need(self.thr, torch.float32, "thr")
+        return _Experts(self.E, self.d, self.f, self.up_packed.data_ptr(), self.gate_t.data_ptr(),
+                        self.down.data_ptr(), self.thr.data_ptr())
+
+    @staticmethod
+    def from_dense(w_up: torch.Tensor, gate_t: torch.Tensor, down: torch.Tensor,
+                   thr: torch.Tensor) -> "Experts":
+        """Pack every W^up [E, d, f] with the library's INT2 quantiser."""
+        E, d, f = w_up.shape
+        up = torch.empty((E, packed_bytes(d, f)), dtype=torch.uint8, device=w_up.device)
+        for e in range(E):
+            pack_int2_up(w_up[e].contiguous(), up[e])
+        return Experts(up, gate_t.contiguous(), down.contiguous(), thr.contiguous())
+
+
+def _empty_experts(d: int, f: int) -> _Experts:
+    return _Experts(0, d, f, None, None, None, None)
+
+
+@dataclass
+class Layer:
+    w_router: torch.Tensor       # fp16 [d, E]
+    routed: Experts
+    k: int
+    renorm: bool = True
+    shared: Optional[Experts] = None
+
+    def c_struct(self) -> _Layer:
+        _need(self.w_router, torch.float16, "w_router")
+        r = self.routed.c_struct()
+        s = self.shared.c_struct() if self.shared is not None else _empty_experts(r.d, r.f)
+        return _Layer(self.k, 1 if self.renorm else 0, self.w_router.data_ptr(), r, s)
+
+    @property
+    def n_slots(self) -> int:
+        return self.k + (self.shared.E if self.shared is not None else 0)
+
+
+def _debug(B: int, S: int, f: int, k: int, device, with_route: bool):
+    t = dict(mask=torch.zeros((B, S, (f + 31) // 32), dtype=torch.int32, device=device),
+             v=torch.zeros((B, S, f), dtype=torch.float32, device=device))
+    if with_route:
+        t["topk_idx"] = torch.zeros((B, k), dtype=torch.int32, device=device)
+        t["topk_w"] = torch.zeros((B, k), dtype=torch.float32, device=device)
+    dbg = _Debug(_ptr(t.get("topk_idx")), _ptr(t.get("topk_w")), _ptr(t["mask"]), _ptr(t["v"]))
+    return dbg, t
+
+
+def route_workspace_bytes(B: int, E: int, k: int) -> int:
+    return int(lib().moe_route_workspace_bytes(B, E, k))
+
+
+def route_topk(x: torch.Tensor, w_router: torch.Tensor, k: int, renorm: bool = True,
+               ws: Optional[Workspace] = None):
+    """-> (topk_idx int32 [B, k], topk_w fp32 [B, k], expert_count int32 [E])."""
+    _need(x, torch.float16, "x")
+    _need(w_router, torch.float16, "w_router")
+    B, d = x.shape
+    E = w_router.shape[1]
+    if ws is None:
+        ws = Workspace(route_workspace_bytes(B, E, k), x.device)
+    idx = torch.empty((B, k), dtype=torch.int32, device=x.device)
+    w = torch.empty((B, k), dtype=torch.float32, device=x.device)
+    cnt = torch.empty((E,), dtype=torch.int32, device=x.device)
+    _check("moe_route_topk", lib().moe_route_topk(_ptr(x), B, d, _ptr(w_router), E, k,
+                                                  1 if renorm else 0, _ptr(idx), _ptr(w),
+                                                  _ptr(cnt), ws.ptr(), ws.nbytes, _stream()))
+    return idx, w, cnt
+
+
+def expert_workspace_bytes(n: int, d: int, f: int) -> int:
+    return int(lib().moe_expert_workspace_bytes(n, d, f))
+
+
+def expert_sparse_swiglu(x: torch.Tensor, experts: Experts, expert: int,
+                         ws: Optional[Workspace] = None, debug: bool = False,
+                         out: Optional[torch.Tensor] = None):
+    """One sparse SwiGLU expert on every row of x (fp16 [n, d]) -> y fp16 [n, d]
+    (and, with debug, a dict with mask int32 [n, 1, ceil(f/32)] and v fp32 [n, 1, f])."""
+    _need(x, torch.float16, "x")
+    n, d = x.shape
+    ex = experts.c_struct()
+    if ws is None:
+        ws = Workspace(expert_workspace_bytes(n, d, experts.f), x.device)
+    y = out if out is not None else torch.empty_like(x)
+    dbg, dt = (None, None)
+    if debug:
+        dbg, dt = _debug(n, 1, experts.f, 1, x.device, False)
+    _check("moe_expert_sparse_swiglu",
+           lib().moe_expert_sparse_swiglu(_ptr(x), n, ctypes.byref(ex), expert, _ptr(y),
+                                          ctypes.byref(dbg) if dbg is not None else None,
+                                          ws.ptr(), ws.nbytes, _stream()))
+    return (y, dt) if debug else y
+
+
+def layer_workspace_bytes(layer: Layer, B: int) -> int:
+    c = layer.c_struct()
+    return int(lib().moe_layer_workspace_bytes(ctypes.byref(c), B))
+
+
+def layer_decode(x: torch.Tensor, layer: Layer, rmsnorm: bool = False,
+                 ws: Optional[Workspace] = None, debug: bool = False,
+                 out: Optional[torch.Tensor] = None, c_layer: Optional[_Layer] = None):
+    """One MoE decode layer on x fp16 [B, d] -> y fp16 [B, d] (and the debug dict)."""
+    _need(x, torch.float16, "x")
+    B, d = x.shape
+    c = c_layer if c_layer is not None else layer.c_struct()
+    if ws is None:
+        ws = Workspace(int(lib().moe_layer_workspace_bytes(ctypes.byref(c), B)), x.device)
+    y = out if out is not None else torch.empty_like(x)
+    dbg, dt = (None, None)
+    if debug:
+        dbg, dt = _debug(B, layer.n_slots, layer.routed.f, layer.k, x.device, True)
+    _check("moe_layer_decode",
+           lib().moe_layer_decode(_ptr(x), B, ctypes.byref(c), _ptr(y), 1 if rmsnorm else 0,
+                                  ctypes.byref(dbg) if dbg is not None else None,
+                                  ws.ptr(), ws.nbytes, _stream()))
+    return (y, dt) if debug else y

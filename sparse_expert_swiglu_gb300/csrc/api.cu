@@ -1,0 +1,396 @@
+// extern "C" entry points: argument checks, workspace carving and kernel launches.
+#include <string.h>
+
+#include "params.cuh"
+
+using namespace sesg;
+
+namespace {
+
+constexpr size_t kWsAlign = 256;
+constexpr int kMaxB = 1024;
+constexpr int kMaxD = 7936;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+struct DeviceInfo {
+  int sms = 0;
+  int smem_optin = 0;
+  int smem_per_sm = 0;
+};
+
+cudaError_t device_info(DeviceInfo& di) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  return cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+}
+
+// Tokens of one expert handled together: their fp32 accumulators must fit in the
+// gather kernel's registers (8 x 8 floats per thread up to d = 4096, 4 x 8 up to 6144).
+int group_cap(int d) { return d <= 4096 ? 8 : d <= 6144 ? 4 : 2; }
+
+int groups_max_routed(int B, int E, int k, int gcap) {
+  const long long pairs = (long long)B * k;
+  const long long bound = (pairs + gcap - 1) / gcap + (E < pairs ? E : pairs);
+  return (int)(pairs < bound ? pairs : bound);
+}
+
+// Workspace carving shared by every entry point.
+struct WsLayout {
+  size_t ctrl, groups, tok_groups, topk_idx, topk_w, group_total, unit_cnt, item_col, item_v,
+      part, yacc, sumsq, tok_ctr, total;
+  int G_max, P3, list_cap;
+};
+
+WsLayout ws_layout(int B, int npairs, int G_max, int d, int f, int P3) {
+  WsLayout L;
+  const int MT = f / kMTile;
+  const int list_cap = (int)(((long long)G_max * f + P3 - 1) / P3 + 1);
+  L.G_max = G_max;
+  L.P3 = P3;
+  L.list_cap = list_cap < 2048 ? list_cap : 2048;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, kWsAlign);
+    return at;
+  };
+  L.ctrl = take(sizeof(Ctrl));
+  L.groups = take(sizeof(GroupDesc) * (size_t)(G_max > 0 ? G_max : 1));
+  L.tok_groups = take(sizeof(int) * (size_t)B * kMaxSlots);
+  L.topk_idx = take(sizeof(int) * (size_t)(npairs > 0 ? npairs : 1));
+  L.topk_w = take(sizeof(float) * (size_t)(npairs > 0 ? npairs : 1));
+  L.group_total = take(sizeof(int) * (size_t)(G_max > 0 ? G_max : 1));
+  L.unit_cnt = take((size_t)G_max * MT);
+  L.item_col = take(sizeof(int) * (size_t)G_max * MT * 16);
+  L.item_v = take(sizeof(float) * (size_t)G_max * MT * 16 * 8);
+  L.part = take(sizeof(float) * (size_t)(P3 + G_max) * kMaxTok * d);
+  L.yacc = take(sizeof(float) * (size_t)B * d);
+  L.sumsq = take(sizeof(float) * (size_t)B * (d / 128));
+  L.tok_ctr = take(sizeof(int) * (size_t)B);
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(ws) + off);
+}
+
+moe_status_t check_experts(const moe_experts_t* ex, int d, int f, bool may_be_empty) {
+  if (!ex) return MOE_ERR_INVALID_ARG;
+  if (ex->E == 0 && may_be_empty) return MOE_OK;
+  if (ex->E < 1 || ex->E > 256) return ex->E < 0 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ex->d != d || ex->f != f) return MOE_ERR_INVALID_ARG;
+  if (!ex->up_packed || !ex->gate_t || !ex->down || !ex->thr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ex->up_packed, 16) || !aligned(ex->gate_t, 16) || !aligned(ex->down, 16) ||
+      !aligned(ex->thr, 4))
+    return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+moe_status_t check_dims(int d, int f) {
+  if (d <= 0 || f <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 256 || d > kMaxD || f % kMTile || f > 65536) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+ExpertSet to_set(const moe_experts_t& ex) {
+  ExpertSet s;
+  s.E = ex.E;
+  s.d = ex.d;
+  s.f = ex.f;
+  s.up = reinterpret_cast<const uint8_t*>(ex.up_packed);
+  s.gate_t = reinterpret_cast<const __half*>(ex.gate_t);
+  s.down = reinterpret_cast<const __half*>(ex.down);
+  s.thr = ex.thr;
+  s.up_stride = packed_bytes_per_expert(ex.d, ex.f);
+  return s;
+}
+
+struct Plan {
+  int up_grid;
+  int stages;
+  int nt;
+};
+
+// Grid of the up kernel, depth of the gather pipeline.
+moe_status_t plan(const DeviceInfo& di, const WsLayout& L, int d, int f, int max_tok, Plan& pl) {
+  const size_t up_smem = up_smem_bytes(d);
+  if (up_smem + 1024 > (size_t)di.smem_optin) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int occ = (int)(di.smem_per_sm / (up_smem + 1024));
+  occ = occ < 1 ? 1 : (occ > 2 ? 2 : occ);
+  pl.up_grid = di.sms * occ;
+  pl.nt = max_tok <= 1 ? 1 : max_tok <= 2 ? 2 : max_tok <= 4 ? 4 : 8;
+  const size_t fixed = gather_smem_bytes(d, 0, pl.nt, L.list_cap) + 2048;
+  const size_t stage = (size_t)4 * d + 32 + 16;
+  if (fixed + 2 * stage > (size_t)di.smem_optin) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int S = (int)((di.smem_optin - fixed) / stage);
+  S = S > 16 ? 16 : S;
+  // the gather prologue borrows the stage buffers as scratch for its scans
+  const size_t scratch = sizeof(int) * ((size_t)2 * L.G_max + f / kMTile + 4);
+  while ((size_t)S * (4 * d + 32) < scratch && S < 64) ++S;
+  if (gather_smem_bytes(d, S, pl.nt, L.list_cap) > (size_t)di.smem_optin)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  pl.stages = S;
+  return MOE_OK;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t expert_int2_up_packed_bytes(int32_t d, int32_t f) {
+  if (d <= 0 || f <= 0 || d % kGroup || f % kMTile) return 0;
+  return packed_bytes_per_expert(d, f);
+}
+
+moe_status_t expert_pack_int2_up(const uint16_t* w_up, int32_t d, int32_t f, void* up_packed,
+                                 void* stream) {
+  if (!w_up || !up_packed || d <= 0 || f <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % kGroup || f % kMTile) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(w_up, 16) || !aligned(up_packed, 16)) return MOE_ERR_ALIGNMENT;
+  return cuda_status(launch_pack(reinterpret_cast<const __half*>(w_up), d, f,
+                                 reinterpret_cast<uint8_t*>(up_packed), (cudaStream_t)stream));
+}
+
+moe_status_t expert_unpack_int2_up(const void* up_packed, int32_t d, int32_t f, uint8_t* q,
+                                   uint16_t* scale, uint16_t* zero, void* stream) {
+  if (!up_packed || d <= 0 || f <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % kGroup || f % kMTile) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(up_packed, 16)) return MOE_ERR_ALIGNMENT;
+  return cuda_status(launch_unpack(reinterpret_cast<const uint8_t*>(up_packed), d, f, q,
+                                   reinterpret_cast<__half*>(scale),
+                                   reinterpret_cast<__half*>(zero), (cudaStream_t)stream));
+}
+
+size_t moe_route_workspace_bytes(int32_t B, int32_t E, int32_t k) {
+  if (B < 0 || E < 1 || k < 1) return 0;
+  return ws_layout(B, B * k, 0, 256, kMTile, 1).total;
+}
+
+moe_status_t moe_route_topk(const uint16_t* x, int32_t B, int32_t d, const uint16_t* w_router,
+                            int32_t E, int32_t k, int32_t renorm, int32_t* topk_idx, float* topk_w,
+                            int32_t* expert_count, void* ws, size_t ws_bytes, void* stream) {
+  if (B < 0 || d <= 0 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (B > kMaxB || E > 256 || k > kMaxTok || d % 256 || d > kMaxD) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return MOE_OK;
+  if (!x || !w_router || !topk_idx || !topk_w || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16)) return MOE_ERR_ALIGNMENT;
+  if (!aligned(ws, kWsAlign)) return MOE_ERR_ALIGNMENT;
+  const WsLayout L = ws_layout(B, B * k, 0, 256, kMTile, 1);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  RouteParams rp = {};
+  rp.x = reinterpret_cast<const __half*>(x);
+  rp.w_router = reinterpret_cast<const __half*>(w_router);
+  rp.B = B;
+  rp.d = d;
+  rp.E = E;
+  rp.k = k;
+  rp.renorm = renorm ? 1 : 0;
+  rp.group = 0;
+  rp.gcap = kMaxTok;
+  rp.topk_idx = at<int32_t>(ws, L.topk_idx);
+  rp.topk_w = at<float>(ws, L.topk_w);
+  rp.user_idx = topk_idx;
+  rp.user_w = topk_w;
+  rp.expert_count = expert_count;
+  rp.ctrl = at<Ctrl>(ws, L.ctrl);
+  return cuda_status(launch_route(rp, (cudaStream_t)stream, true));
+}
+
+// ---------------------------------------------------------------------------
+
+static moe_status_t run_experts(const uint16_t* x, int B, const moe_experts_t* routed,
+                                const moe_experts_t* shared, int n_slots, uint16_t* y,
+                                int rmsnorm, const moe_debug_t* dbg, void* ws,
+                                const WsLayout& L, const DeviceInfo& di, int max_tok,
+                                cudaStream_t st) {
+  Plan pl;
+  moe_status_t s = plan(di, L, routed->d, routed->f, max_tok, pl);
+  if (s != MOE_OK) return s;
+  ExpertParams p = {};
+  p.routed = to_set(*routed);
+  if (shared && shared->E > 0) p.shared = to_set(*shared);
+  p.x = reinterpret_cast<const __half*>(x);
+  p.B = B;
+  p.d = routed->d;
+  p.f = routed->f;
+  p.groups = at<GroupDesc>(ws, L.groups);
+  p.ctrl = at<Ctrl>(ws, L.ctrl);
+  p.unit_cnt = at<uint8_t>(ws, L.unit_cnt);
+  p.item_col = at<int>(ws, L.item_col);
+  p.item_v = at<float>(ws, L.item_v);
+  p.group_total = at<int>(ws, L.group_total);
+  p.part = at<float>(ws, L.part);
+  p.tok_groups = at<int>(ws, L.tok_groups);
+  p.n_slots = n_slots;
+  p.dbg_v = dbg ? dbg->v : nullptr;
+  p.dbg_mask = dbg ? dbg->mask : nullptr;
+  p.y = reinterpret_cast<__half*>(y);
+  p.rmsnorm = rmsnorm;
+  p.yacc = at<float>(ws, L.yacc);
+  p.sumsq = at<float>(ws, L.sumsq);
+  p.tok_ctr = at<int>(ws, L.tok_ctr);
+  p.P3 = L.P3;
+  p.stages = pl.stages;
+  p.list_cap = L.list_cap;
+  p.G_max = L.G_max;
+  cudaError_t e = launch_up(p, pl.up_grid, st, true);
+  if (e == cudaSuccess) e = launch_gather(p, pl.nt, st, true);
+  if (e == cudaSuccess) e = launch_combine(p, st, true);
+  return cuda_status(e);
+}
+
+size_t moe_expert_workspace_bytes(int32_t n, int32_t d, int32_t f) {
+  if (n < 0 || check_dims(d, f) != MOE_OK) return 0;
+  DeviceInfo di;
+  if (device_info(di) != cudaSuccess) return 0;
+  const int gcap = group_cap(d);
+  return ws_layout(n, n, (n + gcap - 1) / gcap, d, f, di.sms).total;
+}
+
+moe_status_t moe_expert_sparse_swiglu(const uint16_t* x, int32_t n, const moe_experts_t* experts,
+                                      int32_t expert, uint16_t* y, const moe_debug_t* dbg, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  if (n < 0 || !experts) return MOE_ERR_INVALID_ARG;
+  moe_status_t s = check_dims(experts->d, experts->f);
+  if (s != MOE_OK) return s;
+  if (n > kMaxB) return MOE_ERR_UNSUPPORTED_SHAPE;
+  s = check_experts(experts, experts->d, experts->f, false);
+  if (s != MOE_OK) return s;
+  if (expert < 0 || expert >= experts->E) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!x || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_ALIGNMENT;
+  if (!aligned(ws, kWsAlign)) return MOE_ERR_ALIGNMENT;
+  DeviceInfo di;
+  if (device_info(di) != cudaSuccess) return MOE_ERR_CUDA;
+  const int gcap = group_cap(experts->d);
+  const WsLayout L = ws_layout(n, n, (n + gcap - 1) / gcap, experts->d, experts->f, di.sms);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = launch_expert_prep(expert, n, gcap, at<GroupDesc>(ws, L.groups),
+                                     at<int>(ws, L.tok_groups), at<int>(ws, L.group_total),
+                                     at<Ctrl>(ws, L.ctrl), st, true);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return run_experts(x, n, experts, nullptr, 1, y, 0, dbg, ws, L, di, n < gcap ? n : gcap, st);
+}
+
+static moe_status_t check_layer(const moe_layer_t* layer, int B) {
+  if (!layer || B < 0) return MOE_ERR_INVALID_ARG;
+  const moe_experts_t& r = layer->routed;
+  moe_status_t s = check_dims(r.d, r.f);
+  if (s != MOE_OK) return s;
+  s = check_experts(&r, r.d, r.f, false);
+  if (s != MOE_OK) return s;
+  s = check_experts(&layer->shared, r.d, r.f, true);
+  if (s != MOE_OK) return s;
+  if (layer->shared.E > 8) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (layer->k < 1 || layer->k > r.E) return MOE_ERR_INVALID_ARG;
+  if (layer->k > kMaxTok || B > kMaxB) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!layer->w_router) return MOE_ERR_INVALID_ARG;
+  if (!aligned(layer->w_router, 16)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+static WsLayout layer_layout(const moe_layer_t* layer, int B, int sms) {
+  const int k = layer->k, E = layer->routed.E, ns = layer->shared.E;
+  const int gcap = group_cap(layer->routed.d);
+  const int G_max = groups_max_routed(B, E, k, gcap) + ns * ((B + gcap - 1) / gcap);
+  return ws_layout(B, B * k, G_max, layer->routed.d, layer->routed.f, sms);
+}
+
+size_t moe_layer_workspace_bytes(const moe_layer_t* layer, int32_t B) {
+  if (check_layer(layer, B) != MOE_OK) return 0;
+  DeviceInfo di;
+  if (device_info(di) != cudaSuccess) return 0;
+  return layer_layout(layer, B, di.sms).total;
+}
+
+moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* layer, uint16_t* y,
+                              int32_t rmsnorm_out, const moe_debug_t* dbg, void* ws,
+                              size_t ws_bytes, void* stream) {
+  moe_status_t s = check_layer(layer, B);
+  if (s != MOE_OK) return s;
+  if (B == 0) return MOE_OK;
+  if (!x || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_ALIGNMENT;
+  if (!aligned(ws, kWsAlign)) return MOE_ERR_ALIGNMENT;
+  DeviceInfo di;
+  if (device_info(di) != cudaSuccess) return MOE_ERR_CUDA;
+  const WsLayout L = layer_layout(layer, B, di.sms);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int k = layer->k;
+  RouteParams rp = {};
+  rp.x = reinterpret_cast<const __half*>(x);
+  rp.w_router = reinterpret_cast<const __half*>(layer->w_router);
+  rp.B = B;
+  rp.d = layer->routed.d;
+  rp.E = layer->routed.E;
+  rp.k = k;
+  rp.renorm = layer->renorm ? 1 : 0;
+  rp.n_shared = layer->shared.E;
+  rp.group = 1;
+  rp.gcap = group_cap(layer->routed.d);
+  rp.topk_idx = at<int32_t>(ws, L.topk_idx);
+  rp.topk_w = at<float>(ws, L.topk_w);
+  rp.user_idx = dbg ? dbg->topk_idx : nullptr;
+  rp.user_w = dbg ? dbg->topk_w : nullptr;
+  rp.expert_count = nullptr;
+  rp.ctrl = at<Ctrl>(ws, L.ctrl);
+  rp.groups = at<GroupDesc>(ws, L.groups);
+  rp.tok_groups = at<int>(ws, L.tok_groups);
+  rp.group_total = at<int>(ws, L.group_total);
+  rp.G_max = L.G_max;
+  if (launch_route(rp, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+  return run_experts(x, B, &layer->routed, &layer->shared, k + layer->shared.E, y,
+                     rmsnorm_out ? 1 : 0, dbg, ws, L, di, B < rp.gcap ? B : rp.gcap, st);
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, kWsAlign)) return MOE_ERR_ALIGNMENT;
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream));
+}
+
+moe_status_t moe_get_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  int status = 0;
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws);  // the control block is always first
+  if (cudaMemcpy(&status, &ctrl->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (status != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(&ctrl->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return status;
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_ALIGNMENT: return "misaligned pointer";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_OOM: return "out of memory";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

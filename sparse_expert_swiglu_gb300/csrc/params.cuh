@@ -1,0 +1,68 @@
+// Kernel parameter blocks and launchers shared by the library's translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace sesg {
+
+struct RouteParams {
+  const __half* x;         // [B][d]
+  const __half* w_router;  // [d][E]
+  int B, d, E, k, renorm;
+  int n_shared;            // always-on shared experts (grouping only)
+  int group;               // 1: build groups for the expert kernels
+  int gcap;                // tokens per group (<= 8)
+  int32_t* topk_idx;       // [B][k] (workspace copy, always written)
+  float* topk_w;           // [B][k]
+  int32_t* user_idx;       // optional copies
+  float* user_w;
+  int32_t* expert_count;   // optional [E]
+  Ctrl* ctrl;
+  GroupDesc* groups;       // grouping outputs
+  int* tok_groups;         // [B][kMaxSlots]: (group << 3) | local token index
+  int* group_total;        // [G_max] zeroed here for the expert kernels
+  int G_max;
+};
+
+struct ExpertParams {
+  ExpertSet routed, shared;
+  const __half* x;          // [B][d]
+  int B, d, f;
+  const GroupDesc* groups;
+  Ctrl* ctrl;
+  uint8_t* unit_cnt;        // [G_max * MT] kept columns per (group, M-tile)
+  int* item_col;            // [G_max * MT * 16]
+  float* item_v;            // [G_max * MT * 16][8]: v of kept columns, 0 for tokens that drop them
+  int* group_total;         // [G_max] kept items per group
+  float* part;              // [(P3 + G_max)][8][d] per-CTA partial outputs
+  const int* tok_groups;    // [B][16]
+  int n_slots;              // slots per token in the debug outputs
+  float* dbg_v;             // [B][n_slots][f] or NULL
+  uint32_t* dbg_mask;       // [B][n_slots][f/32] or NULL
+  __half* y;                // [B][d]
+  int rmsnorm;
+  float* yacc;              // [B][d] (RMSNorm path)
+  float* sumsq;             // [B][d/128]
+  int* tok_ctr;             // [B]
+  int P3;                   // gather CTAs
+  int stages;               // gather pipeline depth
+  int list_cap;             // gather item-list capacity per CTA window
+  int G_max;
+};
+
+// pack.cu
+cudaError_t launch_pack(const __half* w, int d, int f, uint8_t* packed, cudaStream_t st);
+cudaError_t launch_unpack(const uint8_t* packed, int d, int f, uint8_t* q, __half* scale,
+                          __half* zero, cudaStream_t st);
+// route.cu
+cudaError_t launch_route(const RouteParams& p, cudaStream_t st, bool pdl);
+cudaError_t launch_expert_prep(int expert, int n, int gcap, GroupDesc* groups, int* tok_groups,
+                               int* group_total, Ctrl* ctrl, cudaStream_t st, bool pdl);
+// expert.cu
+size_t up_smem_bytes(int d);
+size_t gather_smem_bytes(int d, int stages, int nt, int list_cap);
+cudaError_t launch_up(const ExpertParams& p, int grid, cudaStream_t st, bool pdl);
+cudaError_t launch_gather(const ExpertParams& p, int nt, cudaStream_t st, bool pdl);
+cudaError_t launch_combine(const ExpertParams& p, cudaStream_t st, bool pdl);
+
+}  // namespace sesg

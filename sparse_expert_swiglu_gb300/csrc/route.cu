@@ -1,0 +1,290 @@
+// Router GEMV + softmax top-k of every token, and the grouping of (token, expert)
+// pairs into expert work groups.
+//
+// "MoE-Lightning: High-Throughput MoE Inference on Memory-constrained GPUs", sec. 三
+// "MoE 模型架构": a gating network chooses the top-k experts of every token;
+// "MOE-INFINITY ...", sec. A3 background: Mixtral-8x7B routes each token to 2 of
+// its 8 experts.  Ties between equal logits go to the lower expert index; the
+// chosen experts are listed by logit descending; renorm selects softmax over the
+// chosen logits (1) or the full softmax over all experts (0).
+#include "params.cuh"
+
+namespace sesg {
+
+
+constexpr int kRouteThreads = 256;
+
+// Logits of one token: each thread owns EV consecutive experts and a strided set of rows.
+template <int EV>
+__device__ void router_logits(const RouteParams& p, int b, float* logits, float* red) {
+  const int tid = threadIdx.x;
+  const int nchunk = p.E / EV;          // expert chunks
+  const int nrs = kRouteThreads / nchunk;  // row slots
+  const int ec = tid % nchunk, rs = tid / nchunk;
+  float acc[EV];
+#pragma unroll
+  for (int i = 0; i < EV; ++i) acc[i] = 0.f;
+  if (rs < nrs) {
+    const __half* xb = p.x + (size_t)b * p.d;
+    for (int r = rs; r < p.d; r += nrs) {
+      const float xv = __half2float(xb[r]);
+      const __half* wrow = p.w_router + (size_t)r * p.E + ec * EV;
+      if constexpr (EV == 8) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(wrow);
+        const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 wf = __half22float2(h2[i]);
+          acc[2 * i] = fmaf(xv, wf.x, acc[2 * i]);
+          acc[2 * i + 1] = fmaf(xv, wf.y, acc[2 * i + 1]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < EV; ++i) acc[i] = fmaf(xv, __half2float(wrow[i]), acc[i]);
+      }
+    }
+  }
+  // red[rs][e], then a fixed-order sum over row slots
+  if (rs < nrs) {
+#pragma unroll
+    for (int i = 0; i < EV; ++i) red[rs * p.E + ec * EV + i] = acc[i];
+  }
+  __syncthreads();
+  for (int e = tid; e < p.E; e += kRouteThreads) {
+    float s = 0.f;
+    for (int r = 0; r < nrs; ++r) s += red[r * p.E + e];
+    logits[e] = s;
+  }
+  __syncthreads();
+}
+
+// Warp 0: k rounds of arg-max (larger logit, then lower index), softmax weights.
+__device__ void router_topk(const RouteParams& p, int b, const float* logits) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kPer = 8;  // E <= 256
+  float l[kPer];
+  bool taken[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    l[i] = e < p.E ? logits[e] : -INFINITY;
+    taken[i] = e >= p.E;
+  }
+  float lmax = -INFINITY;
+  int sel_idx[8];
+  float sel_l[8];
+  for (int j = 0; j < p.k; ++j) {
+    float best = -INFINITY;
+    int bidx = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      if (!taken[i] && (l[i] > best || (l[i] == best && e < bidx))) {
+        best = l[i];
+        bidx = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bidx, off);
+      if (ob > best || (ob == best && oi < bidx)) {
+        best = ob;
+        bidx = oi;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (lane + 32 * i == bidx) taken[i] = true;
+    sel_idx[j] = bidx;
+    sel_l[j] = best;
+    if (j == 0) lmax = best;
+  }
+  float denom = 0.f;
+  if (p.renorm) {
+    for (int j = 0; j < p.k; ++j) denom += expf(sel_l[j] - lmax);
+  } else {
+    float part = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (lane + 32 * i < p.E) part += expf(l[i] - lmax);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    denom = part;
+  }
+  if (lane == 0) {
+    for (int j = 0; j < p.k; ++j) {
+      const float w = expf(sel_l[j] - lmax) / denom;
+      p.topk_idx[b * p.k + j] = sel_idx[j];
+      p.topk_w[b * p.k + j] = w;
+      if (p.user_idx) p.user_idx[b * p.k + j] = sel_idx[j];
+      if (p.user_w) p.user_w[b * p.k + j] = w;
+    }
+  }
+}
+
+// Last CTA: counting of tokens per expert and the expert work groups.
+__device__ void router_group(const RouteParams& p) {
+  extern __shared__ float dyn[];
+  int* s_idx = reinterpret_cast<int*>(dyn);   // [B*k]
+  int* s_list = s_idx + p.B * p.k;            // [B*k] (token << 4 | slot) grouped by expert
+  __shared__ int s_cnt[256], s_off[257], s_goff[257];
+  const int tid = threadIdx.x;
+  const int npair = p.B * p.k;
+  for (int i = tid; i < npair; i += kRouteThreads) s_idx[i] = __ldcg(p.topk_idx + i);
+  __syncthreads();
+  for (int e = tid; e < p.E; e += kRouteThreads) {
+    int c = 0;
+    for (int i = 0; i < npair; ++i) c += (s_idx[i] == e);
+    s_cnt[e] = c;
+    if (p.expert_count) p.expert_count[e] = c;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int o = 0, go = 0;
+    for (int e = 0; e < p.E; ++e) {
+      s_off[e] = o;
+      s_goff[e] = go;
+      o += s_cnt[e];
+      go += (s_cnt[e] + p.gcap - 1) / p.gcap;
+    }
+    s_off[p.E] = o;
+    s_goff[p.E] = go;
+  }
+  __syncthreads();
+  if (!p.group) return;
+  // tokens of expert e in ascending order
+  for (int e = tid; e < p.E; e += kRouteThreads) {
+    int o = s_off[e];
+    for (int i = 0; i < npair; ++i)
+      if (s_idx[i] == e) s_list[o++] = ((i / p.k) << 4) | (i % p.k);
+  }
+  __syncthreads();
+  const int g_routed = s_goff[p.E];
+  const int g_per_shared = (p.B + p.gcap - 1) / p.gcap;
+  const int G = g_routed + p.n_shared * g_per_shared;
+  for (int e = tid; e < p.E; e += kRouteThreads) {
+    const int n = s_cnt[e];
+    for (int q = 0; q * p.gcap < n; ++q) {
+      GroupDesc gd;
+      gd.expert = e;
+      gd.n_tok = min(p.gcap, n - q * p.gcap);
+      const int g = s_goff[e] + q;
+      for (int t = 0; t < kMaxTok; ++t) {
+        if (t < gd.n_tok) {
+          const int pr = s_list[s_off[e] + q * p.gcap + t];
+          const int b = pr >> 4, j = pr & 15;
+          gd.tok[t] = b;
+          gd.slot[t] = j;
+          gd.w[t] = __ldcg(p.topk_w + b * p.k + j);
+          p.tok_groups[b * kMaxSlots + j] = (g << 3) | t;
+        } else {
+          gd.tok[t] = 0;
+          gd.slot[t] = 0;
+          gd.w[t] = 0.f;
+        }
+      }
+      p.groups[g] = gd;
+    }
+  }
+  for (int q = tid; q < p.n_shared * g_per_shared; q += kRouteThreads) {
+    const int s = q / g_per_shared, qq = q % g_per_shared;
+    GroupDesc gd;
+    gd.expert = p.E + s;
+    gd.n_tok = min(p.gcap, p.B - qq * p.gcap);
+    const int g = g_routed + q;
+    for (int t = 0; t < kMaxTok; ++t) {
+      const int b = qq * p.gcap + t;
+      gd.tok[t] = t < gd.n_tok ? b : 0;
+      gd.slot[t] = t < gd.n_tok ? p.k + s : 0;
+      gd.w[t] = t < gd.n_tok ? 1.f : 0.f;
+      if (t < gd.n_tok) p.tok_groups[b * kMaxSlots + p.k + s] = (g << 3) | t;
+    }
+    p.groups[g] = gd;
+  }
+  for (int g = tid; g < p.G_max; g += kRouteThreads) p.group_total[g] = 0;
+  if (tid == 0) p.ctrl->G = G;
+}
+
+template <int EV>
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
+  __shared__ float s_logits[256];
+  __shared__ float s_red[kRouteThreads * 8];
+  __shared__ int s_last;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = blockIdx.x;
+  router_logits<EV>(p, b, s_logits, s_red);
+  if (threadIdx.x < 32) router_topk(p, b, s_logits);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(&p.ctrl->route_done, 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  router_group(p);
+  if (threadIdx.x == 0) p.ctrl->route_done = 0;
+}
+
+// Single expert: groups of up to 8 consecutive tokens, weight 1.
+__global__ void expert_prep_kernel(int expert, int n, int gcap, GroupDesc* groups,
+                                   int* tok_groups, int* group_total, Ctrl* ctrl) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int G = (n + gcap - 1) / gcap;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    GroupDesc gd;
+    gd.expert = expert;
+    gd.n_tok = min(gcap, n - g * gcap);
+    for (int t = 0; t < kMaxTok; ++t) {
+      const bool on = t < gd.n_tok;
+      gd.tok[t] = on ? g * gcap + t : 0;
+      gd.slot[t] = 0;
+      gd.w[t] = on ? 1.f : 0.f;
+      if (on) tok_groups[(g * gcap + t) * kMaxSlots] = (g << 3) | t;
+    }
+    groups[g] = gd;
+    group_total[g] = 0;
+  }
+  if (threadIdx.x == 0) ctrl->G = G;
+}
+
+size_t route_group_smem(int B, int k) { return (size_t)2 * B * k * sizeof(int); }
+
+cudaError_t launch_route(const RouteParams& p, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.B);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = route_group_smem(p.B, p.k);
+  cfg.stream = st;
+  if (cfg.dynamicSmemBytes > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(
+        p.E % 8 == 0 ? (const void*)route_kernel<8> : (const void*)route_kernel<1>,
+        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (p.E % 8 == 0) return cudaLaunchKernelEx(&cfg, route_kernel<8>, p);
+  return cudaLaunchKernelEx(&cfg, route_kernel<1>, p);
+}
+
+cudaError_t launch_expert_prep(int expert, int n, int gcap, GroupDesc* groups, int* tok_groups,
+                               int* group_total, Ctrl* ctrl, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(128);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, expert_prep_kernel, expert, n, gcap, groups, tok_groups,
+                            group_total, ctrl);
+}
+
+}  // namespace sesg

@@ -1,0 +1,334 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (marked gpu).
+
+Inputs come from the seeded generator and are handed to both sides; thresholds are
+computed by the oracle from calibration tokens.  Every comparison follows the band
+rule of tests/parity.py.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as orc
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+ses = pytest.importorskip("sparse_expert_swiglu_gb300")
+from sparse_expert_swiglu_gb300 import synth  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ses.build_library()
+    ses.lib()
+
+
+def _np16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+# ---------------------------------------------------------------------------
+# INT2 pack: bit-exact against the oracle's quantiser
+# ---------------------------------------------------------------------------
+
+def _pack_check(w_up: torch.Tensor):
+    d, f = w_up.shape
+    packed = ses.pack_int2_up(w_up.cuda().contiguous())
+    q, s, z = ses.unpack_int2_up(packed, d, f)
+    q_ref, s_ref, z_ref = orc.quantize_int2(_np16(w_up))
+    assert np.array_equal(_np16(q), q_ref)
+    # fp16 values equal (a zero point of -0 and +0 are the same value)
+    assert np.array_equal(_np16(s).astype(np.float64), s_ref.astype(np.float64))
+    assert np.array_equal(_np16(z).astype(np.float64), z_ref.astype(np.float64))
+    # re-packing the same weights gives the same bytes
+    assert torch.equal(packed, ses.pack_int2_up(w_up.cuda().contiguous()))
+
+
+@pytest.mark.parametrize("d,f", [(256, 512), (768, 208), (4096, 1024), (64, 16)])
+def test_pack_random(d, f):
+    _pack_check(synth.normal_f16((d, f), 0.02, 7, d + f))
+
+
+def test_pack_golden_and_degenerate():
+    from tests.test_oracle_pins import _golden_quant_matrix
+    _, w, q_exp = _golden_quant_matrix()
+    w = np.concatenate([w, np.zeros((64, 13), np.float16)], axis=1)  # f = 16, an all-zero group too
+    _pack_check(torch.from_numpy(w))
+    q, _, _ = ses.unpack_int2_up(ses.pack_int2_up(torch.from_numpy(w).cuda()), 64, 16)
+    assert np.array_equal(_np16(q)[:, :3], q_exp)
+
+
+def test_pack_wide_range():
+    # groups with large offsets, tiny spreads and sign mixes
+    rng = np.random.default_rng(3)
+    base = rng.uniform(-1000, 1000, size=(1, 64)).astype(np.float32)
+    spread = 10.0 ** rng.uniform(-6, 2, size=(1, 64)).astype(np.float32)
+    w = (base + spread * rng.standard_normal((512, 64)).astype(np.float32)).astype(np.float16)
+    _pack_check(torch.from_numpy(w))
+
+
+# ---------------------------------------------------------------------------
+# router
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,d,E,k,renorm", [(1, 4096, 8, 2, True), (32, 4096, 8, 2, True),
+                                            (64, 2048, 64, 6, True), (5, 256, 4, 1, False),
+                                            (7, 512, 16, 3, False), (3, 256, 256, 8, True)])
+def test_route_matches_oracle(B, d, E, k, renorm):
+    x = synth.tokens(B, d, 11)
+    wr = synth.router(d, E, 11)
+    idx, w, cnt = ses.route_topk(x.cuda(), wr.cuda(), k, renorm)
+    idx, w, cnt = _np16(idx), _np16(w), _np16(cnt)
+    idx_ref, w_ref, logits = orc.route_topk(_np16(x), _np16(wr), k, renorm)
+    S = np.abs(_np16(x).astype(np.float64)) @ np.abs(_np16(wr).astype(np.float64))
+    ok, n_band = parity.route_band(logits, S, idx, k)
+    assert ok and n_band == 0
+    # weights: the oracle's softmax at the kernel's experts
+    for b in range(B):
+        l = logits[b, idx[b]] if renorm else logits[b]
+        p = np.exp(l - l.max())
+        p /= p.sum()
+        exp = p if renorm else p[idx[b]]
+        np.testing.assert_allclose(w[b], exp, rtol=0, atol=2e-6)
+    assert np.array_equal(cnt, np.bincount(idx.ravel(), minlength=E))
+
+
+def test_route_exact_ties():
+    """Small integers make exact ties; fp32 sums of them are exact, so the kernel must
+    apply the same tie-break (lower index first) as the oracle, with no band."""
+    rng = np.random.default_rng(5)
+    for E, k in [(8, 2), (16, 6), (64, 6), (12, 3)]:
+        B, d = 16, 256
+        x = rng.integers(-2, 3, size=(B, d)).astype(np.float16)
+        wr = rng.integers(-1, 2, size=(d, E)).astype(np.float16)
+        idx, _, _ = ses.route_topk(torch.from_numpy(x).cuda(), torch.from_numpy(wr).cuda(), k, True)
+        idx_ref, _, _ = orc.route_topk(x, wr, k, True)
+        assert np.array_equal(_np16(idx), idx_ref)
+
+
+# ---------------------------------------------------------------------------
+# one expert
+# ---------------------------------------------------------------------------
+
+class OracleExpert:
+    def __init__(self, w_up, gate_t, down):
+        self.q, self.s, self.z = orc.quantize_int2(_np16(w_up))
+        self.w_up_deq = orc.dequantize_int2(self.q, self.s, self.z)
+        self.w_gate = _np16(gate_t).T
+        self.w_down = _np16(down)
+
+    def thr(self, xcal, pct):
+        return np.float32(orc.quantile_threshold(orc.expert_up(xcal, self.w_up_deq), pct))
+
+
+@pytest.mark.parametrize("d,f,n", [(256, 512, 1), (256, 512, 4), (256, 512, 9), (768, 208, 3),
+                                   (768, 208, 17), (2048, 1408, 8), (512, 4096, 2)])
+@pytest.mark.parametrize("pct", [0, 50, 90, 101])
+def test_expert_matches_oracle(d, f, n, pct):
+    E, e = 3, 1
+    de = synth.experts(E, d, f, 21)
+    x = synth.tokens(n, d, 21)
+    ox = OracleExpert(de.w_up[e], de.gate_t[e], de.down[e])
+    xcal = _np16(synth.calibration_tokens(64, d, 21))
+    t = np.float32(math.inf) if pct == 101 else ox.thr(xcal, pct)
+    thr = torch.full((E,), float(t), dtype=torch.float32)
+    ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(), thr.cuda())
+    y, dbg = ses.expert_sparse_swiglu(x.cuda(), ex, e, debug=True)
+    y = _np16(y)
+    v_gpu = _np16(dbg["v"])[:, 0]
+    m_gpu = parity.unpack_mask(_np16(dbg["mask"])[:, 0], f)
+    xs = _np16(x)
+    v_ref = orc.expert_up(xs, ox.w_up_deq)
+    S = parity.up_magnitude(xs, ox.q, ox.s, ox.z)
+    assert parity.check_v(v_gpu, v_ref, S) <= parity.TAU
+    bad, n_band = parity.check_mask(m_gpu, v_ref, S, float(t))
+    assert bad == 0
+    y_ref, _, _ = orc.sparse_swiglu_expert(xs, ox.w_gate, ox.w_up_deq, ox.w_down, float(t), mask=m_gpu)
+    if pct == 101:
+        assert not m_gpu.any()
+        assert np.all(y.view(np.uint16) == 0)  # exactly +0
+    max_abs, rel = parity.check_y(y, y_ref)
+    assert max_abs <= parity.Y_MAX_ABS
+    assert rel <= parity.Y_REL_L2 or np.linalg.norm(y_ref) == 0
+
+
+def test_expert_deterministic():
+    d, f, n = 768, 208, 9
+    de = synth.experts(2, d, f, 5)
+    thr = torch.tensor([0.3, 0.3], dtype=torch.float32).cuda()
+    ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(), thr)
+    x = synth.tokens(n, d, 5).cuda()
+    ws = ses.Workspace(ses.expert_workspace_bytes(n, d, f))
+    y1 = ses.expert_sparse_swiglu(x, ex, 0, ws=ws).clone()
+    y2 = ses.expert_sparse_swiglu(x, ex, 0, ws=ws)
+    assert torch.equal(y1, y2)
+    assert ws.status() == 0
+
+
+def test_expert_empty_batch():
+    d, f = 256, 512
+    de = synth.experts(1, d, f, 5)
+    ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(),
+                                torch.zeros(1, dtype=torch.float32).cuda())
+    y = ses.expert_sparse_swiglu(torch.empty((0, d), dtype=torch.float16, device="cuda"), ex, 0)
+    assert y.shape == (0, d)
+
+
+# ---------------------------------------------------------------------------
+# whole layer
+# ---------------------------------------------------------------------------
+
+def run_layer_case(d, f, E, k, B, shared, pcts, seed, ncal=64, renorm=True, rmsnorm=False,
+                   gen_device="cpu"):
+    dev = gen_device
+    de = synth.experts(E, d, f, seed, device=dev)
+    ds = synth.experts(shared, d, f, seed, device=dev, kind=1) if shared else None
+    wr = synth.router(d, E, seed, device=dev)
+    x = synth.tokens(B, d, seed, device=dev)
+    xs, wrs = _np16(x), _np16(wr)
+    xcal = _np16(synth.calibration_tokens(ncal, d, seed, device=dev))
+    idx_ref, _, logits = orc.route_topk(xs, wrs, k, renorm)
+    S_route = np.abs(xs.astype(np.float64)) @ np.abs(wrs.astype(np.float64))
+    cache = {}
+
+    def oracle_expert(kind, e):
+        key = (kind, e)
+        if key not in cache:
+            src = de if kind == "r" else ds
+            cache[key] = OracleExpert(src.w_up[e], src.gate_t[e], src.down[e])
+        return cache[key]
+
+    routed_used = sorted(set(idx_ref.ravel().tolist()))
+    ex_gpu = ses.Experts.from_dense(de.w_up.to("cuda"), de.gate_t.to("cuda"), de.down.to("cuda"),
+                                    torch.zeros(E, dtype=torch.float32, device="cuda"))
+    sh_gpu = None
+    if shared:
+        sh_gpu = ses.Experts.from_dense(ds.w_up.to("cuda"), ds.gate_t.to("cuda"), ds.down.to("cuda"),
+                                        torch.zeros(shared, dtype=torch.float32, device="cuda"))
+    layer = ses.Layer(wr.to("cuda"), ex_gpu, k, renorm, sh_gpu)
+    ws = ses.Workspace(ses.layer_workspace_bytes(layer, B))
+    results = []
+    for pct in pcts:
+        thr_r = np.zeros(E, np.float32)
+        for e in routed_used:
+            thr_r[e] = math.inf if pct == 101 else oracle_expert("r", e).thr(xcal, pct)
+        thr_s = np.zeros(shared, np.float32)
+        for s in range(shared):
+            thr_s[s] = math.inf if pct == 101 else oracle_expert("s", s).thr(xcal, pct)
+        ex_gpu.thr.copy_(torch.from_numpy(thr_r))
+        if shared:
+            sh_gpu.thr.copy_(torch.from_numpy(thr_s))
+        y, dbg = ses.layer_decode(x.to("cuda"), layer, rmsnorm=rmsnorm, ws=ws, debug=True)
+        assert ws.status() == 0
+        y = _np16(y)
+        idx_gpu = _np16(dbg["topk_idx"])
+        w_gpu = _np16(dbg["topk_w"])
+        ok, n_band_route = parity.route_band(logits, S_route, idx_gpu, k)
+        assert ok
+        # oracle weights at the kernel's experts
+        w_at = np.empty((B, k))
+        for b in range(B):
+            l = logits[b, idx_gpu[b]] if renorm else logits[b]
+            p = np.exp(l - l.max())
+            p /= p.sum()
+            w_at[b] = p if renorm else p[idx_gpu[b]]
+        np.testing.assert_allclose(w_gpu, w_at, rtol=0, atol=2e-6)
+        v_all = _np16(dbg["v"])
+        m_all = parity.unpack_mask(_np16(dbg["mask"]), f)
+        masks = {}
+        experts_o = [None] * E
+        n_band_mask = 0
+        worst_v = 0.0
+        for e in sorted(set(idx_gpu.ravel().tolist())):
+            rows, cols = np.nonzero(idx_gpu == e)
+            order = np.argsort(rows, kind="stable")
+            toks, slots = rows[order], cols[order]
+            ox = oracle_expert("r", e)
+            v_ref = orc.expert_up(xs[toks], ox.w_up_deq)
+            S = parity.up_magnitude(xs[toks], ox.q, ox.s, ox.z)
+            worst_v = max(worst_v, parity.check_v(v_all[toks, slots], v_ref, S))
+            bad, nb = parity.check_mask(m_all[toks, slots], v_ref, S, float(thr_r[e]))
+            assert bad == 0
+            n_band_mask += nb
+            masks[("r", e)] = m_all[toks, slots]
+            experts_o[e] = dict(w_gate=ox.w_gate, w_up_deq=ox.w_up_deq, w_down=ox.w_down,
+                                thr=float(thr_r[e]))
+        shared_o = []
+        for s in range(shared):
+            ox = oracle_expert("s", s)
+            v_ref = orc.expert_up(xs, ox.w_up_deq)
+            S = parity.up_magnitude(xs, ox.q, ox.s, ox.z)
+            worst_v = max(worst_v, parity.check_v(v_all[:, k + s], v_ref, S))
+            bad, nb = parity.check_mask(m_all[:, k + s], v_ref, S, float(thr_s[s]))
+            assert bad == 0
+            n_band_mask += nb
+            masks[("s", s)] = m_all[:, k + s]
+            shared_o.append(dict(w_gate=ox.w_gate, w_up_deq=ox.w_up_deq, w_down=ox.w_down,
+                                 thr=float(thr_s[s])))
+        assert worst_v <= parity.TAU
+        y_ref, _ = orc.moe_layer(xs, wrs, experts_o, k, renorm, shared=shared_o,
+                                 rmsnorm_out=rmsnorm, route=(idx_gpu, w_at), masks=masks)
+        max_abs, rel = parity.check_y(y, y_ref)
+        if pct == 101 and not shared:
+            assert np.all(y.view(np.uint16) == 0)
+        assert max_abs <= parity.Y_MAX_ABS, (pct, max_abs)
+        assert rel <= parity.Y_REL_L2 or np.linalg.norm(y_ref) == 0, (pct, rel)
+        kept = m_all[:, :k].mean() if B else 0.0
+        results.append(dict(pct=pct, max_abs=max_abs, rel=rel, band_mask=n_band_mask,
+                            band_route=n_band_route, worst_v=worst_v, kept=float(kept)))
+    return results
+
+
+def test_layer_tiny():
+    """d=256, f=512, E=8, top-2, 4 tokens; thresholds from 256 calibration tokens."""
+    run_layer_case(256, 512, 8, 2, 4, 0, [0, 50, 90, 101], seed=0, ncal=256)
+
+
+def test_layer_tiny_rmsnorm_and_full_softmax():
+    run_layer_case(256, 512, 8, 2, 4, 0, [50], seed=1, ncal=256, renorm=False, rmsnorm=True)
+
+
+def test_layer_ragged_with_shared():
+    """d=768 (a partial 512-superblock), f=208 (13 column tiles, mask words ragged),
+    9 tokens (a group of 8 and a group of 1), one shared expert."""
+    run_layer_case(768, 208, 4, 2, 9, 1, [0, 50, 101], seed=2)
+
+
+def test_layer_deepseek_v2_lite_shape():
+    """d=2048, f=1408, 64 routed experts top-6, 2 shared experts."""
+    run_layer_case(2048, 1408, 64, 6, 8, 2, [0, 50, 90], seed=3, gen_device="cuda")
+
+
+def test_layer_mixtral_8x7b_b1():
+    """d=4096, f=14336, 8 experts top-2, one decode token, 0/50/70/90% thresholds."""
+    run_layer_case(4096, 14336, 8, 2, 1, 0, [0, 50, 70, 90], seed=4, gen_device="cuda")
+
+
+def test_layer_mixtral_8x7b_batch8():
+    run_layer_case(4096, 14336, 8, 2, 8, 0, [70], seed=5, gen_device="cuda")
+
+
+def test_layer_mixtral_8x22b_shape_b2():
+    """d=6144, f=16384 (groups capped at 4 tokens for this d), RMSNorm output."""
+    run_layer_case(6144, 16384, 8, 2, 2, 0, [70], seed=6, gen_device="cuda", rmsnorm=True)
+
+
+def test_layer_deterministic_and_status():
+    d, f, E, k, B = 768, 208, 4, 2, 9
+    de = synth.experts(E, d, f, 9)
+    ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(),
+                                torch.full((E,), 0.2, dtype=torch.float32).cuda())
+    layer = ses.Layer(synth.router(d, E, 9).cuda(), ex, k)
+    x = synth.tokens(B, d, 9).cuda()
+    ws = ses.Workspace(ses.layer_workspace_bytes(layer, B))
+    y1 = ses.layer_decode(x, layer, ws=ws).clone()
+    y2 = ses.layer_decode(x, layer, ws=ws)
+    assert torch.equal(y1, y2)
+    assert ws.status() == 0
