@@ -93,6 +93,10 @@ typedef struct {
   float* topk_w;       /* [B][k] combine weights */
   uint32_t* mask;      /* [B][S][ceil(f/32)] bit i%32 of word i/32 = (|v_i| > t) */
   float* v;            /* [B][S][f] fp32 v = x W~^up (step 1 of Algorithm 1) */
+  void** events;       /* 5 cudaEvent_t (as void*), recorded on `stream` before the router
+                          (or the single-expert set-up), before the up-projection kernel,
+                          before the gather kernel, before the combine kernel and after it;
+                          for per-kernel timing.  Recording them serialises the kernels. */
 } moe_debug_t;
 
 /* ---------------- INT2 up projection ---------------- */

@@ -43,7 +43,8 @@ class _Layer(ctypes.Structure):
 
 class _Debug(ctypes.Structure):
     _fields_ = [("topk_idx", ctypes.c_void_p), ("topk_w", ctypes.c_void_p),
-                ("mask", ctypes.c_void_p), ("v", ctypes.c_void_p)]
+                ("mask", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("events", ctypes.POINTER(ctypes.c_void_p))]
 
 
 _LIB = None
@@ -244,8 +245,25 @@ def _debug(B: int, S: int, f: int, k: int, device, with_route: bool):
     if with_route:
         t["topk_idx"] = torch.zeros((B, k), dtype=torch.int32, device=device)
         t["topk_w"] = torch.zeros((B, k), dtype=torch.float32, device=device)
-    dbg = _Debug(_ptr(t.get("topk_idx")), _ptr(t.get("topk_w")), _ptr(t["mask"]), _ptr(t["v"]))
+    dbg = _Debug(_ptr(t.get("topk_idx")), _ptr(t.get("topk_w")), _ptr(t["mask"]), _ptr(t["v"]), None)
     return dbg, t
+
+
+def _with_events(dbg, events):
+    """Attach 5 timing events (torch.cuda.Event(enable_timing=True)) to a debug block."""
+    if events is None:
+        return dbg
+    if len(events) != 5:
+        raise ValueError("need 5 events")
+    for ev in events:
+        if ev.cuda_event == 0:  # torch creates the event on its first record
+            ev.record()
+    arr = (ctypes.c_void_p * 5)(*[ev.cuda_event for ev in events])
+    if dbg is None:
+        dbg = _Debug(None, None, None, None, None)
+    dbg.events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+    dbg._keep = arr
+    return dbg
 
 
 def route_workspace_bytes(B: int, E: int, k: int) -> int:
@@ -276,18 +294,20 @@ def expert_workspace_bytes(n: int, d: int, f: int) -> int:
 
 def expert_sparse_swiglu(x: torch.Tensor, experts: Experts, expert: int,
                          ws: Optional[Workspace] = None, debug: bool = False,
-                         out: Optional[torch.Tensor] = None):
+                         out: Optional[torch.Tensor] = None, events=None,
+                         c_experts: Optional[_Experts] = None):
     """One sparse SwiGLU expert on every row of x (fp16 [n, d]) -> y fp16 [n, d]
     (and, with debug, a dict with mask int32 [n, 1, ceil(f/32)] and v fp32 [n, 1, f])."""
     _need(x, torch.float16, "x")
     n, d = x.shape
-    ex = experts.c_struct()
+    ex = c_experts if c_experts is not None else experts.c_struct()
     if ws is None:
         ws = Workspace(expert_workspace_bytes(n, d, experts.f), x.device)
     y = out if out is not None else torch.empty_like(x)
     dbg, dt = (None, None)
     if debug:
         dbg, dt = _debug(n, 1, experts.f, 1, x.device, False)
+    dbg = _with_events(dbg, events)
     _check("moe_expert_sparse_swiglu",
            lib().moe_expert_sparse_swiglu(_ptr(x), n, ctypes.byref(ex), expert, _ptr(y),
                                           ctypes.byref(dbg) if dbg is not None else None,
@@ -302,7 +322,8 @@ def layer_workspace_bytes(layer: Layer, B: int) -> int:
 
 def layer_decode(x: torch.Tensor, layer: Layer, rmsnorm: bool = False,
                  ws: Optional[Workspace] = None, debug: bool = False,
-                 out: Optional[torch.Tensor] = None, c_layer: Optional[_Layer] = None):
+                 out: Optional[torch.Tensor] = None, c_layer: Optional[_Layer] = None,
+                 events=None):
     """One MoE decode layer on x fp16 [B, d] -> y fp16 [B, d] (and the debug dict)."""
     _need(x, torch.float16, "x")
     B, d = x.shape
@@ -313,6 +334,7 @@ def layer_decode(x: torch.Tensor, layer: Layer, rmsnorm: bool = False,
     dbg, dt = (None, None)
     if debug:
         dbg, dt = _debug(B, layer.n_slots, layer.routed.f, layer.k, x.device, True)
+    dbg = _with_events(dbg, events)
     _check("moe_layer_decode",
            lib().moe_layer_decode(_ptr(x), B, ctypes.byref(c), _ptr(y), 1 if rmsnorm else 0,
                                   ctypes.byref(dbg) if dbg is not None else None,

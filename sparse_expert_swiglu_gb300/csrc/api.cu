@@ -144,6 +144,12 @@ moe_status_t plan(const DeviceInfo& di, const WsLayout& L, int d, int f, int max
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Optional per-kernel timing events of moe_debug_t (index 0..4).
+cudaError_t record(const moe_debug_t* dbg, int i, cudaStream_t st) {
+  if (!dbg || !dbg->events || !dbg->events[i]) return cudaSuccess;
+  return cudaEventRecord((cudaEvent_t)dbg->events[i], st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -244,9 +250,13 @@ static moe_status_t run_experts(const uint16_t* x, int B, const moe_experts_t* r
   p.stages = pl.stages;
   p.list_cap = L.list_cap;
   p.G_max = L.G_max;
-  cudaError_t e = launch_up(p, pl.up_grid, st, true);
+  cudaError_t e = record(dbg, 1, st);
+  if (e == cudaSuccess) e = launch_up(p, pl.up_grid, st, true);
+  if (e == cudaSuccess) e = record(dbg, 2, st);
   if (e == cudaSuccess) e = launch_gather(p, pl.nt, st, true);
+  if (e == cudaSuccess) e = record(dbg, 3, st);
   if (e == cudaSuccess) e = launch_combine(p, st, true);
+  if (e == cudaSuccess) e = record(dbg, 4, st);
   return cuda_status(e);
 }
 
@@ -278,6 +288,7 @@ moe_status_t moe_expert_sparse_swiglu(const uint16_t* x, int32_t n, const moe_ex
   const WsLayout L = ws_layout(n, n, (n + gcap - 1) / gcap, experts->d, experts->f, di.sms);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = (cudaStream_t)stream;
+  if (record(dbg, 0, st) != cudaSuccess) return MOE_ERR_CUDA;
   cudaError_t e = launch_expert_prep(expert, n, gcap, at<GroupDesc>(ws, L.groups),
                                      at<int>(ws, L.tok_groups), at<int>(ws, L.group_total),
                                      at<Ctrl>(ws, L.ctrl), st, true);
@@ -352,6 +363,7 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
   rp.tok_groups = at<int>(ws, L.tok_groups);
   rp.group_total = at<int>(ws, L.group_total);
   rp.G_max = L.G_max;
+  if (record(dbg, 0, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_route(rp, st, true) != cudaSuccess) return MOE_ERR_CUDA;
   return run_experts(x, B, &layer->routed, &layer->shared, k + layer->shared.E, y,
                      rmsnorm_out ? 1 : 0, dbg, ws, L, di, B < rp.gcap ? B : rp.gcap, st);
