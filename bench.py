@@ -190,11 +190,11 @@ def calibrate(layers, dev):
         thr = {p: torch.zeros(W["E"], dtype=torch.float32, device=dev) for p in SPARSITIES}
         for e in range(W["E"]):
             _, dbg = ses.expert_sparse_swiglu(xcal, ex, e, ws=ws, debug=True)
-            a = dbg["v"].abs().flatten()
+            a = torch.sort(dbg["v"].abs().flatten()).values
             n = a.numel()
             for p in SPARSITIES:
                 if p > 0:
-                    thr[p][e] = torch.kthvalue(a, (p * n + 99) // 100).values
+                    thr[p][e] = a[(p * n + 99) // 100 - 1]
         for p in SPARSITIES:
             table[p].append(thr[p])
     return table
@@ -296,7 +296,7 @@ def per_kernel_times(prof_graphs, events_list, stream, steps):
 def source_hash():
     import hashlib
     h = hashlib.sha256()
-    for fn in ["expert.cu", "common.cuh", "params.cuh"]:
+    for fn in ["up.cu", "gather.cu", "combine.cu", "common.cuh", "params.cuh"]:
         with open(os.path.join(ROOT, "sparse_expert_swiglu_gb300", "csrc", fn), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -429,6 +429,8 @@ def run_ours(args, world, rank, local):
                           frac_of_measured_hbm=mean_bytes / (us * 1e-6) / 1e9 / peak,
                           bytes_per_step=mean_bytes,
                           kept_fraction=float(np.mean([b["kept_frac"] for b in byts]))))
+        if rank == 0:
+            print(f"sweep {sweep[-1]}", file=sys.stderr, flush=True)
 
     pct = args.sparsity
     set_thresholds(layers, table, pct)

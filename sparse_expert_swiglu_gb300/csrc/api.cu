@@ -122,22 +122,20 @@ struct Plan {
 
 // Grid of the up kernel, depth of the gather pipeline.
 moe_status_t plan(const DeviceInfo& di, const WsLayout& L, int d, int f, int max_tok, Plan& pl) {
-  const size_t up_smem = up_smem_bytes(d);
+  const size_t up_smem = up_smem_bytes(d, max_tok);
   if (up_smem + 1024 > (size_t)di.smem_optin) return MOE_ERR_UNSUPPORTED_SHAPE;
-  int occ = (int)(di.smem_per_sm / (up_smem + 1024));
-  occ = occ < 1 ? 1 : (occ > 2 ? 2 : occ);
+  const int occ = up_blocks_per_sm(d, max_tok);
+  if (occ < 1) return MOE_ERR_UNSUPPORTED_SHAPE;
   pl.up_grid = di.sms * occ;
   pl.nt = max_tok <= 1 ? 1 : max_tok <= 2 ? 2 : max_tok <= 4 ? 4 : 8;
-  const size_t fixed = gather_smem_bytes(d, 0, pl.nt, L.list_cap) + 2048;
+  const size_t fixed = gather_smem_bytes(d, 0, pl.nt, L.list_cap, L.G_max) + 2048;
   const size_t stage = (size_t)4 * d + 32 + 16;
   if (fixed + 2 * stage > (size_t)di.smem_optin) return MOE_ERR_UNSUPPORTED_SHAPE;
   int S = (int)((di.smem_optin - fixed) / stage);
   S = S > 16 ? 16 : S;
-  // the gather prologue borrows the stage buffers as scratch for its scans
-  const size_t scratch = sizeof(int) * ((size_t)2 * L.G_max + f / kMTile + 4);
-  while ((size_t)S * (4 * d + 32) < scratch && S < 64) ++S;
-  if (gather_smem_bytes(d, S, pl.nt, L.list_cap) > (size_t)di.smem_optin)
-    return MOE_ERR_UNSUPPORTED_SHAPE;
+  // the gather prologue borrows the stage buffers for the scan of one group's tile counts
+  const size_t scratch = sizeof(int) * ((size_t)f / kMTile + 2);
+  if ((size_t)S * (4 * d + 32) < scratch) return MOE_ERR_UNSUPPORTED_SHAPE;
   pl.stages = S;
   return MOE_OK;
 }
@@ -147,7 +145,8 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 // Optional per-kernel timing events of moe_debug_t (index 0..4).
 cudaError_t record(const moe_debug_t* dbg, int i, cudaStream_t st) {
   if (!dbg || !dbg->events || !dbg->events[i]) return cudaSuccess;
-  return cudaEventRecord((cudaEvent_t)dbg->events[i], st);
+  // External: inside stream capture this becomes an event-record node of the graph.
+  return cudaEventRecordWithFlags((cudaEvent_t)dbg->events[i], st, cudaEventRecordExternal);
 }
 
 }  // namespace
@@ -250,6 +249,7 @@ static moe_status_t run_experts(const uint16_t* x, int B, const moe_experts_t* r
   p.stages = pl.stages;
   p.list_cap = L.list_cap;
   p.G_max = L.G_max;
+  p.max_tok = max_tok;
   cudaError_t e = record(dbg, 1, st);
   if (e == cudaSuccess) e = launch_up(p, pl.up_grid, st, true);
   if (e == cudaSuccess) e = record(dbg, 2, st);

@@ -48,7 +48,18 @@ struct ExpertParams {
   int stages;               // gather pipeline depth
   int list_cap;             // gather item-list capacity per CTA window
   int G_max;
+  int max_tok;              // largest group of this call (sizes the up kernel's x buffer)
 };
+
+__device__ __forceinline__ const ExpertSet& expert_set(const ExpertParams& p, int expert,
+                                                       int& local) {
+  if (expert < p.routed.E) {
+    local = expert;
+    return p.routed;
+  }
+  local = expert - p.routed.E;
+  return p.shared;
+}
 
 // pack.cu
 cudaError_t launch_pack(const __half* w, int d, int f, uint8_t* packed, cudaStream_t st);
@@ -58,11 +69,16 @@ cudaError_t launch_unpack(const uint8_t* packed, int d, int f, uint8_t* q, __hal
 cudaError_t launch_route(const RouteParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_expert_prep(int expert, int n, int gcap, GroupDesc* groups, int* tok_groups,
                                int* group_total, Ctrl* ctrl, cudaStream_t st, bool pdl);
-// expert.cu
-size_t up_smem_bytes(int d);
-size_t gather_smem_bytes(int d, int stages, int nt, int list_cap);
+// up.cu
+size_t up_smem_bytes(int d, int max_tok);
+int up_threads(int d);
+int up_blocks_per_sm(int d, int max_tok);
 cudaError_t launch_up(const ExpertParams& p, int grid, cudaStream_t st, bool pdl);
+// gather.cu
+size_t gather_smem_bytes(int d, int stages, int nt, int list_cap, int g_max);
 cudaError_t launch_gather(const ExpertParams& p, int nt, cudaStream_t st, bool pdl);
+// combine.cu
+size_t combine_smem_bytes(const ExpertParams& p);
 cudaError_t launch_combine(const ExpertParams& p, cudaStream_t st, bool pdl);
 
 }  // namespace sesg

@@ -14,11 +14,13 @@ namespace sesg {
 
 constexpr int kRouteThreads = 256;
 
-// Logits of one token: each thread owns EV consecutive experts and a strided set of rows.
+// Logits of one token: each thread owns EV consecutive experts and a strided set of
+// rows; the rows are fetched RU at a time so that their loads are in flight together.
 template <int EV>
 __device__ void router_logits(const RouteParams& p, int b, float* logits, float* red) {
+  constexpr int RU = 8;
   const int tid = threadIdx.x;
-  const int nchunk = p.E / EV;          // expert chunks
+  const int nchunk = p.E / EV;             // expert chunks
   const int nrs = kRouteThreads / nchunk;  // row slots
   const int ec = tid % nchunk, rs = tid / nchunk;
   float acc[EV];
@@ -26,33 +28,54 @@ __device__ void router_logits(const RouteParams& p, int b, float* logits, float*
   for (int i = 0; i < EV; ++i) acc[i] = 0.f;
   if (rs < nrs) {
     const __half* xb = p.x + (size_t)b * p.d;
-    for (int r = rs; r < p.d; r += nrs) {
-      const float xv = __half2float(xb[r]);
-      const __half* wrow = p.w_router + (size_t)r * p.E + ec * EV;
-      if constexpr (EV == 8) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(wrow);
-        const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+    for (int r0 = rs; r0 < p.d; r0 += nrs * RU) {
+      float xv[RU];
+      uint4 wv[RU];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 wf = __half22float2(h2[i]);
-          acc[2 * i] = fmaf(xv, wf.x, acc[2 * i]);
-          acc[2 * i + 1] = fmaf(xv, wf.y, acc[2 * i + 1]);
+      for (int u = 0; u < RU; ++u) {
+        const int r = r0 + u * nrs;
+        xv[u] = 0.f;
+        wv[u] = make_uint4(0, 0, 0, 0);
+        if (r < p.d) {
+          xv[u] = __half2float(xb[r]);
+          const __half* wrow = p.w_router + (size_t)r * p.E + ec * EV;
+          if constexpr (EV == 8) wv[u] = *reinterpret_cast<const uint4*>(wrow);
+          else wv[u].x = (uint32_t)__half_as_ushort(wrow[0]);
         }
-      } else {
+      }
 #pragma unroll
-        for (int i = 0; i < EV; ++i) acc[i] = fmaf(xv, __half2float(wrow[i]), acc[i]);
+      for (int u = 0; u < RU; ++u) {
+        if constexpr (EV == 8) {
+          const __half2* h2 = reinterpret_cast<const __half2*>(&wv[u]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 wf = __half22float2(h2[i]);
+            acc[2 * i] = fmaf(xv[u], wf.x, acc[2 * i]);
+            acc[2 * i + 1] = fmaf(xv[u], wf.y, acc[2 * i + 1]);
+          }
+        } else {
+          acc[0] = fmaf(xv[u], __half2float(__ushort_as_half((unsigned short)wv[u].x)), acc[0]);
+        }
       }
     }
   }
-  // red[rs][e], then a fixed-order sum over row slots
+  // red[rs][e], then a two-level fixed-order sum over the row slots
   if (rs < nrs) {
 #pragma unroll
     for (int i = 0; i < EV; ++i) red[rs * p.E + ec * EV + i] = acc[i];
   }
   __syncthreads();
+  const int Q = kRouteThreads / p.E;  // >= 1
+  float part = 0.f;
+  const int e0 = tid % p.E, q0 = tid / p.E;
+  if (q0 < Q)
+    for (int r = q0; r < nrs; r += Q) part += red[r * p.E + e0];
+  __syncthreads();
+  if (q0 < Q) red[q0 * p.E + e0] = part;
+  __syncthreads();
   for (int e = tid; e < p.E; e += kRouteThreads) {
     float s = 0.f;
-    for (int r = 0; r < nrs; ++r) s += red[r * p.E + e];
+    for (int q = 0; q < Q; ++q) s += red[q * p.E + e];
     logits[e] = s;
   }
   __syncthreads();
@@ -213,15 +236,20 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   __shared__ int s_last;
   griddep_wait();
   griddep_launch_dependents();
-  const int b = blockIdx.x;
-  router_logits<EV>(p, b, s_logits, s_red);
-  if (threadIdx.x < 32) router_topk(p, b, s_logits);
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&p.ctrl->route_done, 1) == (int)gridDim.x - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+    router_logits<EV>(p, b, s_logits, s_red);
+    if (threadIdx.x < 32) router_topk(p, b, s_logits);
+    __syncthreads();
+  }
+  if (gridDim.x > 1) {
+    // the last CTA to finish groups the pairs of every token
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(&p.ctrl->route_done, 1) == (int)gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+  }
   router_group(p);
   if (threadIdx.x == 0) p.ctrl->route_done = 0;
 }
@@ -253,7 +281,7 @@ size_t route_group_smem(int B, int k) { return (size_t)2 * B * k * sizeof(int); 
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.B);
+  cfg.gridDim = dim3(p.B <= 4 ? 1 : p.B);  // few tokens: one CTA, no cross-CTA hand-off
   cfg.blockDim = dim3(kRouteThreads);
   cfg.dynamicSmemBytes = route_group_smem(p.B, p.k);
   cfg.stream = st;

@@ -1,0 +1,456 @@
+// Steps 1 and 2 of Algorithm 1 "Efficient Sparse Kernel" of "FloE: On-the-Fly MoE
+// Inference on Memory-constrained GPU" (sec. 三 "系统协同优化"): v = x W^up from the INT2
+// codes (the intra-expert predictor of sec. "双稀疏预测器" reuses exactly this product),
+// then mask = |v| > t, with the kept columns of every 16-column tile compacted into
+// an item list for the gather kernel.
+//
+// Work unit: (group, M-tile) = one expert, up to 8 of its tokens, 16 output columns.
+// Each CTA takes a contiguous range of units.  One producer thread streams the
+// units' packed strips (contiguous in memory) into a 4-stage shared-memory ring
+// with 1-D bulk copies (TMA).  Consumer warp w owns superblock sb = w % nsb of
+// M-tile slot w / nsb, keeps the B fragments (the group's tokens) of its superblock
+// in registers, and runs the INT2 dot products on the tensor cores (mma.sync
+// m16n8k16, fp16 in, fp32 accumulate).  Partial v of the superblocks are summed in
+// a fixed order by one warp per M-tile, which also applies the threshold.
+#include "params.cuh"
+
+namespace sesg {
+
+constexpr int kUpStages = 4;
+
+struct UpLayout {
+  int nsb, mpar, nwc;
+  size_t stage_bytes, off_full, off_empty, off_stage, off_x, off_xg, off_vpart, off_vbuf, total;
+};
+
+__host__ __device__ inline UpLayout up_layout(int d, int max_tok) {
+  UpLayout L;
+  L.nsb = n_superblocks(d);
+  if (L.nsb <= 8) {
+    L.mpar = 8 / L.nsb;
+    L.nwc = L.mpar * L.nsb;
+  } else {
+    L.mpar = 1;
+    L.nwc = L.nsb;
+  }
+  L.stage_bytes = (size_t)L.mpar * L.nsb * kBlkBytes;
+  size_t o = 0;
+  L.off_full = o;
+  o += 8 * kUpStages;
+  L.off_empty = o;
+  o += 8 * kUpStages;
+  o = (o + 127) & ~(size_t)127;
+  L.off_stage = o;
+  o += L.stage_bytes * kUpStages;
+  L.off_x = o;
+  o += (size_t)max_tok * d * 2;
+  o = (o + 15) & ~(size_t)15;
+  L.off_xg = o;
+  o += (size_t)kMaxTok * (d / kGroup) * 4;
+  o = (o + 15) & ~(size_t)15;
+  L.off_vpart = o;
+  o += (size_t)2 * L.nwc * 32 * 16;
+  L.off_vbuf = o;
+  o += (size_t)L.mpar * 16 * kMaxTok * 4;
+  L.total = o;
+  return L;
+}
+
+template <int GI>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t wsh) {
+  // Two 2-bit codes of group slot GI as an fp16x2 of subnormals q * 4^pos * 2^-24
+  // (exact); the power of two is removed after the mma.
+  if constexpr (GI < 5) return w & (0x00030003u << (2 * GI));
+  else return wsh & (0x00030003u << (2 * (GI - 5)));
+}
+
+__device__ __forceinline__ float pos_scale(int gi) {
+  const int pos = gi < 5 ? gi : gi - 5;
+  return __int_as_float((127 + 24 - 2 * pos) << 23);  // 2^(24 - 2 pos)
+}
+
+// One warp: partial v of its superblock of one M-tile.
+//
+// Tensor-core mapping: M = 16 output columns, K = 16 inputs, N = 8 slots.  A slot
+// is a (token, group class) pair: with T tokens (padded to a power of two) there
+// are G = 8/T classes, and a k-step of quantiser group gi only feeds the slots of
+// class gi % G, whose B column carries that token's x; the other B columns are
+// zero.  One accumulator tile therefore collects G quantiser groups side by side,
+// and the per-group correction v += s * (A_g - z * X_g) (X_g = sum of x over the
+// group) is applied once per G groups.  Two accumulator chains (even / odd k-step)
+// halve the mma dependency chain.
+template <int T>
+__device__ __forceinline__ void up_superblock(const uint8_t* __restrict__ blk,
+                                              const uint32_t (&bf)[64],
+                                              const float* __restrict__ xg, int sb, int ng,
+                                              int ngrp, float (&vacc)[2][2]) {
+  constexpr int G = 8 / T;
+  const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
+  uint4 w[4], wsh[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    w[q] = reinterpret_cast<const uint4*>(blk)[q * 32 + lane];
+    wsh[q] = make_uint4(w[q].x >> 10, w[q].y >> 10, w[q].z >> 10, w[q].w >> 10);
+  }
+  const int gi_lane = (G >= 2) ? (2 * c) % G : 0;
+  const uint8_t* szt = blk + kBlkCodeBytes;
+#pragma unroll
+  for (int ph = 0; ph < T; ++ph) {
+    float D0[4] = {0.f, 0.f, 0.f, 0.f}, D1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int gam = 0; gam < G; ++gam) {
+      const int gi = ph * G + gam;
+      if (gi < ng) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          uint32_t a[4];
+#define SESG_CASE(GIV)                          \
+  case GIV:                                     \
+    a[0] = code_pair<GIV>(w[t].x, wsh[t].x);    \
+    a[1] = code_pair<GIV>(w[t].y, wsh[t].y);    \
+    a[2] = code_pair<GIV>(w[t].z, wsh[t].z);    \
+    a[3] = code_pair<GIV>(w[t].w, wsh[t].w);    \
+    break;
+          switch (gi) {
+            SESG_CASE(0) SESG_CASE(1) SESG_CASE(2) SESG_CASE(3)
+            SESG_CASE(4) SESG_CASE(5) SESG_CASE(6) default: SESG_CASE(7)
+          }
+#undef SESG_CASE
+          const int ks = gi * 4 + t;
+          if (t & 1) mma_16816(D1, a, bf[2 * ks], bf[2 * ks + 1]);
+          else mma_16816(D0, a, bf[2 * ks], bf[2 * ks + 1]);
+        }
+      }
+    }
+    // fold this phase's G groups into v
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int gi = (G >= 2) ? ph * G + gi_lane + s : ph;
+      const int tau = (G >= 2) ? (2 * c) / G : 2 * c + s;
+      if (gi < ng) {
+        const float cs = pos_scale(gi);
+        const float X = xg[tau * ngrp + sb * 8 + gi];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const __half2 h = *reinterpret_cast<const __half2*>(szt + ((gl + 8 * r) * 8 + gi) * 4);
+          const float sf = __low2float(h), zf = __high2float(h);
+          const float acc = D0[2 * r + s] + D1[2 * r + s];
+          vacc[r][s] = fmaf(sf, fmaf(-zf, X, acc * cs), vacc[r][s]);
+        }
+      }
+    }
+  }
+}
+
+// One warp, after the superblock partials are summed: per-token v of the M-tile's
+// 16 columns, step 2 (mask = |v| > t, union over the group's tokens), compaction of
+// the kept columns by ballot, and the optional debug outputs.
+template <int T>
+__device__ __forceinline__ void up_finalize(const ExpertParams& p, const GroupDesc& gd, long long u,
+                                            int mt, float thr, const float (&vacc)[2][2],
+                                            float* __restrict__ vbuf) {
+  constexpr int G = 8 / T;
+  const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
+  if constexpr (G >= 2) {
+    float v0 = vacc[0][0] + vacc[0][1];
+    float v1 = vacc[1][0] + vacc[1][1];
+    if constexpr (G >= 4) {
+      v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+      v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+    }
+    if constexpr (G == 8) {
+      v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+      v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+    }
+    const int tau = (2 * c) / G;
+    if ((c % (G / 2)) == 0) {
+      vbuf[gl * 8 + tau] = v0;
+      vbuf[(gl + 8) * 8 + tau] = v1;
+    }
+  } else {
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      vbuf[gl * 8 + 2 * c + s] = vacc[0][s];
+      vbuf[(gl + 8) * 8 + 2 * c + s] = vacc[1][s];
+    }
+  }
+  __syncwarp();
+  float vv[kMaxTok];
+  uint32_t mbits = 0;
+#pragma unroll
+  for (int t = 0; t < kMaxTok; ++t) {
+    vv[t] = 0.f;
+    if (t < gd.n_tok && lane < 16) {
+      vv[t] = vbuf[lane * 8 + t];
+      if (fabsf(vv[t]) > thr) mbits |= 1u << t;
+    }
+  }
+  __syncwarp();
+  const bool kept = mbits != 0;
+  const uint32_t bal = __ballot_sync(0xffffffffu, kept);
+  if (kept) {
+    const int rank = __popc(bal & ((1u << lane) - 1u));
+    const long long slot = u * 16 + rank;
+    p.item_col[slot] = mt * kMTile + lane;
+    float hv[kMaxTok];
+#pragma unroll
+    for (int t = 0; t < kMaxTok; ++t) hv[t] = ((mbits >> t) & 1u) ? vv[t] : 0.f;
+    float4* dst = reinterpret_cast<float4*>(p.item_v + slot * 8);
+    dst[0] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+    dst[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
+  }
+  if (lane == 0) {
+    p.unit_cnt[u] = (uint8_t)__popc(bal);
+    const int g = (int)(u / (p.f / kMTile));
+    if (bal) atomicAdd(&p.group_total[g], __popc(bal));
+  }
+  if (p.dbg_v || p.dbg_mask) {
+#pragma unroll
+    for (int t = 0; t < kMaxTok; ++t) {
+      if (t < gd.n_tok) {
+        const size_t row = (size_t)gd.tok[t] * p.n_slots + gd.slot[t];
+        if (p.dbg_v && lane < 16) p.dbg_v[row * p.f + mt * kMTile + lane] = vv[t];
+        const uint32_t mb = __ballot_sync(0xffffffffu, (mbits >> t) & 1u) & 0xffffu;
+        if (p.dbg_mask && lane == 0)
+          reinterpret_cast<uint16_t*>(p.dbg_mask)[row * (size_t)(2 * ((p.f + 31) / 32)) + mt] =
+              (uint16_t)mb;
+      }
+    }
+  }
+}
+
+// B fragments of superblock sb for the current group: k-step ks of quantiser group
+// gi = ks / 4 feeds slot gl (token gl / G) only when gl % G == gi % G.
+__device__ __forceinline__ void build_bfrag_regs(const __half* __restrict__ xs, int d, int n_tok,
+                                                 int T, int sb, uint32_t (&bf)[64]) {
+  const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
+  const int G = 8 / T, tau = gl / G;
+#pragma unroll
+  for (int ks = 0; ks < 32; ++ks) {
+    const int gi = ks >> 2;
+    const int k = sb * kSuper + 16 * ks + 2 * c;
+    uint32_t b0 = 0, b1 = 0;
+    if ((gl % G) == (gi % G) && tau < n_tok && k < d) {
+      const __half* xr = xs + (size_t)tau * d + k;
+      b0 = *reinterpret_cast<const uint32_t*>(xr);
+      b1 = *reinterpret_cast<const uint32_t*>(xr + 8);
+    }
+    bf[2 * ks] = b0;
+    bf[2 * ks + 1] = b1;
+  }
+}
+
+__device__ __forceinline__ int barrier_or(int id, int nthreads, bool pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred pin, pout;\n\t"
+      "setp.ne.u32 pin, %1, 0;\n\t"
+      "barrier.red.or.pred pout, %2, %3, pin;\n\t"
+      "selp.u32 %0, 1, 0, pout;\n\t}"
+      : "=r"(r)
+      : "r"((unsigned)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r;
+}
+
+template <int MAXT>
+__global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int d = p.d;
+  const UpLayout L = up_layout(d, p.max_tok);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.off_empty);
+  uint8_t* stage = smem + L.off_stage;
+  __half* xs = reinterpret_cast<__half*>(smem + L.off_x);
+  float* xg = reinterpret_cast<float*>(smem + L.off_xg);
+  float4* vpart = reinterpret_cast<float4*>(smem + L.off_vpart);
+  float* vbuf = reinterpret_cast<float*>(smem + L.off_vbuf);
+  __shared__ GroupDesc s_gd;
+  __shared__ int s_abort, s_issued, s_consumed;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwc = L.nwc, nct = nwc * 32, nsb = L.nsb;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kUpStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nwc);
+    }
+    fence_barrier_init();
+    s_abort = 0;
+    s_issued = 0;
+    s_consumed = 0;
+  }
+  __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+  const int G = *reinterpret_cast<volatile int*>(&p.ctrl->G);
+  const int MT = p.f / kMTile;
+  const long long U = (long long)G * MT;
+  const long long u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
+  const int ngrp = d / kGroup;
+
+  if (warp == nwc) {
+    // ---- producer: one bulk copy per unit (its whole d-strip), one ring stage per step
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int j = 0, last_g = -1;
+      const uint8_t* base = nullptr;
+      for (long long us = u0; us < u1; ++j) {
+        const long long ue = min(min(us + L.mpar, u1), (us / MT + 1) * MT);
+        const int s = j % kUpStages;
+        if (j >= kUpStages && !mbar_wait(&empty[s], ((j / kUpStages) - 1) & 1)) {
+          set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+          break;
+        }
+        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
+        const int g = (int)(us / MT);
+        if (g != last_g) {
+          last_g = g;
+          int el;
+          const ExpertSet& es = expert_set(p, p.groups[g].expert, el);
+          base = es.up + (size_t)el * es.up_stride;
+        }
+        const uint32_t strip = (uint32_t)(nsb * kBlkBytes);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(ue - us) * strip);
+        for (long long u = us; u < ue; ++u)
+          bulk_g2s(stage + (size_t)s * L.stage_bytes + (size_t)(u - us) * strip,
+                   base + (size_t)(u - (long long)g * MT) * strip, strip, &full[s], pol);
+        s_issued = j + 1;
+        us = ue;
+      }
+    }
+  } else {
+    // ---- consumers
+    const int m_slot = warp / nsb, sb = warp % nsb;
+    const int ng = min(8, (d - sb * kSuper) / kGroup);
+    int cur_g = -1, T = 1;
+    float thr = 0.f;
+    uint32_t bf[64];
+    int j = 0;
+    for (long long us = u0; us < u1; ++j) {
+      const long long ue = min(min(us + L.mpar, u1), (us / MT + 1) * MT);
+      const int g = (int)(us / MT);
+      if (g != cur_g) {
+        named_barrier(1, nct);
+        if (threadIdx.x == 0) s_gd = p.groups[g];
+        named_barrier(1, nct);
+        const int n_tok = s_gd.n_tok;
+        for (int i = threadIdx.x; i < n_tok * (d / 8); i += nct) {
+          const int t = i / (d / 8), o = i % (d / 8);
+          reinterpret_cast<uint4*>(xs + (size_t)t * d)[o] =
+              __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)s_gd.tok[t] * d) + o);
+        }
+        named_barrier(1, nct);
+        for (int i = threadIdx.x; i < kMaxTok * ngrp; i += nct) {
+          const int t = i / ngrp, grp = i % ngrp;
+          float sum = 0.f;
+          if (t < n_tok) {
+            const __half2* xr = reinterpret_cast<const __half2*>(xs + (size_t)t * d + grp * kGroup);
+#pragma unroll 8
+            for (int r = 0; r < kGroup / 2; ++r) {
+              const float2 f2 = __half22float2(xr[r]);
+              sum += f2.x;
+              sum += f2.y;
+            }
+          }
+          xg[i] = sum;
+        }
+        T = n_tok <= 1 ? 1 : n_tok <= 2 ? 2 : n_tok <= 4 ? 4 : 8;
+        build_bfrag_regs(xs, d, n_tok, T, sb, bf);
+        int el;
+        const ExpertSet& es = expert_set(p, s_gd.expert, el);
+        thr = es.thr[el];
+        named_barrier(1, nct);
+        cur_g = g;
+      }
+      const int s = j % kUpStages;
+      const bool ok = mbar_wait(&full[s], (j / kUpStages) & 1);
+      const bool active = us + m_slot < ue;
+      float vacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      if (active && ok) {
+        const uint8_t* blk = stage + (size_t)s * L.stage_bytes + (size_t)(m_slot * nsb + sb) * kBlkBytes;
+        switch (T) {
+          case 1: up_superblock<1>(blk, bf, xg, sb, ng, ngrp, vacc); break;
+          case 2: up_superblock<2>(blk, bf, xg, sb, ng, ngrp, vacc); break;
+          case 4: up_superblock<4>(blk, bf, xg, sb, ng, ngrp, vacc); break;
+          default: up_superblock<8>(blk, bf, xg, sb, ng, ngrp, vacc); break;
+        }
+      }
+      vpart[((j & 1) * nwc + warp) * 32 + lane] = make_float4(vacc[0][0], vacc[0][1], vacc[1][0], vacc[1][1]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (barrier_or(1, nct, !ok)) {
+        if (threadIdx.x == 0) {
+          set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+        }
+        break;
+      }
+      if (threadIdx.x == 0) s_consumed = j + 1;
+      if (sb == 0 && active) {
+        float v[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        for (int q = 0; q < nsb; ++q) {
+          const float4 pv = vpart[((j & 1) * nwc + m_slot * nsb + q) * 32 + lane];
+          v[0][0] += pv.x;
+          v[0][1] += pv.y;
+          v[1][0] += pv.z;
+          v[1][1] += pv.w;
+        }
+        const long long u = us + m_slot;
+        const int mt = (int)(u - (long long)g * MT);
+        float* vb = vbuf + m_slot * 16 * kMaxTok;
+        switch (T) {
+          case 1: up_finalize<1>(p, s_gd, u, mt, thr, v, vb); break;
+          case 2: up_finalize<2>(p, s_gd, u, mt, thr, v, vb); break;
+          case 4: up_finalize<4>(p, s_gd, u, mt, thr, v, vb); break;
+          default: up_finalize<8>(p, s_gd, u, mt, thr, v, vb); break;
+        }
+      }
+      us = ue;
+    }
+  }
+  __syncthreads();
+  // on an abort, wait (bounded) for copies still in flight before the CTA exits
+  if (s_abort && threadIdx.x == 0)
+    for (int jj = s_consumed; jj < s_issued; ++jj) (void)mbar_wait(&full[jj % kUpStages], (jj / kUpStages) & 1);
+}
+
+size_t up_smem_bytes(int d, int max_tok) { return up_layout(d, max_tok).total; }
+int up_threads(int d) { return (up_layout(d, 1).nwc + 1) * 32; }
+
+// Register budget: 9 warps (d <= 4096) or up to 17 warps per CTA.
+static const void* up_kernel_for(int d) {
+  return up_threads(d) <= 288 ? (const void*)up_kernel<288> : (const void*)up_kernel<544>;
+}
+
+int up_blocks_per_sm(int d, int max_tok) {
+  const size_t smem = up_smem_bytes(d, max_tok);
+  const void* fn = up_kernel_for(d);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, up_threads(d), smem) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+cudaError_t launch_up(const ExpertParams& p, int grid, cudaStream_t st, bool pdl) {
+  const size_t smem = up_smem_bytes(p.d, p.max_tok);
+  const void* fn = up_kernel_for(p.d);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(up_threads(p.d));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (up_threads(p.d) <= 288) return cudaLaunchKernelEx(&cfg, up_kernel<288>, p);
+  return cudaLaunchKernelEx(&cfg, up_kernel<544>, p);
+}
+
+}  // namespace sesg
