@@ -196,12 +196,13 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
     __syncthreads();
 
     if (producer) {
-      if (lane == 0) {
+      // two producer lanes (even / odd items): two bulk-copy transactions in flight per SM
+      if (lane < 2) {
         const uint64_t pol = policy_evict_first();
         int last_g = -1;
         const __half* gbase_ptr = nullptr;
         const __half* dbase_ptr = nullptr;
-        for (int i = 0; i < n; ++i) {
+        for (int i = lane; i < n; i += 2) {
           const int gidx = base + i;
           const int s = gidx % S;
           if (gidx >= S && !mbar_wait(&empty[s], ((gidx / S) - 1) & 1)) {
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
           bulk_g2s(st, gbase_ptr + roff, (uint32_t)(2 * d), &full[s], pol);
           bulk_g2s(st + 2 * d, dbase_ptr + roff, (uint32_t)(2 * d), &full[s], pol);
           bulk_g2s(st + 4 * d, p.item_v + (size_t)lslot[i] * 8, 32u, &full[s], pol);
-          s_issued = gidx + 1;
+          atomicMax(&s_issued, gidx + 1);
         }
       }
     } else {

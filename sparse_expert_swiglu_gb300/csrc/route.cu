@@ -18,7 +18,7 @@ constexpr int kRouteThreads = 256;
 // rows; the rows are fetched RU at a time so that their loads are in flight together.
 template <int EV>
 __device__ void router_logits(const RouteParams& p, int b, float* logits, float* red) {
-  constexpr int RU = 8;
+  constexpr int RU = 16;
   const int tid = threadIdx.x;
   const int nchunk = p.E / EV;             // expert chunks
   const int nrs = kRouteThreads / nchunk;  // row slots
@@ -82,7 +82,8 @@ __device__ void router_logits(const RouteParams& p, int b, float* logits, float*
 }
 
 // Warp 0: k rounds of arg-max (larger logit, then lower index), softmax weights.
-__device__ void router_topk(const RouteParams& p, int b, const float* logits) {
+__device__ void router_topk(const RouteParams& p, int b, const float* logits, int* s_idx_out,
+                            float* s_w_out) {
   const int lane = threadIdx.x & 31;
   constexpr int kPer = 8;  // E <= 256
   float l[kPer];
@@ -140,6 +141,10 @@ __device__ void router_topk(const RouteParams& p, int b, const float* logits) {
       const float w = expf(sel_l[j] - lmax) / denom;
       p.topk_idx[b * p.k + j] = sel_idx[j];
       p.topk_w[b * p.k + j] = w;
+      if (s_idx_out) {
+        s_idx_out[b * p.k + j] = sel_idx[j];
+        s_w_out[b * p.k + j] = w;
+      }
       if (p.user_idx) p.user_idx[b * p.k + j] = sel_idx[j];
       if (p.user_w) p.user_w[b * p.k + j] = w;
     }
@@ -147,14 +152,20 @@ __device__ void router_topk(const RouteParams& p, int b, const float* logits) {
 }
 
 // Last CTA: counting of tokens per expert and the expert work groups.
-__device__ void router_group(const RouteParams& p) {
+__device__ void router_group(const RouteParams& p, bool local) {
   extern __shared__ float dyn[];
   int* s_idx = reinterpret_cast<int*>(dyn);   // [B*k]
   int* s_list = s_idx + p.B * p.k;            // [B*k] (token << 4 | slot) grouped by expert
+  float* s_w = reinterpret_cast<float*>(s_list + p.B * p.k);  // [B*k]
   __shared__ int s_cnt[256], s_off[257], s_goff[257];
   const int tid = threadIdx.x;
   const int npair = p.B * p.k;
-  for (int i = tid; i < npair; i += kRouteThreads) s_idx[i] = __ldcg(p.topk_idx + i);
+  if (!local) {  // top-k results of other CTAs: read them back through L2
+    for (int i = tid; i < npair; i += kRouteThreads) {
+      s_idx[i] = __ldcg(p.topk_idx + i);
+      s_w[i] = __ldcg(p.topk_w + i);
+    }
+  }
   __syncthreads();
   for (int e = tid; e < p.E; e += kRouteThreads) {
     int c = 0;
@@ -199,7 +210,7 @@ __device__ void router_group(const RouteParams& p) {
           const int b = pr >> 4, j = pr & 15;
           gd.tok[t] = b;
           gd.slot[t] = j;
-          gd.w[t] = __ldcg(p.topk_w + b * p.k + j);
+          gd.w[t] = s_w[b * p.k + j];
           p.tok_groups[b * kMaxSlots + j] = (g << 3) | t;
         } else {
           gd.tok[t] = 0;
@@ -236,9 +247,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   __shared__ int s_last;
   griddep_wait();
   griddep_launch_dependents();
+  extern __shared__ float dyn[];
+  const bool local = gridDim.x == 1;
+  int* s_idx = reinterpret_cast<int*>(dyn);
+  float* s_w = reinterpret_cast<float*>(s_idx + 2 * p.B * p.k);
   for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
     router_logits<EV>(p, b, s_logits, s_red);
-    if (threadIdx.x < 32) router_topk(p, b, s_logits);
+    if (threadIdx.x < 32) router_topk(p, b, s_logits, local ? s_idx : nullptr, local ? s_w : nullptr);
     __syncthreads();
   }
   if (gridDim.x > 1) {
@@ -250,7 +265,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
     if (!s_last) return;
     __threadfence();
   }
-  router_group(p);
+  router_group(p, local);
   if (threadIdx.x == 0) p.ctrl->route_done = 0;
 }
 
@@ -277,7 +292,7 @@ __global__ void expert_prep_kernel(int expert, int n, int gcap, GroupDesc* group
   if (threadIdx.x == 0) ctrl->G = G;
 }
 
-size_t route_group_smem(int B, int k) { return (size_t)2 * B * k * sizeof(int); }
+size_t route_group_smem(int B, int k) { return (size_t)3 * B * k * sizeof(int); }
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};

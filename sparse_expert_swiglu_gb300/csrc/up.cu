@@ -16,13 +16,17 @@
 
 namespace sesg {
 
-constexpr int kUpStages = 4;
+constexpr int kUpMaxStages = 4;
+constexpr size_t kUpSmemBudget = 200 * 1024;
 
 struct UpLayout {
-  int nsb, mpar, nwc;
-  size_t stage_bytes, off_full, off_empty, off_stage, off_x, off_xg, off_vpart, off_vbuf, total;
+  int nsb, mpar, nwc, spp, stages;
+  size_t strip, stage_bytes, off_full, off_empty, off_stage, off_x, off_xg, off_vpart, off_vbuf, total;
 };
 
+// Geometry: nwc compute warps (one superblock of one of mpar M-tiles each), one finalize
+// warp, one producer warp.  A ring stage holds spp steps of mpar M-tile strips, so that
+// every bulk-copy transaction moves >= 32 KB (smaller ones cost the same fixed time).
 __host__ __device__ inline UpLayout up_layout(int d, int max_tok) {
   UpLayout L;
   L.nsb = n_superblocks(d);
@@ -33,15 +37,23 @@ __host__ __device__ inline UpLayout up_layout(int d, int max_tok) {
     L.mpar = 1;
     L.nwc = L.nsb;
   }
-  L.stage_bytes = (size_t)L.mpar * L.nsb * kBlkBytes;
+  L.strip = (size_t)L.nsb * kBlkBytes;
+  const size_t step = L.strip * L.mpar;
+  L.spp = step >= 32768 ? 1 : (int)((32768 + step - 1) / step);
+  size_t fixed = 256 + (size_t)max_tok * d * 2 + (size_t)kMaxTok * (d / kGroup) * 4 +
+                 (size_t)2 * L.nwc * 32 * 16 + (size_t)L.mpar * 16 * kMaxTok * 4 + 64;
+  while (L.spp > 1 && fixed + 2 * step * L.spp > kUpSmemBudget) --L.spp;
+  L.stage_bytes = step * L.spp;
+  L.stages = (int)((kUpSmemBudget - fixed) / L.stage_bytes);
+  L.stages = L.stages > kUpMaxStages ? kUpMaxStages : (L.stages < 2 ? 2 : L.stages);
   size_t o = 0;
   L.off_full = o;
-  o += 8 * kUpStages;
+  o += 8 * kUpMaxStages;
   L.off_empty = o;
-  o += 8 * kUpStages;
+  o += 8 * kUpMaxStages;
   o = (o + 127) & ~(size_t)127;
   L.off_stage = o;
-  o += L.stage_bytes * kUpStages;
+  o += L.stage_bytes * L.stages;
   L.off_x = o;
   o += (size_t)max_tok * d * 2;
   o = (o + 15) & ~(size_t)15;
@@ -57,16 +69,85 @@ __host__ __device__ inline UpLayout up_layout(int d, int max_tok) {
 }
 
 template <int GI>
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t wsh) {
+__device__ __forceinline__ uint32_t code_pair(uint32_t w) {
   // Two 2-bit codes of group slot GI as an fp16x2 of subnormals q * 4^pos * 2^-24
-  // (exact); the power of two is removed after the mma.
+  // (exact); the power of two is removed after the mma.  Slots 5..7 sit above the
+  // 10-bit mantissa and are shifted down first.
   if constexpr (GI < 5) return w & (0x00030003u << (2 * GI));
-  else return wsh & (0x00030003u << (2 * (GI - 5)));
+  else return (w >> 10) & (0x00030003u << (2 * (GI - 5)));
 }
 
 __device__ __forceinline__ float pos_scale(int gi) {
   const int pos = gi < 5 ? gi : gi - 5;
   return __int_as_float((127 + 24 - 2 * pos) << 23);  // 2^(24 - 2 pos)
+}
+
+// k-steps of quantiser group GI (compile time): 4 mma into the 4 accumulator chains.
+template <int GI>
+__device__ __forceinline__ void up_group(const uint4 (&w)[4], const uint32_t (&bf)[64],
+                                         float (&D)[4][4]) {
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    uint32_t a[4];
+    a[0] = code_pair<GI>(w[t].x);
+    a[1] = code_pair<GI>(w[t].y);
+    a[2] = code_pair<GI>(w[t].z);
+    a[3] = code_pair<GI>(w[t].w);
+    mma_16816(D[t], a, bf[2 * (GI * 4 + t)], bf[2 * (GI * 4 + t) + 1]);
+  }
+}
+
+template <int T, int PH, int GAM>
+__device__ __forceinline__ void up_phase_groups(const uint4 (&w)[4],
+                                                const uint32_t (&bf)[64], float (&D)[4][4], int ng) {
+  constexpr int G = 8 / T;
+  if constexpr (GAM < G) {
+    constexpr int GI = PH * G + GAM;
+    if (GI < ng) up_group<GI>(w, bf, D);
+    up_phase_groups<T, PH, GAM + 1>(w, bf, D, ng);
+  }
+}
+
+// Fold the accumulators of phase PH (G quantiser groups side by side) into v.
+template <int T, int PH>
+__device__ __forceinline__ void up_phase(const uint4 (&w)[4],
+                                         const uint32_t (&bf)[64], const uint8_t* __restrict__ szt,
+                                         const float* __restrict__ xg, int sb, int ng, int ngrp,
+                                         float (&vacc)[2][2]) {
+  constexpr int G = 8 / T;
+  const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
+  float D[4][4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) D[t][0] = D[t][1] = D[t][2] = D[t][3] = 0.f;
+  up_phase_groups<T, PH, 0>(w, bf, D, ng);
+  const int gi_lane = (G >= 2) ? (2 * c) % G : 0;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int gi = (G >= 2) ? PH * G + gi_lane + s : PH;
+    const int tau = (G >= 2) ? (2 * c) / G : 2 * c + s;
+    if (gi < ng) {
+      const float cs = pos_scale(gi);
+      const float X = xg[tau * ngrp + sb * 8 + gi];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const __half2 h = *reinterpret_cast<const __half2*>(szt + ((gl + 8 * r) * 8 + gi) * 4);
+        const float sf = __low2float(h), zf = __high2float(h);
+        const float acc = (D[0][2 * r + s] + D[1][2 * r + s]) + (D[2][2 * r + s] + D[3][2 * r + s]);
+        vacc[r][s] = fmaf(sf, fmaf(-zf, X, acc * cs), vacc[r][s]);
+      }
+    }
+  }
+}
+
+template <int T, int PH>
+__device__ __forceinline__ void up_phases(const uint4 (&w)[4],
+                                          const uint32_t (&bf)[64], const uint8_t* __restrict__ szt,
+                                          const float* __restrict__ xg, int sb, int ng, int ngrp,
+                                          float (&vacc)[2][2]) {
+  if constexpr (PH < T) {
+    up_phase<T, PH>(w, bf, szt, xg, sb, ng, ngrp, vacc);
+    up_phases<T, PH + 1>(w, bf, szt, xg, sb, ng, ngrp, vacc);
+  }
 }
 
 // One warp: partial v of its superblock of one M-tile.
@@ -77,69 +158,19 @@ __device__ __forceinline__ float pos_scale(int gi) {
 // class gi % G, whose B column carries that token's x; the other B columns are
 // zero.  One accumulator tile therefore collects G quantiser groups side by side,
 // and the per-group correction v += s * (A_g - z * X_g) (X_g = sum of x over the
-// group) is applied once per G groups.  Two accumulator chains (even / odd k-step)
-// halve the mma dependency chain.
+// group) is applied once per G groups.  Four accumulator chains (one per k-step of a
+// group) shorten the mma dependency chain.  Every group index is a compile-time
+// constant, so the codes, fragments and accumulators stay in registers.
 template <int T>
 __device__ __forceinline__ void up_superblock(const uint8_t* __restrict__ blk,
                                               const uint32_t (&bf)[64],
                                               const float* __restrict__ xg, int sb, int ng,
                                               int ngrp, float (&vacc)[2][2]) {
-  constexpr int G = 8 / T;
-  const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
-  uint4 w[4], wsh[4];
+  const int lane = threadIdx.x & 31;
+  uint4 w[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    w[q] = reinterpret_cast<const uint4*>(blk)[q * 32 + lane];
-    wsh[q] = make_uint4(w[q].x >> 10, w[q].y >> 10, w[q].z >> 10, w[q].w >> 10);
-  }
-  const int gi_lane = (G >= 2) ? (2 * c) % G : 0;
-  const uint8_t* szt = blk + kBlkCodeBytes;
-#pragma unroll
-  for (int ph = 0; ph < T; ++ph) {
-    float D0[4] = {0.f, 0.f, 0.f, 0.f}, D1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int gam = 0; gam < G; ++gam) {
-      const int gi = ph * G + gam;
-      if (gi < ng) {
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          uint32_t a[4];
-#define SESG_CASE(GIV)                          \
-  case GIV:                                     \
-    a[0] = code_pair<GIV>(w[t].x, wsh[t].x);    \
-    a[1] = code_pair<GIV>(w[t].y, wsh[t].y);    \
-    a[2] = code_pair<GIV>(w[t].z, wsh[t].z);    \
-    a[3] = code_pair<GIV>(w[t].w, wsh[t].w);    \
-    break;
-          switch (gi) {
-            SESG_CASE(0) SESG_CASE(1) SESG_CASE(2) SESG_CASE(3)
-            SESG_CASE(4) SESG_CASE(5) SESG_CASE(6) default: SESG_CASE(7)
-          }
-#undef SESG_CASE
-          const int ks = gi * 4 + t;
-          if (t & 1) mma_16816(D1, a, bf[2 * ks], bf[2 * ks + 1]);
-          else mma_16816(D0, a, bf[2 * ks], bf[2 * ks + 1]);
-        }
-      }
-    }
-    // fold this phase's G groups into v
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const int gi = (G >= 2) ? ph * G + gi_lane + s : ph;
-      const int tau = (G >= 2) ? (2 * c) / G : 2 * c + s;
-      if (gi < ng) {
-        const float cs = pos_scale(gi);
-        const float X = xg[tau * ngrp + sb * 8 + gi];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const __half2 h = *reinterpret_cast<const __half2*>(szt + ((gl + 8 * r) * 8 + gi) * 4);
-          const float sf = __low2float(h), zf = __high2float(h);
-          const float acc = D0[2 * r + s] + D1[2 * r + s];
-          vacc[r][s] = fmaf(sf, fmaf(-zf, X, acc * cs), vacc[r][s]);
-        }
-      }
-    }
-  }
+  for (int q = 0; q < 4; ++q) w[q] = reinterpret_cast<const uint4*>(blk)[q * 32 + lane];
+  up_phases<T, 0>(w, bf, blk + kBlkCodeBytes, xg, sb, ng, ngrp, vacc);
 }
 
 // One warp, after the superblock partials are summed: per-token v of the M-tile's
@@ -268,9 +299,11 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
   __shared__ GroupDesc s_gd;
   __shared__ int s_abort, s_issued, s_consumed;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwc = L.nwc, nct = nwc * 32, nsb = L.nsb;
+  const int nwc = L.nwc, nsb = L.nsb, S = L.stages, spp = L.spp;
+  const int fin_warp = nwc, prod_warp = nwc + 1;
+  const int nbar = (nwc + 1) * 32;  // compute warps + the finalize warp
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kUpStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], nwc);
     }
@@ -287,123 +320,148 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
   const long long U = (long long)G * MT;
   const long long u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
   const int ngrp = d / kGroup;
+  // steps: up to mpar consecutive units of one group; stage = spp consecutive steps
+  auto step_end = [&](long long us) { return min(min(us + L.mpar, u1), (us / MT + 1) * MT); };
 
-  if (warp == nwc) {
-    // ---- producer: one bulk copy per unit (its whole d-strip), one ring stage per step
+  if (warp == prod_warp) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int j = 0, last_g = -1;
-      const uint8_t* base = nullptr;
-      for (long long us = u0; us < u1; ++j) {
-        const long long ue = min(min(us + L.mpar, u1), (us / MT + 1) * MT);
-        const int s = j % kUpStages;
-        if (j >= kUpStages && !mbar_wait(&empty[s], ((j / kUpStages) - 1) & 1)) {
+      int j = 0;
+      for (long long us = u0; us < u1;) {
+        const int st = j / spp;
+        const int s = st % S;
+        if (st >= S && !mbar_wait(&empty[s], ((st / S) - 1) & 1)) {
           set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
           atomicExch(&s_abort, 1);
           break;
         }
         if (*reinterpret_cast<volatile int*>(&s_abort)) break;
-        const int g = (int)(us / MT);
-        if (g != last_g) {
-          last_g = g;
+        // the stage's steps and bytes
+        long long ends[4];
+        uint32_t bytes = 0;
+        int nst = 0;
+        for (long long v = us; v < u1 && nst < spp; ++nst) {
+          ends[nst] = step_end(v);
+          bytes += (uint32_t)((ends[nst] - v) * L.strip);
+          v = ends[nst];
+        }
+        mbar_arrive_expect_tx(&full[s], bytes);
+        for (int q = 0; q < nst; ++q) {
+          const long long ue = ends[q];
+          const int g = (int)(us / MT);
           int el;
           const ExpertSet& es = expert_set(p, p.groups[g].expert, el);
-          base = es.up + (size_t)el * es.up_stride;
+          const uint8_t* src = es.up + (size_t)el * es.up_stride + (size_t)(us - (long long)g * MT) * L.strip;
+          bulk_g2s(stage + (size_t)s * L.stage_bytes + (size_t)q * L.mpar * L.strip, src,
+                   (uint32_t)((ue - us) * L.strip), &full[s], pol);
+          us = ue;
+          ++j;
         }
-        const uint32_t strip = (uint32_t)(nsb * kBlkBytes);
-        mbar_arrive_expect_tx(&full[s], (uint32_t)(ue - us) * strip);
-        for (long long u = us; u < ue; ++u)
-          bulk_g2s(stage + (size_t)s * L.stage_bytes + (size_t)(u - us) * strip,
-                   base + (size_t)(u - (long long)g * MT) * strip, strip, &full[s], pol);
-        s_issued = j + 1;
-        us = ue;
+        s_issued = st + 1;
       }
     }
   } else {
-    // ---- consumers
-    const int m_slot = warp / nsb, sb = warp % nsb;
+    // ---- compute warps (w < nwc) and the finalize warp (w == nwc)
+    const bool fin = warp == fin_warp;
+    const int m_slot = fin ? 0 : warp / nsb, sb = fin ? 0 : warp % nsb;
     const int ng = min(8, (d - sb * kSuper) / kGroup);
     int cur_g = -1, T = 1;
     float thr = 0.f;
     uint32_t bf[64];
     int j = 0;
     for (long long us = u0; us < u1; ++j) {
-      const long long ue = min(min(us + L.mpar, u1), (us / MT + 1) * MT);
+      const long long ue = step_end(us);
       const int g = (int)(us / MT);
       if (g != cur_g) {
-        named_barrier(1, nct);
+        named_barrier(1, nbar);
         if (threadIdx.x == 0) s_gd = p.groups[g];
-        named_barrier(1, nct);
+        named_barrier(1, nbar);
         const int n_tok = s_gd.n_tok;
-        for (int i = threadIdx.x; i < n_tok * (d / 8); i += nct) {
+        for (int i = threadIdx.x; i < n_tok * (d / 8); i += nbar) {
           const int t = i / (d / 8), o = i % (d / 8);
           reinterpret_cast<uint4*>(xs + (size_t)t * d)[o] =
               __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)s_gd.tok[t] * d) + o);
         }
-        named_barrier(1, nct);
-        for (int i = threadIdx.x; i < kMaxTok * ngrp; i += nct) {
+        int el;
+        const ExpertSet& es = expert_set(p, s_gd.expert, el);
+        thr = es.thr[el];
+        named_barrier(1, nbar);
+        for (int i = threadIdx.x; i < kMaxTok * ngrp; i += nbar) {
           const int t = i / ngrp, grp = i % ngrp;
           float sum = 0.f;
           if (t < n_tok) {
-            const __half2* xr = reinterpret_cast<const __half2*>(xs + (size_t)t * d + grp * kGroup);
-#pragma unroll 8
-            for (int r = 0; r < kGroup / 2; ++r) {
-              const float2 f2 = __half22float2(xr[r]);
-              sum += f2.x;
-              sum += f2.y;
+            const uint4* xr = reinterpret_cast<const uint4*>(xs + (size_t)t * d + grp * kGroup);
+#pragma unroll
+            for (int r = 0; r < kGroup / 8; ++r) {
+              const uint4 v = xr[r];
+              const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f2 = __half22float2(h2[e]);
+                sum += f2.x;
+                sum += f2.y;
+              }
             }
           }
           xg[i] = sum;
         }
         T = n_tok <= 1 ? 1 : n_tok <= 2 ? 2 : n_tok <= 4 ? 4 : 8;
-        build_bfrag_regs(xs, d, n_tok, T, sb, bf);
-        int el;
-        const ExpertSet& es = expert_set(p, s_gd.expert, el);
-        thr = es.thr[el];
-        named_barrier(1, nct);
+        if (!fin) build_bfrag_regs(xs, d, n_tok, T, sb, bf);
+        named_barrier(1, nbar);
         cur_g = g;
       }
-      const int s = j % kUpStages;
-      const bool ok = mbar_wait(&full[s], (j / kUpStages) & 1);
-      const bool active = us + m_slot < ue;
-      float vacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-      if (active && ok) {
-        const uint8_t* blk = stage + (size_t)s * L.stage_bytes + (size_t)(m_slot * nsb + sb) * kBlkBytes;
-        switch (T) {
-          case 1: up_superblock<1>(blk, bf, xg, sb, ng, ngrp, vacc); break;
-          case 2: up_superblock<2>(blk, bf, xg, sb, ng, ngrp, vacc); break;
-          case 4: up_superblock<4>(blk, bf, xg, sb, ng, ngrp, vacc); break;
-          default: up_superblock<8>(blk, bf, xg, sb, ng, ngrp, vacc); break;
+      const int st = j / spp, s = st % S;
+      const bool first = (j % spp) == 0;
+      const bool last = ((j % spp) == spp - 1) || ue >= u1;
+      bool ok = true;
+      if (!fin) {
+        if (first) ok = mbar_wait(&full[s], (st / S) & 1);
+        const bool active = us + m_slot < ue;
+        float vacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        if (active && ok) {
+          const uint8_t* blk = stage + (size_t)s * L.stage_bytes +
+                               ((size_t)(j % spp) * L.mpar + m_slot) * L.strip + (size_t)sb * kBlkBytes;
+          switch (T) {
+            case 1: up_superblock<1>(blk, bf, xg, sb, ng, ngrp, vacc); break;
+            case 2: up_superblock<2>(blk, bf, xg, sb, ng, ngrp, vacc); break;
+            case 4: up_superblock<4>(blk, bf, xg, sb, ng, ngrp, vacc); break;
+            default: up_superblock<8>(blk, bf, xg, sb, ng, ngrp, vacc); break;
+          }
         }
+        vpart[((j & 1) * nwc + warp) * 32 + lane] =
+            make_float4(vacc[0][0], vacc[0][1], vacc[1][0], vacc[1][1]);
+        __syncwarp();
+        if (last && lane == 0) mbar_arrive(&empty[s]);
       }
-      vpart[((j & 1) * nwc + warp) * 32 + lane] = make_float4(vacc[0][0], vacc[0][1], vacc[1][0], vacc[1][1]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      if (barrier_or(1, nct, !ok)) {
+      if (barrier_or(1, nbar, !ok)) {
         if (threadIdx.x == 0) {
           set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
           atomicExch(&s_abort, 1);
         }
         break;
       }
-      if (threadIdx.x == 0) s_consumed = j + 1;
-      if (sb == 0 && active) {
-        float v[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        for (int q = 0; q < nsb; ++q) {
-          const float4 pv = vpart[((j & 1) * nwc + m_slot * nsb + q) * 32 + lane];
-          v[0][0] += pv.x;
-          v[0][1] += pv.y;
-          v[1][0] += pv.z;
-          v[1][1] += pv.w;
-        }
-        const long long u = us + m_slot;
-        const int mt = (int)(u - (long long)g * MT);
-        float* vb = vbuf + m_slot * 16 * kMaxTok;
-        switch (T) {
-          case 1: up_finalize<1>(p, s_gd, u, mt, thr, v, vb); break;
-          case 2: up_finalize<2>(p, s_gd, u, mt, thr, v, vb); break;
-          case 4: up_finalize<4>(p, s_gd, u, mt, thr, v, vb); break;
-          default: up_finalize<8>(p, s_gd, u, mt, thr, v, vb); break;
+      if (threadIdx.x == 0 && last) s_consumed = st + 1;
+      if (fin) {
+        // sum the superblock partials of every M-tile of step j; threshold and compaction
+        for (int m = 0; m < L.mpar; ++m) {
+          if (us + m >= ue) break;
+          float v[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+          for (int q = 0; q < nsb; ++q) {
+            const float4 pv = vpart[((j & 1) * nwc + m * nsb + q) * 32 + lane];
+            v[0][0] += pv.x;
+            v[0][1] += pv.y;
+            v[1][0] += pv.z;
+            v[1][1] += pv.w;
+          }
+          const long long u = us + m;
+          const int mt = (int)(u - (long long)g * MT);
+          float* vb = vbuf + m * 16 * kMaxTok;
+          switch (T) {
+            case 1: up_finalize<1>(p, s_gd, u, mt, thr, v, vb); break;
+            case 2: up_finalize<2>(p, s_gd, u, mt, thr, v, vb); break;
+            case 4: up_finalize<4>(p, s_gd, u, mt, thr, v, vb); break;
+            default: up_finalize<8>(p, s_gd, u, mt, thr, v, vb); break;
+          }
         }
       }
       us = ue;
@@ -412,15 +470,15 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
   __syncthreads();
   // on an abort, wait (bounded) for copies still in flight before the CTA exits
   if (s_abort && threadIdx.x == 0)
-    for (int jj = s_consumed; jj < s_issued; ++jj) (void)mbar_wait(&full[jj % kUpStages], (jj / kUpStages) & 1);
+    for (int q = max(s_consumed, s_issued - S); q < s_issued; ++q) (void)mbar_wait(&full[q % S], (q / S) & 1);
 }
 
 size_t up_smem_bytes(int d, int max_tok) { return up_layout(d, max_tok).total; }
-int up_threads(int d) { return (up_layout(d, 1).nwc + 1) * 32; }
+int up_threads(int d) { return (up_layout(d, 1).nwc + 2) * 32; }
 
-// Register budget: 9 warps (d <= 4096) or up to 17 warps per CTA.
+// Register budget: 10 warps (d <= 4096) or up to 18 warps per CTA.
 static const void* up_kernel_for(int d) {
-  return up_threads(d) <= 288 ? (const void*)up_kernel<288> : (const void*)up_kernel<544>;
+  return up_threads(d) <= 320 ? (const void*)up_kernel<320> : (const void*)up_kernel<576>;
 }
 
 int up_blocks_per_sm(int d, int max_tok) {
@@ -449,8 +507,8 @@ cudaError_t launch_up(const ExpertParams& p, int grid, cudaStream_t st, bool pdl
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (up_threads(p.d) <= 288) return cudaLaunchKernelEx(&cfg, up_kernel<288>, p);
-  return cudaLaunchKernelEx(&cfg, up_kernel<544>, p);
+  if (up_threads(p.d) <= 320) return cudaLaunchKernelEx(&cfg, up_kernel<320>, p);
+  return cudaLaunchKernelEx(&cfg, up_kernel<576>, p);
 }
 
 }  // namespace sesg
