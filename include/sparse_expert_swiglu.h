@@ -145,6 +145,28 @@ moe_status_t moe_route_topk(const uint16_t* x, int32_t B, int32_t d, const uint1
                             int32_t E, int32_t k, int32_t renorm, int32_t* topk_idx, float* topk_w,
                             int32_t* expert_count, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * moe_route_topk_noalloc -- moe_route_topk without a caller workspace.  The
+ * papers have no counterpart to this call: it is a deployment convenience.
+ * It serves callers that cannot allocate device memory (a plugin given only its
+ * input and output pointers, a runtime with a fixed memory pool, a path where an
+ * allocation would synchronise the device).  Its scratch is a static device array
+ * inside the library, one per device, sized for at most
+ * MOE_ROUTE_NOALLOC_MAX_PAIRS = B * k (token, expert) pairs.
+ *   Arguments, layouts and results are those of moe_route_topk.
+ *   B * k > MOE_ROUTE_NOALLOC_MAX_PAIRS: MOE_ERR_WORKSPACE_TOO_SMALL, nothing enqueued.
+ *   The first call on a device looks up the scratch address (with that device
+ *   current); make it before capturing a stream.  Every call clears the scratch's
+ *   control block on `stream` before the kernel.  Calls that overlap in time on
+ *   one device (different streams or host threads) share the scratch and race:
+ *   order them on one stream.
+ */
+#define MOE_ROUTE_NOALLOC_MAX_PAIRS 2048
+moe_status_t moe_route_topk_noalloc(const uint16_t* x, int32_t B, int32_t d,
+                                    const uint16_t* w_router, int32_t E, int32_t k,
+                                    int32_t renorm, int32_t* topk_idx, float* topk_w,
+                                    int32_t* expert_count, void* stream);
+
 /* ---------------- one expert ---------------- */
 
 /*

@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     pack_int2_up,
     packed_bytes,
     route_topk,
+    route_topk_noalloc,
     route_workspace_bytes,
     unpack_int2_up,
 )

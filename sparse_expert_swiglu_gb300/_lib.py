@@ -61,6 +61,10 @@ _SIGS = {
                                       ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                       ctypes.c_void_p]),
+    "moe_route_topk_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p]),
     "moe_expert_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32] * 3),
     "moe_expert_sparse_swiglu": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
                                                 ctypes.POINTER(_Experts), ctypes.c_int32,
@@ -285,6 +289,26 @@ def route_topk(x: torch.Tensor, w_router: torch.Tensor, k: int, renorm: bool = T
     _check("moe_route_topk", lib().moe_route_topk(_ptr(x), B, d, _ptr(w_router), E, k,
                                                   1 if renorm else 0, _ptr(idx), _ptr(w),
                                                   _ptr(cnt), ws.ptr(), ws.nbytes, _stream()))
+    return idx, w, cnt
+
+
+ROUTE_NOALLOC_MAX_PAIRS = 2048
+
+
+def route_topk_noalloc(x: torch.Tensor, w_router: torch.Tensor, k: int, renorm: bool = True):
+    """route_topk through the entry point that uses the library's static scratch
+    instead of a workspace (B * k <= ROUTE_NOALLOC_MAX_PAIRS)."""
+    _need(x, torch.float16, "x")
+    _need(w_router, torch.float16, "w_router")
+    B, d = x.shape
+    E = w_router.shape[1]
+    idx = torch.empty((B, k), dtype=torch.int32, device=x.device)
+    w = torch.empty((B, k), dtype=torch.float32, device=x.device)
+    cnt = torch.empty((E,), dtype=torch.int32, device=x.device)
+    _check("moe_route_topk_noalloc",
+           lib().moe_route_topk_noalloc(_ptr(x), B, d, _ptr(w_router), E, k,
+                                        1 if renorm else 0, _ptr(idx), _ptr(w), _ptr(cnt),
+                                        _stream()))
     return idx, w, cnt
 
 

@@ -83,6 +83,10 @@ def test_host_argument_checks(so):
     assert lib.moe_route_topk(fake, 1, 256, fake, 8, 9, 1, fake, fake, None, fake, 1 << 20, None) == -1
     assert lib.moe_route_topk(fake, 1, 300, fake, 8, 2, 1, fake, fake, None, fake, 1 << 20, None) == -2
     assert lib.moe_route_topk(fake, 0, 256, fake, 8, 2, 1, fake, fake, None, fake, 1 << 20, None) == 0
+    # the static-scratch router: more than 2048 (token, expert) pairs is refused up front
+    assert lib.moe_route_topk_noalloc(fake, 1024, 256, fake, 8, 4, 1, fake, fake, None, None) == -4
+    assert lib.moe_route_topk_noalloc(fake, 1, 256, fake, 8, 9, 1, fake, fake, None, None) == -1
+    assert lib.moe_route_topk_noalloc(fake, 0, 256, fake, 8, 2, 1, fake, fake, None, None) == 0
 
     ex = _lib._Experts(8, 4096, 14336, 0x10000, 0x20000, 0x30000, 0x40000)
     layer = _lib._Layer(2, 1, 0x50000, ex, _lib._Experts(0, 4096, 14336, None, None, None, None))
