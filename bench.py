@@ -40,7 +40,10 @@ METRIC = "MoE decode layer expert-tokens/s (Mixtral-8x7B-shaped layer, 1 token, 
 
 # ncu DRAM bytes per launch of the dominant kernel, keyed by the source file hash it was
 # taken on; reported only while the kernel source is unchanged.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # gather_kernel, layer copy 0 at 70% (1-copy small case): 144.54 MB read + 3.10 MB written
+    ("gather", "dbf6946cb4876587"): 147.64e6,
+}
 
 
 def parse_args():
@@ -51,6 +54,10 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sparsity", type=int, default=HEADLINE_PCT)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--copies", type=int, default=N_LAYER_COPIES,
+                    help="rotating layer copies (fewer: a small case for profiling; below 8 the "
+                         "weights no longer exceed L2 by a wide margin)")
+    ap.add_argument("--no-sweep", action="store_true", help="time only the headline sparsity")
     return ap.parse_args()
 
 
@@ -406,7 +413,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     W = WORKLOAD
     d, f, E, k, B = W["d"], W["f"], W["E"], W["k"], W["B"]
-    R = N_LAYER_COPIES
+    R = max(1, args.copies)
     layers = build_layers(dev, R)
     table = calibrate(layers, dev)
     xs = [synth.tokens(B, d, 1000 + r + 100 * rank, device=dev) for r in range(R)]
@@ -417,7 +424,7 @@ def run_ours(args, world, rank, local):
     # per-sparsity sweep (the headline is re-timed below with the clock sampler)
     graphs, stream = capture_graphs(layers, xs, ys, ws_list)
     sweep = []
-    for pct in SPARSITIES:
+    for pct in (() if args.no_sweep else SPARSITIES):
         set_thresholds(layers, table, pct)
         byts = algorithmic_bytes(layers, xs, ws_list)
         secs = time_steps(graphs, stream, max(200, args.steps // 4), args.warmup, world, dev)
@@ -507,7 +514,7 @@ def run_ours(args, world, rank, local):
                    "gate_down": "fp16", "rmsnorm": True, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {R} rotating layer copies "
                          f"({sum(l.routed.gate_t.numel() * 4 + l.routed.up_packed.numel() for l in layers) / 1e9:.1f} GB), "
-                         "each reused only after 7 others",
+                         f"each reused only after {R - 1} others",
                    "graphs": "one CUDA graph per layer copy, PDL between kernels"},
         "layer_us": ms_per_step * 1e3,
         "layer_roofline": {"bytes_per_step": mean_bytes, "hbm_gbs": mean_bytes / (ms_per_step * 1e-3) / 1e9,
