@@ -174,7 +174,8 @@ def build_layers(dev, R):
     for r in range(R):
         de = synth.experts(W["E"], W["d"], W["f"], 100 + r, device=dev, layer=r)
         ex = ses.Experts.from_dense(de.w_up, de.gate_t, de.down,
-                                    torch.zeros(W["E"], dtype=torch.float32, device=dev))
+                                    torch.zeros(W["E"], dtype=torch.float32, device=dev),
+                                    interleave=True)
         del de
         wr = synth.router(W["d"], W["E"], 100 + r, device=dev, layer=r)
         layers.append(ses.Layer(wr, ex, W["k"], True))

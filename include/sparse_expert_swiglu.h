@@ -18,8 +18,8 @@
  *
  * Conventions shared by every entry point:
  *   - Every tensor pointer is a DEVICE pointer owned by the caller, unless the
- *     comment says "host".  The library allocates nothing and keeps no global
- *     mutable state; all scratch lives in the caller's workspace.
+ *     comment says "host".  The library allocates nothing; all scratch lives in the
+ *     caller's workspace, except the static scratch of moe_route_topk_noalloc.
  *   - fp16 tensors are IEEE binary16 bit patterns passed as uint16_t.  All
  *     arrays are dense, row-major, and start on a 16-byte boundary.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
@@ -70,7 +70,10 @@ typedef struct {
   const void* up_packed;     /* [E][expert_int2_up_packed_bytes(d, f)] from expert_pack_int2_up */
   const uint16_t* gate_t;    /* fp16 [E][f][d]: row i = column i of W^gate */
   const uint16_t* down;      /* fp16 [E][f][d]: row i = row i of W^down (the transposed,
-                                column-major W^down of FloE's kernel optimisation list) */
+                                column-major W^down of FloE's kernel optimisation list).
+                                Interleaved form: one buffer [E][f][2][d] holding gate row i
+                                then down row i; pass gate_t = buffer, down = buffer + d.
+                                The two rows of a kept column are then one contiguous read. */
   const float* thr;          /* fp32 [E]: threshold t_ij of Algorithm 1, one per expert */
 } moe_experts_t;
 
@@ -96,7 +99,10 @@ typedef struct {
   void** events;       /* 5 cudaEvent_t (as void*), recorded on `stream` before the router
                           (or the single-expert set-up), before the up-projection kernel,
                           before the gather kernel, before the combine kernel and after it;
-                          for per-kernel timing.  Recording them serialises the kernels. */
+                          for per-kernel timing.  Recording them serialises the kernels.
+                          On the decode path (moe_layer_decode with 1 or 2 tokens) the
+                          router runs inside the up-projection kernel: events 0 and 1 are
+                          recorded back to back. */
 } moe_debug_t;
 
 /* ---------------- INT2 up projection ---------------- */

@@ -201,22 +201,41 @@ class Experts:
     def d(self):
         return self.gate_t.shape[2]
 
+    @property
+    def interleaved(self) -> bool:
+        """gate and down rows share one buffer [E, f, 2, d] (gate row i, then down row i)."""
+        return (self.gate_t.dim() == 3 and self.gate_t.stride() == self.down.stride()
+                and self.gate_t.stride(1) == 2 * self.d
+                and self.down.data_ptr() == self.gate_t.data_ptr() + 2 * self.d)
+
     def c_struct(self) -> _Experts:
         _need(self.up_packed, torch.uint8, "up_packed")
-        _need(self.gate_t, torch.float16, "gate_t")
-        _need(self.down, torch.float16, "down")
         _need(self.thr, torch.float32, "thr")
+        if self.interleaved:
+            both = self.gate_t.as_strided((self.E, self.f, 2, self.d),
+                                          (self.f * 2 * self.d, 2 * self.d, self.d, 1))
+            _need(both, torch.float16, "gate_t/down (interleaved)")
+        else:
+            _need(self.gate_t, torch.float16, "gate_t")
+            _need(self.down, torch.float16, "down")
         return _Experts(self.E, self.d, self.f, self.up_packed.data_ptr(), self.gate_t.data_ptr(),
                         self.down.data_ptr(), self.thr.data_ptr())
 
     @staticmethod
     def from_dense(w_up: torch.Tensor, gate_t: torch.Tensor, down: torch.Tensor,
-                   thr: torch.Tensor) -> "Experts":
-        """Pack every W^up [E, d, f] with the library's INT2 quantiser."""
+                   thr: torch.Tensor, interleave: bool = False) -> "Experts":
+        """Pack every W^up [E, d, f] with the library's INT2 quantiser.  interleave=True
+        stores gate and down rows in one buffer [E, f, 2, d], so that a kept column's two
+        rows are one contiguous 4d-byte read."""
         E, d, f = w_up.shape
         up = torch.empty((E, packed_bytes(d, f)), dtype=torch.uint8, device=w_up.device)
         for e in range(E):
             pack_int2_up(w_up[e].contiguous(), up[e])
+        if interleave:
+            gd = torch.empty((E, f, 2, d), dtype=gate_t.dtype, device=gate_t.device)
+            gd[:, :, 0, :] = gate_t
+            gd[:, :, 1, :] = down
+            return Experts(up, gd[:, :, 0, :], gd[:, :, 1, :], thr.contiguous())
         return Experts(up, gate_t.contiguous(), down.contiguous(), thr.contiguous())
 
 

@@ -44,7 +44,7 @@ int groups_max_routed(int B, int E, int k, int gcap) {
 // Workspace carving shared by every entry point.
 struct WsLayout {
   size_t ctrl, groups, tok_groups, topk_idx, topk_w, group_total, unit_cnt, item_col, item_v,
-      part, yacc, sumsq, tok_ctr, total;
+      part, sumsq, tok_ctr, cta_total, total;
   int G_max, P3, list_cap;
 };
 
@@ -71,9 +71,9 @@ WsLayout ws_layout(int B, int npairs, int G_max, int d, int f, int P3) {
   L.item_col = take(sizeof(int) * (size_t)G_max * MT * 16);
   L.item_v = take(sizeof(float) * (size_t)G_max * MT * 16 * 8);
   L.part = take(sizeof(float) * (size_t)(P3 + G_max) * kMaxTok * d);
-  L.yacc = take(sizeof(float) * (size_t)B * d);
-  L.sumsq = take(sizeof(float) * (size_t)B * (d / 128));
-  L.tok_ctr = take(sizeof(int) * (size_t)B);
+  L.sumsq = take(sizeof(float) * (size_t)B * (d / 32));
+  L.tok_ctr = take(sizeof(int) * (size_t)2 * B);
+  L.cta_total = take(sizeof(int) * (size_t)P3);
   L.total = o;
   return L;
 }
@@ -111,6 +111,7 @@ ExpertSet to_set(const moe_experts_t& ex) {
   s.down = reinterpret_cast<const __half*>(ex.down);
   s.thr = ex.thr;
   s.up_stride = packed_bytes_per_expert(ex.d, ex.f);
+  s.rs = (s.down == s.gate_t + ex.d) ? 2 * ex.d : ex.d;
   return s;
 }
 
@@ -242,9 +243,6 @@ static moe_status_t run_experts(const uint16_t* x, int B, const moe_experts_t* r
   p.dbg_mask = dbg ? dbg->mask : nullptr;
   p.y = reinterpret_cast<__half*>(y);
   p.rmsnorm = rmsnorm;
-  p.yacc = at<float>(ws, L.yacc);
-  p.sumsq = at<float>(ws, L.sumsq);
-  p.tok_ctr = at<int>(ws, L.tok_ctr);
   p.P3 = L.P3;
   p.stages = pl.stages;
   p.list_cap = L.list_cap;
@@ -342,6 +340,56 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = (cudaStream_t)stream;
   const int k = layer->k;
+  const int P = di.sms;
+  int su = 0, sr = 0;
+  const int cap = decode_list_cap(B, layer->routed.f, k, layer->shared.E, P);
+  if (decode_supported(B, layer->routed.d, layer->routed.f, layer->routed.E, k, layer->shared.E, P) &&
+      decode_plan(B, layer->routed.d, layer->routed.E, cap, P, di.smem_optin, su, sr)) {
+    // one or two tokens: up kernel, gather kernel, combine kernel
+    DecodeParams dp = {};
+    dp.x = reinterpret_cast<const __half*>(x);
+    dp.w_router = reinterpret_cast<const __half*>(layer->w_router);
+    dp.B = B;
+    dp.d = layer->routed.d;
+    dp.f = layer->routed.f;
+    dp.k = k;
+    dp.renorm = layer->renorm ? 1 : 0;
+    dp.n_shared = layer->shared.E;
+    dp.routed = to_set(layer->routed);
+    if (layer->shared.E > 0) dp.shared = to_set(layer->shared);
+    dp.ctrl = at<Ctrl>(ws, L.ctrl);
+    dp.groups = at<GroupDesc>(ws, L.groups);
+    dp.kcol = at<int>(ws, L.item_col);
+    dp.kv = at<float>(ws, L.item_v);
+    dp.ucnt = at<uint8_t>(ws, L.unit_cnt);
+    dp.cta_total = at<int>(ws, L.cta_total);
+    dp.part = at<float>(ws, L.part);
+    dp.P = P;
+    dp.list_cap = cap;
+    dp.topk_idx = at<int32_t>(ws, L.topk_idx);
+    dp.topk_w = at<float>(ws, L.topk_w);
+    dp.user_idx = dbg ? dbg->topk_idx : nullptr;
+    dp.user_w = dbg ? dbg->topk_w : nullptr;
+    dp.n_slots = k + layer->shared.E;
+    dp.dbg_v = dbg ? dbg->v : nullptr;
+    dp.dbg_mask = dbg ? dbg->mask : nullptr;
+    dp.su = su;
+    dp.sr = sr;
+    dp.y = reinterpret_cast<__half*>(y);
+    dp.rmsnorm = rmsnorm_out ? 1 : 0;
+    dp.sumsq = at<float>(ws, L.sumsq);
+    dp.tok_ctr = at<int>(ws, L.tok_ctr);
+    // the router runs inside the up kernel: events 0 and 1 mark the same point
+    cudaError_t e = record(dbg, 0, st);
+    if (e == cudaSuccess) e = record(dbg, 1, st);
+    if (e == cudaSuccess) e = launch_decode_up(dp, st, true);
+    if (e == cudaSuccess) e = record(dbg, 2, st);
+    if (e == cudaSuccess) e = launch_decode_gather(dp, st, true);
+    if (e == cudaSuccess) e = record(dbg, 3, st);
+    if (e == cudaSuccess) e = launch_decode_combine(dp, st, true);
+    if (e == cudaSuccess) e = record(dbg, 4, st);
+    return cuda_status(e);
+  }
   RouteParams rp = {};
   rp.x = reinterpret_cast<const __half*>(x);
   rp.w_router = reinterpret_cast<const __half*>(layer->w_router);

@@ -44,6 +44,21 @@ __host__ __device__ inline size_t packed_bytes_per_expert(int d, int f) {
   return (size_t)(f / kMTile) * n_superblocks(d) * kBlkBytes;
 }
 
+// Codes of one block word as an mma A-operand register.
+template <int GI>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w) {
+  // Two 2-bit codes of group slot GI as an fp16x2 of subnormals q * 4^pos * 2^-24
+  // (exact); the power of two is removed after the mma.  Slots 5..7 sit above the
+  // 10-bit mantissa and are shifted down first.
+  if constexpr (GI < 5) return w & (0x00030003u << (2 * GI));
+  else return (w >> 10) & (0x00030003u << (2 * (GI - 5)));
+}
+
+__device__ __forceinline__ float pos_scale(int gi) {
+  const int pos = gi < 5 ? gi : gi - 5;
+  return __int_as_float((127 + 24 - 2 * pos) << 23);  // 2^(24 - 2 pos)
+}
+
 // Device copy of moe_experts_t.
 struct ExpertSet {
   int E, d, f;
@@ -52,6 +67,8 @@ struct ExpertSet {
   const __half* down;
   const float* thr;
   size_t up_stride;  // bytes per expert of the packed up projection
+  int rs;            // elements between consecutive gate (and down) rows: d, or 2d when
+                     // gate and down rows are interleaved in one buffer (down == gate_t + d)
 };
 
 // One unit of expert work: an expert and up to 8 of the tokens routed to it.
@@ -68,9 +85,10 @@ struct Ctrl {
   int status;        // first device-side error, MOE_OK if none
   int route_done;    // last-CTA counter of the router
   int G;             // number of groups of the current call
-  int pad0;
+  int work;          // next unclaimed unit of the decode kernel
   int N;             // total kept items of the current call (written by the gather kernel)
-  int pad1[3];
+  int work_done;     // decode CTAs that have claimed their last unit
+  int pad1[2];
 };
 
 __device__ inline void set_status(int* status, int code) { atomicCAS(status, 0, code); }
@@ -165,6 +183,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 

@@ -1,0 +1,1177 @@
+// Decode path for one or two tokens: the MoE layer of "FloE: On-the-Fly MoE
+// Inference on Memory-constrained GPU" (sec. 三 "系统协同优化", Algorithm 1
+// "Efficient Sparse Kernel" for every chosen expert) as three kernels chained by
+// programmatic dependent launch:
+//
+//   decode_up_kernel      one CTA per SM.  Routes the tokens (router GEMV from a copy
+//                         of the router weight fetched before the previous kernel
+//                         ends, softmax top-k, expert groups; every CTA redundantly,
+//                         the result is identical), then steps 1-2 of Algorithm 1 on a
+//                         fixed, equal share of the work units (16 output columns of
+//                         one expert): packed INT2 strips stream through a TMA ring;
+//                         16 warps, one 512-input superblock each, two units in
+//                         flight; the last warp of a unit to finish adds the
+//                         superblock partials, applies mask = |v| > t and writes the
+//                         unit's kept columns.
+//   decode_gather_kernel  one CTA per SM.  An equal share of all kept columns, in
+//                         (group, column) order: their gate and down rows stream
+//                         through a TMA ring; 16 warps form x . gate for a batch of
+//                         rows (one barrier per batch), h = SiLU(.) * v * router
+//                         weight, acc += h * down, and write the CTA's partial sum.
+//   decode_combine_kernel adds the partial sums in a fixed order, rounds to fp16 once
+//                         and applies the RMSNorm of stacked layers.
+//
+// Shares and orders are fixed, so the result is bitwise reproducible.  Every wait is
+// bounded; on expiry a CTA records MOE_ERR_TIMEOUT, stops, and waits (bounded) for
+// its copies in flight before it exits.
+#include "params.cuh"
+
+namespace sesg {
+
+namespace {
+
+constexpr int kDecMaxG = 24;     // groups: 2 tokens x 8 experts + 8 shared experts
+constexpr int kDecMaxE = 32;     // routed experts of the in-kernel router
+constexpr int kDecMaxSb = 8;     // superblocks of 512 inputs (d <= 4096)
+constexpr int kDecNV = 4;        // unit slots of superblock partials (a power of two)
+constexpr int kDecMaxSu = 12;    // up-ring stages
+constexpr int kDecMaxSr = 16;    // row-ring stages
+constexpr int kDecMaxUnits = 128;  // units per CTA
+constexpr int kDecRows = 4;      // kept rows per gather batch
+constexpr int kDecMaxGw = 16;    // gather warps
+constexpr int kUpThreads = 2 * kDecMaxSb * 32;
+constexpr int kGaThreads = kDecMaxGw * 32;
+constexpr int kDecMaxD = 4096;
+constexpr int kCombCols = 32;    // hidden elements per combine CTA
+constexpr int kCombThr = 256;
+
+__host__ __device__ inline size_t al16(size_t o) { return (o + 15) & ~(size_t)15; }
+
+// ---- up kernel shared memory
+struct UpMisc {
+  int abort;
+  int G;
+  int ucnt[kDecNV];            // superblock partials written for the unit in the slot
+  int pend[kDecMaxSu];         // strip in flight in the stage (issue index + 1) or 0
+  int scnt[kDecMaxUnits];      // kept columns of this CTA's units
+  float logits[2][kDecMaxE];
+  int tidx[2][kMaxTok];
+  float tw[2][kMaxTok];
+  float vbuf[kDecNV][16 * 2];
+};
+
+struct UpLayoutD {
+  int nsb, nwarps, su;
+  size_t strip, wr_bytes, ring;
+  size_t off_bar, off_misc, off_ring, off_x, off_vpart, off_xg, off_grp, off_lred, total;
+};
+
+__host__ __device__ inline UpLayoutD up_layout_d(int d, int B, int E, int su) {
+  UpLayoutD L;
+  L.nsb = n_superblocks(d);
+  L.nwarps = 2 * L.nsb;
+  L.su = su;
+  L.strip = (size_t)L.nsb * kBlkBytes;
+  L.wr_bytes = (size_t)d * E * 2;
+  L.ring = L.strip * su;
+  if (L.ring < L.wr_bytes) L.ring = L.wr_bytes;
+  size_t o = 0;
+  L.off_bar = o;
+  o += 8 * (size_t)(kDecMaxSu + kDecNV + 1);
+  o = al16(o);
+  L.off_misc = o;
+  o += al16(sizeof(UpMisc));
+  o = (o + 127) & ~(size_t)127;
+  L.off_ring = o;
+  o += al16(L.ring);
+  L.off_x = o;
+  o += al16((size_t)B * d * 2);
+  L.off_vpart = o;
+  o += (size_t)kDecNV * L.nsb * 32 * 16;
+  L.off_xg = o;
+  o += (size_t)2 * L.nsb * 16 * 4;
+  L.off_grp = o;
+  o += al16(sizeof(GroupDesc) * kDecMaxG);
+  L.off_lred = o;
+  o += (size_t)L.nwarps * 2 * kDecMaxE * 4;
+  L.total = o;
+  return L;
+}
+
+// ---- gather kernel shared memory
+struct GaRow {
+  int col;    // kept column
+  int g;      // group
+  float v[2]; // v per group token (0 where that token drops the column)
+};
+
+struct GaMisc {
+  int abort;
+  int G;
+  int c0, c1;                  // up CTAs whose units hold this CTA's rows
+  int issued;                  // rows issued (0 .. issued-1)
+  int consumed;                // rows whose stages are free again
+  int tmap[kDecMaxG][2];       // group token of batch token b, -1 if none
+  float tw[kDecMaxG][2];       // its combine weight
+};
+
+struct GaLayoutD {
+  int ngw, nwarps, sr, cap;
+  size_t row;
+  size_t off_bar, off_misc, off_ring, off_list, off_red, off_pre, off_scan, off_grp, total;
+};
+
+__host__ __device__ inline GaLayoutD ga_layout_d(int d, int sr, int cap, int P) {
+  GaLayoutD L;
+  L.ngw = d / 256;
+  L.nwarps = L.ngw;
+  L.sr = sr;
+  L.cap = cap;
+  L.row = (size_t)4 * d;
+  size_t o = 0;
+  L.off_bar = o;
+  o += 8 * (size_t)kDecMaxSr;
+  o = al16(o);
+  L.off_misc = o;
+  o += al16(sizeof(GaMisc));
+  o = (o + 127) & ~(size_t)127;
+  L.off_ring = o;
+  o += L.row * sr;
+  L.off_list = o;
+  o += sizeof(GaRow) * (size_t)cap;
+  L.off_red = o;
+  o += (size_t)2 * kDecRows * 2 * kDecMaxGw * 4;
+  L.off_pre = o;
+  o += al16(4 * ((size_t)P + 1));
+  L.off_scan = o;
+  o += al16(4 * ((size_t)kGaThreads + 1));
+  L.off_grp = o;
+  o += al16(sizeof(GroupDesc) * kDecMaxG);
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ const ExpertSet& dec_set(const DecodeParams& p, int expert, int& local) {
+  if (expert < p.routed.E) {
+    local = expert;
+    return p.routed;
+  }
+  local = expert - p.routed.E;
+  return p.shared;
+}
+
+__device__ __forceinline__ int vload(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+
+__device__ __forceinline__ void dec_fail(const DecodeParams& p, int* abort_flag) {
+  set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
+  atomicExch(abort_flag, 1);
+}
+
+// SiLU with the fast division (2 ulp): g / (1 + e^-g)
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+__device__ __forceinline__ long long muldiv(long long a, long long b, long long c) { return a * b / c; }
+
+// ---------------------------------------------------------------------------
+// Routing (all threads of the CTA): logits, softmax top-k, groups.  Ties between
+// equal logits go to the lower expert index; groups are the chosen experts in
+// ascending order, each with its tokens in ascending order, then the shared experts.
+// wr: the router weight [d][E], in shared memory.
+// ---------------------------------------------------------------------------
+template <int B>
+__device__ void dec_route(const DecodeParams& p, int nthreads, const __half* wr, const __half* xs,
+                          float* lred, UpMisc* m, GroupDesc* grp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = nthreads / 32;
+  const int E = p.routed.E, d = p.d, k = p.k;
+  const int nchunk = E / 8;
+  const int ec = tid % nchunk, rs = tid / nchunk, nrs = nthreads / nchunk;
+  float acc[B][8];
+#pragma unroll
+  for (int b = 0; b < B; ++b)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[b][i] = 0.f;
+  constexpr int RU = 8;
+  for (int r0 = rs; r0 < d; r0 += RU * nrs) {
+    uint4 wv[RU];
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      const int r = r0 + u * nrs;
+      wv[u] = r < d ? *reinterpret_cast<const uint4*>(wr + (size_t)r * E + ec * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      const int r = r0 + u * nrs;
+      if (r < d) {
+        const __half2* h2 = reinterpret_cast<const __half2*>(&wv[u]);
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+          const float xv = __half2float(xs[(size_t)b * d + r]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 wf = __half22float2(h2[i]);
+            acc[b][2 * i] = fmaf(xv, wf.x, acc[b][2 * i]);
+            acc[b][2 * i + 1] = fmaf(xv, wf.y, acc[b][2 * i + 1]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < B; ++b)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float v = acc[b][i];
+      for (int off = 16; off >= nchunk; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane < nchunk) lred[(warp * B + b) * kDecMaxE + lane * 8 + i] = v;
+    }
+  __syncthreads();
+  for (int t = tid; t < B * E; t += nthreads) {
+    const int b = t / E, e = t % E;
+    float s = 0.f;
+    for (int w = 0; w < nw; ++w) s += lred[(w * B + b) * kDecMaxE + e];
+    m->logits[b][e] = s;
+  }
+  __syncthreads();
+  if (warp < B) {
+    const int b = warp;
+    const float l = lane < E ? m->logits[b][lane] : -INFINITY;
+    bool taken = lane >= E;
+    float sel_l[kMaxTok];
+    int sel_i[kMaxTok];
+#pragma unroll
+    for (int j = 0; j < kMaxTok; ++j) {
+      sel_l[j] = 0.f;
+      sel_i[j] = 0;
+      if (j < k) {
+        float best = taken ? -INFINITY : l;
+        int bi = taken ? 0x7fffffff : lane;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+          if (ob > best || (ob == best && oi < bi)) {
+            best = ob;
+            bi = oi;
+          }
+        }
+        if (lane == bi) taken = true;
+        sel_l[j] = best;
+        sel_i[j] = bi;
+      }
+    }
+    const float lmax = sel_l[0];
+    float denom = 0.f;
+    if (p.renorm) {
+#pragma unroll
+      for (int j = 0; j < kMaxTok; ++j)
+        if (j < k) denom += expf(sel_l[j] - lmax);
+    } else {
+      float part = lane < E ? expf(l - lmax) : 0.f;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      denom = part;
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < kMaxTok; ++j) {
+        if (j < k) {
+          const float w = expf(sel_l[j] - lmax) / denom;
+          m->tidx[b][j] = sel_i[j];
+          m->tw[b][j] = w;
+          if (blockIdx.x == 0) {
+            p.topk_idx[b * k + j] = sel_i[j];
+            p.topk_w[b * k + j] = w;
+            if (p.user_idx) p.user_idx[b * k + j] = sel_i[j];
+            if (p.user_w) p.user_w[b * k + j] = w;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int np = B * k;
+    int e = -1, bb = 0, jj = 0;
+    float ww = 0.f;
+    if (lane < np) {
+      bb = lane / k;
+      jj = lane % k;
+      e = m->tidx[bb][jj];
+      ww = m->tw[bb][jj];
+    }
+    bool first = lane < np;
+    int pos = 0, cnt = 0;
+    for (int q = 0; q < np; ++q) {
+      const int eq = __shfl_sync(0xffffffffu, e, q), bq = __shfl_sync(0xffffffffu, bb, q);
+      if (lane < np && eq == e) {
+        ++cnt;
+        if (bq < bb) {
+          first = false;
+          ++pos;
+        }
+      }
+    }
+    const unsigned fm = __ballot_sync(0xffffffffu, first);
+    int gi = 0;
+    for (int q = 0; q < np; ++q) {
+      const int eq = __shfl_sync(0xffffffffu, e, q);
+      if (((fm >> q) & 1u) && eq < e) ++gi;
+    }
+    const int GR = __popc(fm);
+    if (lane < np) {
+      GroupDesc& gd = grp[gi];
+      gd.tok[pos] = bb;
+      gd.slot[pos] = jj;
+      gd.w[pos] = ww;
+      if (first) {
+        gd.expert = e;
+        gd.n_tok = cnt;
+        for (int t = cnt; t < kMaxTok; ++t) {
+          gd.tok[t] = 0;
+          gd.slot[t] = 0;
+          gd.w[t] = 0.f;
+        }
+      }
+    }
+    if (lane < p.n_shared) {
+      GroupDesc& gd = grp[GR + lane];
+      gd.expert = E + lane;
+      gd.n_tok = B;
+      for (int t = 0; t < kMaxTok; ++t) {
+        gd.tok[t] = t < B ? t : 0;
+        gd.slot[t] = t < B ? k + lane : 0;
+        gd.w[t] = t < B ? 1.f : 0.f;
+      }
+    }
+    if (lane == 0) m->G = GR + p.n_shared;
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Up projection of one superblock (one warp).
+//
+// Tensor-core mapping as in the up kernel of the general path: M = 16 output
+// columns, K = 16 inputs, N = 8 slots; slot n is (token n / G, class n % G) with
+// G = 8 / T classes, and a k-step of quantiser group gi feeds only the slots of
+// class gi % G.  A lane supplies B column gl, so it only ever holds x of its own
+// token and class: T x 4 k-steps x 2 registers, selected (or zeroed) per mma.
+// ---------------------------------------------------------------------------
+template <int T>
+__device__ __forceinline__ void dec_up_setup(const __half* xs, int d, const GroupDesc& gd, int sb,
+                                             int ng, uint32_t (&xr)[T][4][2], float* xgw) {
+  constexpr int G = 8 / T;
+  const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
+  const int tau = gl / G, cl = gl % G;
+  const int n_tok = gd.n_tok;
+#pragma unroll
+  for (int jj = 0; jj < T; ++jj) {
+    const int gi = cl + G * jj;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      uint32_t b0 = 0, b1 = 0;
+      if (tau < n_tok && gi < ng) {
+        const __half* xp = xs + (size_t)gd.tok[tau] * d + sb * kSuper + gi * kGroup + 16 * t + 2 * c;
+        b0 = *reinterpret_cast<const uint32_t*>(xp);
+        b1 = *reinterpret_cast<const uint32_t*>(xp + 8);
+      }
+      xr[jj][t][0] = b0;
+      xr[jj][t][1] = b1;
+    }
+  }
+  // X[tau][gi] = sum of x over quantiser group gi of this superblock (4 / T lanes each)
+  constexpr int LPS = 4 / T;
+  const int q = lane / LPS, part = lane % LPS;
+  const int qt = q / 8, qg = q % 8;
+  float s = 0.f;
+  if (qt < n_tok && qg < ng) {
+    const uint4* src = reinterpret_cast<const uint4*>(xs + (size_t)gd.tok[qt] * d + sb * kSuper +
+                                                      qg * kGroup + part * (16 * T));
+#pragma unroll
+    for (int mm = 0; mm < 2 * T; ++mm) {
+      const uint4 v = src[mm];
+      const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f2 = __half22float2(h2[e]);
+        s += f2.x;
+        s += f2.y;
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 1; off < LPS; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (part == 0) xgw[qt * 8 + qg] = s;
+  __syncwarp();
+}
+
+template <int T, int PH, int GAM>
+__device__ __forceinline__ void dec_groups(const uint4 (&w)[4], const uint32_t (&xr)[T][4][2],
+                                           int cl, float (&D)[4][4], int ng) {
+  constexpr int G = 8 / T;
+  if constexpr (GAM < G) {
+    constexpr int GI = PH * G + GAM;
+    if (GI < ng) {
+      const bool on = cl == GAM;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        uint32_t a[4];
+        a[0] = code_pair<GI>(w[t].x);
+        a[1] = code_pair<GI>(w[t].y);
+        a[2] = code_pair<GI>(w[t].z);
+        a[3] = code_pair<GI>(w[t].w);
+        mma_16816(D[t], a, on ? xr[PH][t][0] : 0u, on ? xr[PH][t][1] : 0u);
+      }
+    }
+    dec_groups<T, PH, GAM + 1>(w, xr, cl, D, ng);
+  }
+}
+
+template <int T, int PH>
+__device__ __forceinline__ void dec_phases(const uint4 (&w)[4], const uint32_t (&xr)[T][4][2],
+                                           const uint8_t* __restrict__ szt, const float* xgw,
+                                           int ng, float (&vacc)[2][2]) {
+  if constexpr (PH < T) {
+    constexpr int G = 8 / T;
+    const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
+    float D[4][4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) D[t][0] = D[t][1] = D[t][2] = D[t][3] = 0.f;
+    dec_groups<T, PH, 0>(w, xr, gl % G, D, ng);
+    const int gi_lane = (2 * c) % G, tau = (2 * c) / G;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int gi = PH * G + gi_lane + s;
+      if (gi < ng) {
+        const float cs = pos_scale(gi);
+        const float X = xgw[tau * 8 + gi];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const __half2 h = *reinterpret_cast<const __half2*>(szt + ((gl + 8 * r) * 8 + gi) * 4);
+          const float sf = __low2float(h), zf = __high2float(h);
+          const float acc = (D[0][2 * r + s] + D[1][2 * r + s]) + (D[2][2 * r + s] + D[3][2 * r + s]);
+          vacc[r][s] = fmaf(sf, fmaf(-zf, X, acc * cs), vacc[r][s]);
+        }
+      }
+    }
+    dec_phases<T, PH + 1>(w, xr, szt, xgw, ng, vacc);
+  }
+}
+
+template <int T>
+__device__ __forceinline__ void dec_superblock(const uint8_t* __restrict__ blk,
+                                               const uint32_t (&xr)[T][4][2], const float* xgw,
+                                               int ng, float (&vacc)[2][2]) {
+  const int lane = threadIdx.x & 31;
+  uint4 w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) w[q] = reinterpret_cast<const uint4*>(blk)[q * 32 + lane];
+  dec_phases<T, 0>(w, xr, blk + kBlkCodeBytes, xgw, ng, vacc);
+}
+
+// The superblock partials of one unit added in a fixed order, per-token v of its 16
+// columns, mask = |v| > t (union over the group's tokens) and the unit's kept list:
+// kcol[u][rank] (ascending columns), kv[u][rank][t] (0 for a token that drops the
+// column), ucnt[u].  Returns the number of kept columns.
+template <int T>
+__device__ int dec_finalize(const DecodeParams& p, const float4* vpart, int nsb, const GroupDesc& gd,
+                            int u, int mt, float thr, float* vbuf) {
+  constexpr int G = 8 / T;
+  const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
+  float v00 = 0.f, v01 = 0.f, v10 = 0.f, v11 = 0.f;
+  for (int q = 0; q < nsb; ++q) {
+    const float4 pv = vpart[q * 32 + lane];
+    v00 += pv.x;
+    v01 += pv.y;
+    v10 += pv.z;
+    v11 += pv.w;
+  }
+  float v0 = v00 + v01, v1 = v10 + v11;
+  if constexpr (G >= 4) {
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+  }
+  if constexpr (G == 8) {
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+  }
+  const int tau = (2 * c) / G;
+  if ((c % (G / 2)) == 0) {
+    vbuf[gl * 2 + tau] = v0;
+    vbuf[(gl + 8) * 2 + tau] = v1;
+  }
+  __syncwarp();
+  float vv[T];
+  uint32_t mbits = 0;
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    vv[t] = 0.f;
+    if (t < gd.n_tok && lane < 16) {
+      vv[t] = vbuf[lane * 2 + t];
+      if (fabsf(vv[t]) > thr) mbits |= 1u << t;
+    }
+  }
+  __syncwarp();
+  const uint32_t bal = __ballot_sync(0xffffffffu, mbits != 0);
+  if (mbits) {
+    const int rank = __popc(bal & ((1u << lane) - 1u));
+    const size_t e = (size_t)u * 16 + rank;
+    p.kcol[e] = mt * kMTile + lane;
+    float2 kv;
+    kv.x = (mbits & 1u) ? vv[0] : 0.f;
+    kv.y = (T > 1 && ((mbits >> 1) & 1u)) ? vv[T > 1 ? 1 : 0] : 0.f;
+    reinterpret_cast<float2*>(p.kv)[e] = kv;
+  }
+  const int cnt = __popc(bal);
+  if (lane == 0) p.ucnt[u] = (uint8_t)cnt;
+  if (p.dbg_v || p.dbg_mask) {
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      if (t < gd.n_tok) {
+        const size_t row = (size_t)gd.tok[t] * p.n_slots + gd.slot[t];
+        if (p.dbg_v && lane < 16) p.dbg_v[row * p.f + mt * kMTile + lane] = vv[t];
+        const uint32_t mb = __ballot_sync(0xffffffffu, (mbits >> t) & 1u) & 0xffffu;
+        if (p.dbg_mask && lane == 0)
+          reinterpret_cast<uint16_t*>(p.dbg_mask)[row * (size_t)(2 * ((p.f + 31) / 32)) + mt] =
+              (uint16_t)mb;
+      }
+    }
+  }
+  return cnt;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Up kernel.  B = tokens (1 or 2), also the group width of the tensor-core mapping.
+// ---------------------------------------------------------------------------
+template <int B>
+__global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t usm[];
+  const int d = p.d, SU = p.su;
+  const UpLayoutD L = up_layout_d(d, B, p.routed.E, SU);
+  uint64_t* full = reinterpret_cast<uint64_t*>(usm + L.off_bar);
+  uint64_t* vfree = full + kDecMaxSu;
+  uint64_t* wbar = vfree + kDecNV;
+  UpMisc* m = reinterpret_cast<UpMisc*>(usm + L.off_misc);
+  uint8_t* ring = usm + L.off_ring;
+  __half* xs = reinterpret_cast<__half*>(usm + L.off_x);
+  float4* vpart = reinterpret_cast<float4*>(usm + L.off_vpart);
+  float* xg = reinterpret_cast<float*>(usm + L.off_xg);
+  GroupDesc* grp = reinterpret_cast<GroupDesc*>(usm + L.off_grp);
+  float* lred = reinterpret_cast<float*>(usm + L.off_lred);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nsb = L.nsb, nthreads = L.nwarps * 32;
+  if (tid == 0) {
+    for (int s = 0; s < SU; ++s) mbar_init(&full[s], 1);
+    for (int v = 0; v < kDecNV; ++v) mbar_init(&vfree[v], 1);
+    mbar_init(wbar, 1);
+    fence_barrier_init();
+    // the router weight is not written by the previous kernel: fetch it before waiting
+    mbar_arrive_expect_tx(wbar, (uint32_t)L.wr_bytes);
+    for (size_t o = 0; o < L.wr_bytes; o += 32768) {
+      const size_t n = L.wr_bytes - o < 32768 ? L.wr_bytes - o : 32768;
+      bulk_g2s(ring + o, reinterpret_cast<const uint8_t*>(p.w_router) + o, (uint32_t)n, wbar,
+               policy_evict_last());
+    }
+    m->abort = 0;
+    for (int v = 0; v < kDecNV; ++v) m->ucnt[v] = 0;
+    for (int s = 0; s < kDecMaxSu; ++s) m->pend[s] = 0;
+  }
+  __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+  for (int i = tid; i < B * d / 8; i += nthreads)
+    reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
+  const bool wok = mbar_wait(wbar, 0);
+  if (__syncthreads_or(!wok)) {
+    if (tid == 0) {
+      set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
+      (void)mbar_wait(wbar, 0);
+    }
+    return;
+  }
+  dec_route<B>(p, nthreads, reinterpret_cast<const __half*>(ring), xs, lred, m, grp);
+  const int G = m->G;
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < G * (int)(sizeof(GroupDesc) / 4); i += nthreads)
+      reinterpret_cast<int*>(p.groups)[i] = reinterpret_cast<const int*>(grp)[i];
+    if (tid == 0) p.ctrl->G = G;
+  }
+  // the ring held the router weight (generic reads); the strips are written by TMA
+  fence_proxy_async_smem();
+  __syncthreads();
+  const int MT = p.f / kMTile;
+  const int U = G * MT;
+  const int u0 = (int)muldiv(U, blockIdx.x, gridDim.x), u1 = (int)muldiv(U, blockIdx.x + 1, gridDim.x);
+  const int n = u1 - u0;
+
+  const uint64_t pol = policy_evict_first();
+  // strip of unit j of this CTA into its stage
+  auto issue = [&](int j) {
+    const int s = j % SU, u = u0 + j, g = u / MT, mt = u - g * MT;
+    int el;
+    const ExpertSet& es = dec_set(p, grp[g].expert, el);
+    m->pend[s] = j + 1;
+    mbar_arrive_expect_tx(&full[s], (uint32_t)L.strip);
+    bulk_g2s(ring + (size_t)s * L.strip, es.up + (size_t)el * es.up_stride + (size_t)mt * L.strip,
+             (uint32_t)L.strip, &full[s], pol);
+  };
+  if (tid == 0)
+    for (int j = 0; j < min(n, SU); ++j) issue(j);
+  {
+    // ---- up warps: unit lane ug (units j = ug, ug + 2, ...), superblock sb.  No
+    // producer warp: the last warp to finish a unit refills its stage.
+    const int uw = warp, ug = uw / nsb, sb = uw % nsb;
+    const int ng = min(8, (d - sb * kSuper) / kGroup);
+    float* xgw = xg + uw * 16;
+    uint32_t xr[B][4][2];
+    int cur_g = -1;
+    float thr = 0.f;
+    // stage s = j % SU with full-barrier parity ph = (j / SU) & 1, and unit u = u0 + j as
+    // (group g, M-tile mt), all advanced by 2 units per iteration without divisions
+    int s = ug % SU, ph = (ug / SU) & 1;
+    int g = (u0 + ug) / MT, mt = (u0 + ug) - g * MT;
+    for (int j = ug; j < n; j += 2) {
+      const int slot = j & (kDecNV - 1);
+      const bool ab = vload(&m->abort) != 0;
+      bool ok = __all_sync(0xffffffffu, !ab && mbar_wait(&full[s], ph));
+      if (!ok) {
+        if (!ab && lane == 0) dec_fail(p, &m->abort);
+        break;
+      }
+      const int u = u0 + j;
+      if (g != cur_g) {
+        int el;
+        const ExpertSet& es = dec_set(p, grp[g].expert, el);
+        thr = es.thr[el];
+        dec_up_setup<B>(xs, d, grp[g], sb, ng, xr, xgw);
+        cur_g = g;
+      }
+      float vacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      dec_superblock<B>(ring + (size_t)s * L.strip + (size_t)sb * kBlkBytes, xr, xgw, ng, vacc);
+      // the slot's previous unit must have been finalized
+      if (j >= kDecNV &&
+          !__all_sync(0xffffffffu, mbar_wait(&vfree[slot], ((j >> 2) - 1) & 1))) {
+        if (lane == 0) dec_fail(p, &m->abort);
+        break;
+      }
+      vpart[((size_t)slot * nsb + sb) * 32 + lane] = make_float4(vacc[0][0], vacc[0][1], vacc[1][0], vacc[1][1]);
+      __syncwarp();
+      int prev = 0;
+      if (lane == 0) {
+        __threadfence_block();
+        prev = atomicAdd(&m->ucnt[slot], 1);
+      }
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      __syncwarp();
+      if (prev == nsb - 1) {
+        // last superblock of the unit: the stage is free, and this warp finalizes the unit
+        __threadfence_block();
+        if (lane == 0) {
+          m->ucnt[slot] = 0;
+          m->pend[s] = 0;
+          if (j + SU < n && !vload(&m->abort)) {
+            fence_proxy_async_smem();
+            issue(j + SU);
+          }
+        }
+        const int cnt = dec_finalize<B>(p, vpart + (size_t)slot * nsb * 32, nsb, grp[g], u, mt,
+                                        thr, m->vbuf[slot]);
+        if (lane == 0) m->scnt[j] = cnt;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&vfree[slot]);
+      }
+      s += 2;
+      if (s >= SU) {
+        s -= SU;
+        ph ^= 1;
+      }
+      mt += 2;
+      while (mt >= MT) {
+        mt -= MT;
+        ++g;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    if (m->abort) {
+      // wait (bounded) for the strips still in flight before the CTA exits
+      for (int s = 0; s < SU; ++s) {
+        const int q = m->pend[s];
+        if (q > 0) (void)mbar_wait(&full[s], ((q - 1) / SU) & 1);
+      }
+    }
+    int tot = 0;
+    for (int j = 0; j < n; ++j) tot += m->scnt[j];
+    p.cta_total[blockIdx.x] = tot;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Gather kernel.  No producer warp: thread 0 issues the first ring fill, and after the
+// barrier of every batch (when all warps are done with the previous batch) it issues
+// the rows that reuse the freed stages.  A kept column whose gate and down rows are
+// interleaved in one buffer costs one 4d-byte copy, else two 2d-byte copies.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ga_issue(const DecodeParams& p, const GaRow* list, const GroupDesc* grp,
+                                         uint8_t* ring, uint64_t* full, int i, int SR, size_t row,
+                                         int d, uint64_t pol) {
+  const GaRow gr = list[i];
+  int el;
+  const ExpertSet& es = dec_set(p, grp[gr.g].expert, el);
+  const size_t roff = ((size_t)el * es.f + gr.col) * es.rs;
+  const int s = i % SR;
+  uint8_t* st = ring + (size_t)s * row;
+  mbar_arrive_expect_tx(&full[s], (uint32_t)row);
+  if (es.rs == 2 * d) {
+    bulk_g2s(st, es.gate_t + roff, (uint32_t)(4 * d), &full[s], pol);
+  } else {
+    bulk_g2s(st, es.gate_t + roff, (uint32_t)(2 * d), &full[s], pol);
+    bulk_g2s(st + 2 * d, es.down + roff, (uint32_t)(2 * d), &full[s], pol);
+  }
+}
+
+template <int B>
+__global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t gsm[];
+  const int d = p.d, SR = p.sr, P = gridDim.x;
+  const GaLayoutD L = ga_layout_d(d, SR, p.list_cap, P);
+  uint64_t* full = reinterpret_cast<uint64_t*>(gsm + L.off_bar);
+  GaMisc* m = reinterpret_cast<GaMisc*>(gsm + L.off_misc);
+  uint8_t* ring = gsm + L.off_ring;
+  GaRow* list = reinterpret_cast<GaRow*>(gsm + L.off_list);
+  float* red = reinterpret_cast<float*>(gsm + L.off_red);
+  int* pre = reinterpret_cast<int*>(gsm + L.off_pre);
+  int* scan = reinterpret_cast<int*>(gsm + L.off_scan);
+  GroupDesc* grp = reinterpret_cast<GroupDesc*>(gsm + L.off_grp);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ngw = L.ngw, nthreads = ngw * 32;
+  if (tid == 0) {
+    for (int s = 0; s < SR; ++s) mbar_init(&full[s], 1);
+    fence_barrier_init();
+    m->abort = 0;
+    m->issued = 0;
+    m->consumed = 0;
+  }
+  for (int i = tid; i < 2 * kDecRows * 2 * kDecMaxGw; i += nthreads) red[i] = 0.f;
+  // this thread's 8 hidden elements of the tokens (x precedes the up kernel)
+  float xf[B][8];
+#pragma unroll
+  for (int b = 0; b < B; ++b) {
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)b * d) + tid);
+    const __half2* h2 = reinterpret_cast<const __half2*>(&xv);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f2 = __half22float2(h2[e]);
+      xf[b][2 * e] = f2.x;
+      xf[b][2 * e + 1] = f2.y;
+    }
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+
+  // ---- prologue: this CTA's rows [a, bnd) of the kept columns in unit order
+  if (tid < 32) {
+    int carry = 0;
+    for (int base = 0; base < P; base += 32) {
+      const int c = base + lane;
+      const int v = c < P ? __ldcg(p.cta_total + c) : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (c < P) pre[c] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      pre[P] = carry;
+      m->G = __ldcg(&p.ctrl->G);
+    }
+  }
+  __syncthreads();
+  const int N = pre[P], G = m->G;
+  for (int i = tid; i < G * (int)(sizeof(GroupDesc) / 4); i += nthreads)
+    reinterpret_cast<int*>(grp)[i] = __ldcg(reinterpret_cast<const int*>(p.groups) + i);
+  const int MT = p.f / kMTile, U = G * MT;
+  const int a = (int)muldiv(N, blockIdx.x, P), bnd = (int)muldiv(N, blockIdx.x + 1, P);
+  const int nrows = bnd - a;
+  // up CTAs whose units hold rows [a, bnd): the last c with pre[c] <= a, the last with pre[c] < bnd
+  for (int c = tid; c < P; c += nthreads) {
+    if (pre[c] <= a && (c + 1 == P || pre[c + 1] > a)) m->c0 = c;
+    if (pre[c] < bnd && (c + 1 == P || pre[c + 1] >= bnd)) m->c1 = c;
+  }
+  __syncthreads();
+  if (tid < G * 2) {
+    const int g = tid >> 1, b = tid & 1;
+    const GroupDesc& gd = grp[g];
+    int t_of_b = -1;
+    float w = 0.f;
+    for (int t = 0; t < gd.n_tok; ++t)
+      if (gd.tok[t] == b) {
+        t_of_b = t;
+        w = gd.w[t];
+      }
+    m->tmap[g][b] = t_of_b;
+    m->tw[g][b] = w;
+  }
+  if (nrows > 0) {
+    // candidate units, nthreads at a time: counts, prefix, then 16 lanes per unit copy
+    // the unit's rows that fall in [a, bnd)
+    const int c0 = m->c0, c1 = max(m->c0, m->c1);
+    const int v0 = (int)muldiv(U, c0, P), v1 = (int)muldiv(U, c1 + 1, P);
+    int run = pre[c0];
+    for (int base = v0; base < v1; base += nthreads) {
+      const int u = base + tid;
+      scan[tid] = u < v1 ? (int)__ldcg(p.ucnt + u) : 0;
+      __syncthreads();
+      if (tid < 32) {
+        int carry = 0;
+        for (int o = 0; o < nthreads; o += 32) {
+          const int v = scan[o + lane];
+          int incl = v;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += t;
+          }
+          scan[o + lane] = carry + incl - v;
+          carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) scan[nthreads] = carry;
+      }
+      __syncthreads();
+      const int nu = min(nthreads, v1 - base);
+      for (int q = tid; q < nu * 16; q += nthreads) {
+        const int k = q >> 4, r = q & 15;
+        const int cnt = scan[k + 1] - scan[k];
+        const int row = run + scan[k] + r;
+        if (r < cnt && row >= a && row < bnd) {
+          const size_t e = (size_t)(base + k) * 16 + r;
+          GaRow gr;
+          gr.col = __ldcg(p.kcol + e);
+          gr.g = (base + k) / MT;
+          const float2 kv = __ldcg(reinterpret_cast<const float2*>(p.kv) + e);
+          gr.v[0] = kv.x;
+          gr.v[1] = kv.y;
+          list[row - a] = gr;
+        }
+      }
+      run += scan[nthreads];
+      __syncthreads();
+    }
+  }
+  __syncthreads();
+  const uint64_t pol = policy_evict_first();
+  if (tid == 0) {
+    const int n0 = min(nrows, SR);
+    for (int i = 0; i < n0; ++i) ga_issue(p, list, grp, ring, full, i, SR, L.row, d, pol);
+    m->issued = n0;
+  }
+
+  // ---- batches of up to kDecRows rows, one barrier per batch
+  float acc[B][8];
+#pragma unroll
+  for (int b = 0; b < B; ++b)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[b][e] = 0.f;
+  int batch = 0;
+  int s0 = 0, ph0 = 0;  // stage and full-barrier parity of row i0
+  for (int i0 = 0; i0 < nrows; i0 += kDecRows, ++batch) {
+    const int nb = min(kDecRows, nrows - i0);
+    int st[kDecRows];
+    bool ok = !vload(&m->abort);
+#pragma unroll
+    for (int q = 0; q < kDecRows; ++q) {
+      int sq = s0 + q, pq = ph0;
+      if (sq >= SR) {
+        sq -= SR;
+        pq ^= 1;
+      }
+      st[q] = sq;
+      if (q < nb) ok = ok && mbar_wait(&full[sq], pq);
+    }
+    s0 += kDecRows;
+    if (s0 >= SR) {
+      s0 -= SR;
+      ph0 ^= 1;
+    }
+    float dot[kDecRows][B];
+#pragma unroll
+    for (int q = 0; q < kDecRows; ++q) {
+#pragma unroll
+      for (int b = 0; b < B; ++b) dot[q][b] = 0.f;
+      if (q < nb && ok) {
+        const uint4 gr = reinterpret_cast<const uint4*>(ring + (size_t)st[q] * L.row)[tid];
+        const __half2* gh = reinterpret_cast<const __half2*>(&gr);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 gf = __half22float2(gh[e]);
+#pragma unroll
+          for (int b = 0; b < B; ++b) {
+            dot[q][b] = fmaf(xf[b][2 * e], gf.x, dot[q][b]);
+            dot[q][b] = fmaf(xf[b][2 * e + 1], gf.y, dot[q][b]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+      for (int q = 0; q < kDecRows; ++q)
+#pragma unroll
+        for (int b = 0; b < B; ++b) dot[q][b] += __shfl_xor_sync(0xffffffffu, dot[q][b], off);
+    float* rb = red + (size_t)(batch & 1) * kDecRows * 2 * kDecMaxGw;
+    if (lane == 0) {
+#pragma unroll
+      for (int q = 0; q < kDecRows; ++q)
+#pragma unroll
+        for (int b = 0; b < B; ++b) rb[(q * 2 + b) * kDecMaxGw + warp] = dot[q][b];
+    }
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) dec_fail(p, &m->abort);
+      break;
+    }
+    if (tid == 0) {
+      // every warp is done with the previous batch: refill its stages
+      m->consumed = i0;
+      fence_proxy_async_smem();
+      const int hi = min(nrows, i0 + SR);
+      for (int i = m->issued; i < hi; ++i) ga_issue(p, list, grp, ring, full, i, SR, L.row, d, pol);
+      if (hi > m->issued) m->issued = hi;
+    }
+    float h[kDecRows][B];
+#pragma unroll
+    for (int q = 0; q < kDecRows; ++q) {
+      const GaRow gr = list[min(i0 + q, nrows - 1)];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        h[q][b] = 0.f;
+        const int t = m->tmap[gr.g][b];
+        if (q < nb && t >= 0) {
+          const float4* pr = reinterpret_cast<const float4*>(rb + (q * 2 + b) * kDecMaxGw);
+          const float4 p0 = pr[0], p1 = pr[1], p2 = pr[2], p3 = pr[3];  // unused slots hold 0
+          const float gs = (((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w))) +
+                           (((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w)));
+          h[q][b] = silu_fast(gs) * (t == 0 ? gr.v[0] : gr.v[1]) * m->tw[gr.g][b];
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kDecRows; ++q) {
+      if (q < nb) {
+        const uint4 dr = reinterpret_cast<const uint4*>(ring + (size_t)st[q] * L.row + 2 * d)[tid];
+        const __half2* dh = reinterpret_cast<const __half2*>(&dr);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 df = __half22float2(dh[e]);
+#pragma unroll
+          for (int b = 0; b < B; ++b) {
+            acc[b][2 * e] = fmaf(h[q][b], df.x, acc[b][2 * e]);
+            acc[b][2 * e + 1] = fmaf(h[q][b], df.y, acc[b][2 * e + 1]);
+          }
+        }
+      }
+    }
+  }
+  // this CTA's partial output (every CTA writes one, zeros if it had no rows)
+#pragma unroll
+  for (int b = 0; b < B; ++b) {
+    float4* dst = reinterpret_cast<float4*>(p.part + ((size_t)blockIdx.x * B + b) * d + tid * 8);
+    dst[0] = make_float4(acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
+    dst[1] = make_float4(acc[b][4], acc[b][5], acc[b][6], acc[b][7]);
+  }
+  __syncthreads();
+  if (m->abort && tid == 0) {
+    // wait (bounded) for the rows still in flight before the CTA exits
+    for (int i = max(m->consumed, m->issued - SR); i < m->issued; ++i)
+      (void)mbar_wait(&full[i % SR], (i / SR) & 1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Sum of the per-CTA partials (fixed order), the single fp16 rounding and, for
+// stacked layers, y / sqrt(mean(y^2) + 1e-6).  Every CTA owns 32 hidden elements of
+// one token.  With RMSNorm the CTAs of a token publish their sums of squares, wait
+// (bounded) until all of them have, and scale their own elements: all CTAs of the
+// grid are resident together (a few small CTAs per SM), so the wait always ends.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+template <bool RMS>
+__global__ void __launch_bounds__(kCombThr) decode_combine_kernel(DecodeParams p) {
+  __shared__ float4 s_red[kCombThr / 32][8];
+  __shared__ float s_rinv;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int slice = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int d = p.d, ns = d / kCombCols;
+  constexpr int NSUB = kCombThr / 8;  // subsets of the partial rows: 8 float4 columns per row
+  const int f4 = tid & 7, sub = tid >> 3;
+  const int col = slice * kCombCols + f4 * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int LU = 8;
+  for (int c0 = sub; c0 < p.P; c0 += NSUB * LU) {
+    float4 v[LU];
+#pragma unroll
+    for (int u = 0; u < LU; ++u) {
+      const int c = c0 + u * NSUB;
+      v[u] = c < p.P ? __ldcg(reinterpret_cast<const float4*>(p.part + ((size_t)c * p.B + b) * d + col))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < LU; ++u) {
+      acc.x += v[u].x;
+      acc.y += v[u].y;
+      acc.z += v[u].z;
+      acc.w += v[u].w;
+    }
+  }
+  // the warp's 4 subsets of every column, then the 8 warps, in a fixed order
+#pragma unroll
+  for (int off = 8; off < 32; off <<= 1) {
+    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+  }
+  if (lane < 8) s_red[warp][lane] = acc;
+  __syncthreads();
+  float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+  float ss = 0.f;
+  if (tid < 8) {
+    y = s_red[0][tid];
+#pragma unroll
+    for (int w = 1; w < kCombThr / 32; ++w) {
+      const float4 v = s_red[w][tid];
+      y.x += v.x;
+      y.y += v.y;
+      y.z += v.z;
+      y.w += v.w;
+    }
+    ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) ss += __shfl_xor_sync(0x000000ffu, ss, off);
+  }
+  float rinv = 1.f;
+  if constexpr (RMS) {
+    if (tid == 0) {
+      p.sumsq[(size_t)b * ns + slice] = ss;
+      __threadfence();
+      atomicAdd(&p.tok_ctr[b], 1);
+      bool done = false;
+      for (int it = 0; it < (1 << 26) && !done; ++it) {
+        done = ld_acquire(&p.tok_ctr[b]) >= ns;
+        if (!done) __nanosleep(64);
+      }
+      if (!done) set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float t = 0.f;
+      for (int s = lane; s < ns; s += 32) t += __ldcg(p.sumsq + (size_t)b * ns + s);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+      if (lane == 0) s_rinv = rsqrtf(t / (float)d + 1e-6f);
+    }
+    __syncthreads();
+    rinv = s_rinv;
+    // the last CTA of the token to have read the sums resets both counters
+    if (tid == 0 && atomicAdd(&p.tok_ctr[p.B + b], 1) == ns - 1) {
+      p.tok_ctr[b] = 0;
+      p.tok_ctr[p.B + b] = 0;
+    }
+  }
+  if (tid < 8) {
+    __half2* yo = reinterpret_cast<__half2*>(p.y + (size_t)b * d + col);
+    yo[0] = __floats2half2_rn(y.x * rinv, y.y * rinv);
+    yo[1] = __floats2half2_rn(y.z * rinv, y.w * rinv);
+  }
+}
+
+
+bool decode_supported(int B, int d, int f, int E, int k, int n_shared, int P) {
+  // the in-kernel router splits the experts into 1, 2 or 4 chunks of 8
+  if (!(B >= 1 && B <= 2 && d <= kDecMaxD && d % 256 == 0 && (E == 8 || E == 16 || E == 32) &&
+        k <= kMaxTok && B * k + n_shared <= kDecMaxG && n_shared <= 8 && P >= 1))
+    return false;
+  const long long units = (long long)(B * k + n_shared) * (f / kMTile);
+  return (units + P - 1) / P <= kDecMaxUnits;
+}
+
+int decode_list_cap(int B, int f, int k, int n_shared, int P) {
+  const long long rows = (long long)(B * k + n_shared) * f;
+  return (int)((rows + P - 1) / P) + 1;
+}
+
+int decode_plan(int B, int d, int E, int list_cap, int P, int smem_optin, int& su, int& sr) {
+  su = sr = 0;
+  const UpLayoutD u0 = up_layout_d(d, B, E, 0);
+  const size_t strip = u0.strip;
+  size_t fixed = up_layout_d(d, B, E, 0).total - al16(u0.ring);
+  int s = (int)(((size_t)smem_optin - fixed - 256) / strip);
+  if (s > kDecMaxSu) s = kDecMaxSu;
+  if (s < 2 || up_layout_d(d, B, E, s).total > (size_t)smem_optin) return 0;
+  su = s;
+  const GaLayoutD g0 = ga_layout_d(d, 0, list_cap, P);
+  const size_t row = (size_t)4 * d;
+  if (g0.total + 4 * row > (size_t)smem_optin) return 0;
+  int r = (int)(((size_t)smem_optin - g0.total) / row);
+  sr = r > kDecMaxSr ? kDecMaxSr : r;
+  return 1;
+}
+
+size_t decode_up_smem(const DecodeParams& p) { return up_layout_d(p.d, p.B, p.routed.E, p.su).total; }
+size_t decode_gather_smem(const DecodeParams& p) { return ga_layout_d(p.d, p.sr, p.list_cap, p.P).total; }
+
+static cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                  cudaLaunchAttribute* attr, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cfg;
+}
+
+cudaError_t launch_decode_up(const DecodeParams& p, cudaStream_t st, bool pdl) {
+  const UpLayoutD L = up_layout_d(p.d, p.B, p.routed.E, p.su);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_cfg(dim3(p.P), dim3(L.nwarps * 32), L.total, st, attr, pdl);
+  const void* fn = p.B == 1 ? (const void*)decode_up_kernel<1> : (const void*)decode_up_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+  if (e != cudaSuccess) return e;
+  if (p.B == 1) return cudaLaunchKernelEx(&cfg, decode_up_kernel<1>, p);
+  return cudaLaunchKernelEx(&cfg, decode_up_kernel<2>, p);
+}
+
+cudaError_t launch_decode_gather(const DecodeParams& p, cudaStream_t st, bool pdl) {
+  const GaLayoutD L = ga_layout_d(p.d, p.sr, p.list_cap, p.P);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_cfg(dim3(p.P), dim3(L.nwarps * 32), L.total, st, attr, pdl);
+  const void* fn = p.B == 1 ? (const void*)decode_gather_kernel<1> : (const void*)decode_gather_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+  if (e != cudaSuccess) return e;
+  if (p.B == 1) return cudaLaunchKernelEx(&cfg, decode_gather_kernel<1>, p);
+  return cudaLaunchKernelEx(&cfg, decode_gather_kernel<2>, p);
+}
+
+cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_cfg(dim3(p.d / kCombCols, p.B), dim3(kCombThr), 0, st, attr, pdl);
+  if (p.rmsnorm) return cudaLaunchKernelEx(&cfg, decode_combine_kernel<true>, p);
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<false>, p);
+}
+
+}  // namespace sesg

@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
         int last_g = -1;
         const __half* gbase_ptr = nullptr;
         const __half* dbase_ptr = nullptr;
+        int row_stride = d;
         for (int i = lane; i < n; i += 2) {
           const int gidx = base + i;
           const int s = gidx % S;
@@ -216,10 +217,11 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
             last_g = gi;
             int el;
             const ExpertSet& es = expert_set(p, p.groups[gi].expert, el);
-            gbase_ptr = es.gate_t + (size_t)el * es.f * d;
-            dbase_ptr = es.down + (size_t)el * es.f * d;
+            gbase_ptr = es.gate_t + (size_t)el * es.f * es.rs;
+            dbase_ptr = es.down + (size_t)el * es.f * es.rs;
+            row_stride = es.rs;
           }
-          const size_t roff = (size_t)lcol[i] * d;
+          const size_t roff = (size_t)lcol[i] * row_stride;
           uint8_t* st = stage + (size_t)s * L.stage_bytes;
           mbar_arrive_expect_tx(&full[s], (uint32_t)(4 * d + 32));
           bulk_g2s(st, gbase_ptr + roff, (uint32_t)(2 * d), &full[s], pol);

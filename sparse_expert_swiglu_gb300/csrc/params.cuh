@@ -41,14 +41,41 @@ struct ExpertParams {
   uint32_t* dbg_mask;       // [B][n_slots][f/32] or NULL
   __half* y;                // [B][d]
   int rmsnorm;
-  float* yacc;              // [B][d] (RMSNorm path)
-  float* sumsq;             // [B][d/128]
-  int* tok_ctr;             // [B]
   int P3;                   // gather CTAs
   int stages;               // gather pipeline depth
   int list_cap;             // gather item-list capacity per CTA window
   int G_max;
   int max_tok;              // largest group of this call (sizes the up kernel's x buffer)
+};
+
+// The decode path (one or two tokens): up kernel (routing, up projection, mask, kept
+// lists), gather kernel (kept gate/down rows, per-CTA partial sums), combine kernel.
+struct DecodeParams {
+  const __half* x;          // [B][d]
+  const __half* w_router;   // [d][E]
+  int B, d, f, k, renorm, n_shared;
+  ExpertSet routed, shared;
+  Ctrl* ctrl;
+  GroupDesc* groups;        // [<= 24] written by CTA 0 of the up kernel
+  int* kcol;                // [units][16] kept columns of every unit
+  float* kv;                // [units][16][2] their v per group token
+  uint8_t* ucnt;            // [units] kept columns per unit
+  int* cta_total;           // [P] kept columns per up CTA
+  float* part;              // [P][B][d] per-CTA partial outputs of the gather kernel
+  int P;                    // CTAs of the up and gather kernels (one per SM)
+  int list_cap;             // rows per gather CTA, at most
+  int32_t* topk_idx;        // [B][k] workspace copies (written by CTA 0)
+  float* topk_w;
+  int32_t* user_idx;        // optional copies for the caller
+  float* user_w;
+  int n_slots;              // k + n_shared (debug row stride)
+  float* dbg_v;             // [B][n_slots][f] or NULL
+  uint32_t* dbg_mask;       // [B][n_slots][f/32] or NULL
+  int su, sr;               // depths of the up-strip ring and of the row ring
+  __half* y;                // [B][d]
+  int rmsnorm;
+  float* sumsq;             // [B][d/32] (RMSNorm: per-slice sums of squares)
+  int* tok_ctr;             // [2][B] (RMSNorm: slices published, slices done reading)
 };
 
 __device__ __forceinline__ const ExpertSet& expert_set(const ExpertParams& p, int expert,
@@ -80,5 +107,12 @@ cudaError_t launch_gather(const ExpertParams& p, int nt, cudaStream_t st, bool p
 // combine.cu
 size_t combine_smem_bytes(const ExpertParams& p);
 cudaError_t launch_combine(const ExpertParams& p, cudaStream_t st, bool pdl);
+// decode.cu
+bool decode_supported(int B, int d, int f, int E, int k, int n_shared, int P);
+int decode_list_cap(int B, int f, int k, int n_shared, int P);
+int decode_plan(int B, int d, int E, int list_cap, int P, int smem_optin, int& su, int& sr);
+cudaError_t launch_decode_up(const DecodeParams& p, cudaStream_t st, bool pdl);
+cudaError_t launch_decode_gather(const DecodeParams& p, cudaStream_t st, bool pdl);
+cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t st, bool pdl);
 
 }  // namespace sesg

@@ -68,20 +68,6 @@ __host__ __device__ inline UpLayout up_layout(int d, int max_tok) {
   return L;
 }
 
-template <int GI>
-__device__ __forceinline__ uint32_t code_pair(uint32_t w) {
-  // Two 2-bit codes of group slot GI as an fp16x2 of subnormals q * 4^pos * 2^-24
-  // (exact); the power of two is removed after the mma.  Slots 5..7 sit above the
-  // 10-bit mantissa and are shifted down first.
-  if constexpr (GI < 5) return w & (0x00030003u << (2 * GI));
-  else return (w >> 10) & (0x00030003u << (2 * (GI - 5)));
-}
-
-__device__ __forceinline__ float pos_scale(int gi) {
-  const int pos = gi < 5 ? gi : gi - 5;
-  return __int_as_float((127 + 24 - 2 * pos) << 23);  // 2^(24 - 2 pos)
-}
-
 // k-steps of quantiser group GI (compile time): 4 mma into the 4 accumulator chains.
 template <int GI>
 __device__ __forceinline__ void up_group(const uint4 (&w)[4], const uint32_t (&bf)[64],

@@ -186,7 +186,7 @@ def test_expert_empty_batch():
 # ---------------------------------------------------------------------------
 
 def run_layer_case(d, f, E, k, B, shared, pcts, seed, ncal=64, renorm=True, rmsnorm=False,
-                   gen_device="cpu"):
+                   gen_device="cpu", interleave=False):
     dev = gen_device
     de = synth.experts(E, d, f, seed, device=dev)
     ds = synth.experts(shared, d, f, seed, device=dev, kind=1) if shared else None
@@ -207,11 +207,13 @@ def run_layer_case(d, f, E, k, B, shared, pcts, seed, ncal=64, renorm=True, rmsn
 
     routed_used = sorted(set(idx_ref.ravel().tolist()))
     ex_gpu = ses.Experts.from_dense(de.w_up.to("cuda"), de.gate_t.to("cuda"), de.down.to("cuda"),
-                                    torch.zeros(E, dtype=torch.float32, device="cuda"))
+                                    torch.zeros(E, dtype=torch.float32, device="cuda"),
+                                    interleave=interleave)
     sh_gpu = None
     if shared:
         sh_gpu = ses.Experts.from_dense(ds.w_up.to("cuda"), ds.gate_t.to("cuda"), ds.down.to("cuda"),
-                                        torch.zeros(shared, dtype=torch.float32, device="cuda"))
+                                        torch.zeros(shared, dtype=torch.float32, device="cuda"),
+                                        interleave=interleave)
     layer = ses.Layer(wr.to("cuda"), ex_gpu, k, renorm, sh_gpu)
     ws = ses.Workspace(ses.layer_workspace_bytes(layer, B))
     results = []
@@ -318,6 +320,60 @@ def test_layer_mixtral_8x7b_batch8():
 def test_layer_mixtral_8x22b_shape_b2():
     """d=6144, f=16384 (groups capped at 4 tokens for this d), RMSNorm output."""
     run_layer_case(6144, 16384, 8, 2, 2, 0, [70], seed=6, gen_device="cuda", rmsnorm=True)
+
+
+# One or two tokens with 8, 16 or 32 routed experts take the fused decode kernel
+# (routing, up projection, mask, gathered rows and sums in one kernel).
+
+@pytest.mark.parametrize("B", [1, 2])
+def test_decode_tiny(B):
+    """d=256 (one partial superblock of 4 groups), f=512, E=8, top-2."""
+    run_layer_case(256, 512, 8, 2, B, 0, [0, 50, 90, 101], seed=20 + B, ncal=256)
+
+
+def test_decode_rmsnorm_and_full_softmax():
+    run_layer_case(512, 512, 8, 2, 2, 0, [50], seed=23, ncal=256, renorm=False, rmsnorm=True)
+
+
+def test_decode_ragged_with_shared():
+    """d=768 (a partial superblock), f=208 (13 column tiles), two tokens, one shared expert."""
+    run_layer_case(768, 208, 8, 2, 2, 1, [0, 50, 101], seed=24)
+
+
+@pytest.mark.parametrize("E,k,shared,d,f", [(16, 4, 0, 1024, 704), (32, 8, 2, 2048, 1408)])
+def test_decode_wider_routing(E, k, shared, d, f):
+    run_layer_case(d, f, E, k, 2, shared, [0, 70], seed=25 + k, gen_device="cuda")
+
+
+def test_decode_mixtral_8x7b_b2():
+    run_layer_case(4096, 14336, 8, 2, 2, 0, [50, 90], seed=30, gen_device="cuda", rmsnorm=True)
+
+
+@pytest.mark.parametrize("B", [1, 2, 5])
+def test_layer_interleaved_gate_down(B):
+    """gate and down rows interleaved in one buffer (one read per kept column), on the
+    decode path (1 or 2 tokens) and on the general path (5 tokens), with a shared expert."""
+    assert ses.Experts.from_dense(*[torch.zeros(s, dtype=torch.float16, device="cuda")
+                                    for s in [(1, 256, 16), (1, 16, 256), (1, 16, 256)]],
+                                  torch.zeros(1, device="cuda"), interleave=True).interleaved
+    run_layer_case(1024, 352, 8, 2, B, 1, [0, 70], seed=40 + B, interleave=True)
+
+
+def test_decode_repeated_calls_share_the_workspace():
+    """The unit counter of the decode kernel is reset by the kernel itself: many calls
+    in a row on one workspace give the same output up to fp32 summation order."""
+    d, f, E, k = 1024, 512, 8, 2
+    de = synth.experts(E, d, f, 31)
+    ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(),
+                                torch.full((E,), 0.05, dtype=torch.float32).cuda())
+    layer = ses.Layer(synth.router(d, E, 31).cuda(), ex, k)
+    x = synth.tokens(1, d, 31).cuda()
+    ws = ses.Workspace(ses.layer_workspace_bytes(layer, 1))
+    y0 = ses.layer_decode(x, layer, ws=ws).float().clone()
+    for _ in range(20):
+        y = ses.layer_decode(x, layer, ws=ws).float()
+        assert torch.allclose(y, y0, rtol=0, atol=2e-3)
+    assert ws.status() == 0
 
 
 def test_layer_deterministic_and_status():
