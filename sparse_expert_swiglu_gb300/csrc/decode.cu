@@ -39,8 +39,8 @@ constexpr int kDecMaxSr = 16;    // row-ring stages
 constexpr int kDecMaxUnits = 128;  // units per CTA
 constexpr int kDecRows = 4;      // kept rows per gather batch
 constexpr int kDecMaxGw = 16;    // gather warps
-constexpr int kUpThreads = 2 * kDecMaxSb * 32;
-constexpr int kGaThreads = kDecMaxGw * 32;
+constexpr int kUpThreads = (2 * kDecMaxSb + 1) * 32;  // up warps + the strip producer warp
+constexpr int kGaThreads = (kDecMaxGw + 1) * 32;      // gather warps + the row producer warp
 constexpr int kDecMaxD = 4096;
 constexpr int kCombCols = 32;    // hidden elements per combine CTA
 constexpr int kCombThr = 256;
@@ -56,6 +56,7 @@ struct UpMisc {
   int scnt[kDecMaxUnits];      // kept columns of this CTA's units
   float logits[2][kDecMaxE];
   int tidx[2][kMaxTok];
+  float tlog[2][kMaxTok];
   float tw[2][kMaxTok];
   float vbuf[kDecNV][16 * 2];
 };
@@ -69,7 +70,7 @@ struct UpLayoutD {
 __host__ __device__ inline UpLayoutD up_layout_d(int d, int B, int E, int su) {
   UpLayoutD L;
   L.nsb = n_superblocks(d);
-  L.nwarps = 2 * L.nsb;
+  L.nwarps = 2 * L.nsb + 1;
   L.su = su;
   L.strip = (size_t)L.nsb * kBlkBytes;
   L.wr_bytes = (size_t)d * E * 2;
@@ -77,7 +78,7 @@ __host__ __device__ inline UpLayoutD up_layout_d(int d, int B, int E, int su) {
   if (L.ring < L.wr_bytes) L.ring = L.wr_bytes;
   size_t o = 0;
   L.off_bar = o;
-  o += 8 * (size_t)(kDecMaxSu + kDecNV + 1);
+  o += 8 * (size_t)(2 * kDecMaxSu + kDecNV + 1);
   o = al16(o);
   L.off_misc = o;
   o += al16(sizeof(UpMisc));
@@ -124,13 +125,13 @@ struct GaLayoutD {
 __host__ __device__ inline GaLayoutD ga_layout_d(int d, int sr, int cap, int P) {
   GaLayoutD L;
   L.ngw = d / 256;
-  L.nwarps = L.ngw;
+  L.nwarps = L.ngw + 1;
   L.sr = sr;
   L.cap = cap;
   L.row = (size_t)4 * d;
   size_t o = 0;
   L.off_bar = o;
-  o += 8 * (size_t)kDecMaxSr;
+  o += 8 * (size_t)(2 * kDecMaxSr);
   o = al16(o);
   L.off_misc = o;
   o += al16(sizeof(GaMisc));
@@ -233,57 +234,36 @@ __device__ void dec_route(const DecodeParams& p, int nthreads, const __half* wr,
   }
   __syncthreads();
   if (warp < B) {
+    // top-k by rank: an expert's rank counts the experts with a larger logit, or an
+    // equal one and a lower index; ranks 0..k-1 are chosen, listed by rank
     const int b = warp;
     const float l = lane < E ? m->logits[b][lane] : -INFINITY;
-    bool taken = lane >= E;
-    float sel_l[kMaxTok];
-    int sel_i[kMaxTok];
-#pragma unroll
-    for (int j = 0; j < kMaxTok; ++j) {
-      sel_l[j] = 0.f;
-      sel_i[j] = 0;
-      if (j < k) {
-        float best = taken ? -INFINITY : l;
-        int bi = taken ? 0x7fffffff : lane;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float ob = __shfl_xor_sync(0xffffffffu, best, off);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-          if (ob > best || (ob == best && oi < bi)) {
-            best = ob;
-            bi = oi;
-          }
-        }
-        if (lane == bi) taken = true;
-        sel_l[j] = best;
-        sel_i[j] = bi;
-      }
+    int rank = 0;
+    for (int e = 0; e < E; ++e) {
+      const float le = m->logits[b][e];
+      rank += (le > l || (le == l && e < lane)) ? 1 : 0;
     }
-    const float lmax = sel_l[0];
-    float denom = 0.f;
-    if (p.renorm) {
-#pragma unroll
-      for (int j = 0; j < kMaxTok; ++j)
-        if (j < k) denom += expf(sel_l[j] - lmax);
-    } else {
-      float part = lane < E ? expf(l - lmax) : 0.f;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-      denom = part;
+    if (lane < E && rank < k) {
+      m->tidx[b][rank] = lane;
+      m->tlog[b][rank] = l;
     }
+    __syncwarp();
     if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < kMaxTok; ++j) {
-        if (j < k) {
-          const float w = expf(sel_l[j] - lmax) / denom;
-          m->tidx[b][j] = sel_i[j];
-          m->tw[b][j] = w;
-          if (blockIdx.x == 0) {
-            p.topk_idx[b * k + j] = sel_i[j];
-            p.topk_w[b * k + j] = w;
-            if (p.user_idx) p.user_idx[b * k + j] = sel_i[j];
-            if (p.user_w) p.user_w[b * k + j] = w;
-          }
+      // softmax weights, the denominator summed in a fixed order
+      const float lmax = m->tlog[b][0];
+      float denom = 0.f;
+      if (p.renorm)
+        for (int j = 0; j < k; ++j) denom += expf(m->tlog[b][j] - lmax);
+      else
+        for (int e = 0; e < E; ++e) denom += expf(m->logits[b][e] - lmax);
+      for (int j = 0; j < k; ++j) {
+        const float w = expf(m->tlog[b][j] - lmax) / denom;
+        m->tw[b][j] = w;
+        if (blockIdx.x == 0) {
+          p.topk_idx[b * k + j] = m->tidx[b][j];
+          p.topk_w[b * k + j] = w;
+          if (p.user_idx) p.user_idx[b * k + j] = m->tidx[b][j];
+          if (p.user_w) p.user_w[b * k + j] = w;
         }
       }
     }
@@ -551,7 +531,8 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
   const int d = p.d, SU = p.su;
   const UpLayoutD L = up_layout_d(d, B, p.routed.E, SU);
   uint64_t* full = reinterpret_cast<uint64_t*>(usm + L.off_bar);
-  uint64_t* vfree = full + kDecMaxSu;
+  uint64_t* empty = full + kDecMaxSu;
+  uint64_t* vfree = empty + kDecMaxSu;
   uint64_t* wbar = vfree + kDecNV;
   UpMisc* m = reinterpret_cast<UpMisc*>(usm + L.off_misc);
   uint8_t* ring = usm + L.off_ring;
@@ -563,7 +544,10 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nsb = L.nsb, nthreads = L.nwarps * 32;
   if (tid == 0) {
-    for (int s = 0; s < SU; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < SU; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nsb);
+    }
     for (int v = 0; v < kDecNV; ++v) mbar_init(&vfree[v], 1);
     mbar_init(wbar, 1);
     fence_barrier_init();
@@ -606,22 +590,35 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
   const int u0 = (int)muldiv(U, blockIdx.x, gridDim.x), u1 = (int)muldiv(U, blockIdx.x + 1, gridDim.x);
   const int n = u1 - u0;
 
-  const uint64_t pol = policy_evict_first();
-  // strip of unit j of this CTA into its stage
-  auto issue = [&](int j) {
-    const int s = j % SU, u = u0 + j, g = u / MT, mt = u - g * MT;
-    int el;
-    const ExpertSet& es = dec_set(p, grp[g].expert, el);
-    m->pend[s] = j + 1;
-    mbar_arrive_expect_tx(&full[s], (uint32_t)L.strip);
-    bulk_g2s(ring + (size_t)s * L.strip, es.up + (size_t)el * es.up_stride + (size_t)mt * L.strip,
-             (uint32_t)L.strip, &full[s], pol);
-  };
-  if (tid == 0)
-    for (int j = 0; j < min(n, SU); ++j) issue(j);
-  {
-    // ---- up warps: unit lane ug (units j = ug, ug + 2, ...), superblock sb.  No
-    // producer warp: the last warp to finish a unit refills its stage.
+  if (warp == 2 * nsb) {
+    // ---- producer warp: the strips of this CTA's units, in order
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int s = 0, ph = 0, g = u0 / MT, mt = u0 - g * MT;
+      for (int j = 0; j < n; ++j) {
+        if (j >= SU && !mbar_wait(&empty[s], ph ^ 1)) {
+          dec_fail(p, &m->abort);
+          break;
+        }
+        if (vload(&m->abort)) break;
+        int el;
+        const ExpertSet& es = dec_set(p, grp[g].expert, el);
+        m->pend[s] = j + 1;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)L.strip);
+        bulk_g2s(ring + (size_t)s * L.strip, es.up + (size_t)el * es.up_stride + (size_t)mt * L.strip,
+                 (uint32_t)L.strip, &full[s], pol);
+        if (++s == SU) {
+          s = 0;
+          ph ^= 1;
+        }
+        if (++mt == MT) {
+          mt = 0;
+          ++g;
+        }
+      }
+    }
+  } else {
+    // ---- up warps: unit lane ug (units j = ug, ug + 2, ...), superblock sb
     const int uw = warp, ug = uw / nsb, sb = uw % nsb;
     const int ng = min(8, (d - sb * kSuper) / kGroup);
     float* xgw = xg + uw * 16;
@@ -650,6 +647,11 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
       }
       float vacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
       dec_superblock<B>(ring + (size_t)s * L.strip + (size_t)sb * kBlkBytes, xr, xgw, ng, vacc);
+      __syncwarp();
+      if (lane == 0) {
+        if (sb == 0) m->pend[s] = 0;
+        mbar_arrive(&empty[s]);
+      }
       // the slot's previous unit must have been finalized
       if (j >= kDecNV &&
           !__all_sync(0xffffffffu, mbar_wait(&vfree[slot], ((j >> 2) - 1) & 1))) {
@@ -666,16 +668,9 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
       prev = __shfl_sync(0xffffffffu, prev, 0);
       __syncwarp();
       if (prev == nsb - 1) {
-        // last superblock of the unit: the stage is free, and this warp finalizes the unit
+        // last superblock of the unit: this warp finalizes it
         __threadfence_block();
-        if (lane == 0) {
-          m->ucnt[slot] = 0;
-          m->pend[s] = 0;
-          if (j + SU < n && !vload(&m->abort)) {
-            fence_proxy_async_smem();
-            issue(j + SU);
-          }
-        }
+        if (lane == 0) m->ucnt[slot] = 0;
         const int cnt = dec_finalize<B>(p, vpart + (size_t)slot * nsb * 32, nsb, grp[g], u, mt,
                                         thr, m->vbuf[slot]);
         if (lane == 0) m->scnt[j] = cnt;
@@ -710,35 +705,18 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
 }
 
 // ---------------------------------------------------------------------------
-// Gather kernel.  No producer warp: thread 0 issues the first ring fill, and after the
-// barrier of every batch (when all warps are done with the previous batch) it issues
-// the rows that reuse the freed stages.  A kept column whose gate and down rows are
-// interleaved in one buffer costs one 4d-byte copy, else two 2d-byte copies.
+// Gather kernel.  A producer warp streams the kept rows through the ring; the gather
+// warps release a stage once every warp is done with its row.  A kept column whose
+// gate and down rows are interleaved in one buffer costs one 4d-byte copy, else two
+// 2d-byte copies.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void ga_issue(const DecodeParams& p, const GaRow* list, const GroupDesc* grp,
-                                         uint8_t* ring, uint64_t* full, int i, int SR, size_t row,
-                                         int d, uint64_t pol) {
-  const GaRow gr = list[i];
-  int el;
-  const ExpertSet& es = dec_set(p, grp[gr.g].expert, el);
-  const size_t roff = ((size_t)el * es.f + gr.col) * es.rs;
-  const int s = i % SR;
-  uint8_t* st = ring + (size_t)s * row;
-  mbar_arrive_expect_tx(&full[s], (uint32_t)row);
-  if (es.rs == 2 * d) {
-    bulk_g2s(st, es.gate_t + roff, (uint32_t)(4 * d), &full[s], pol);
-  } else {
-    bulk_g2s(st, es.gate_t + roff, (uint32_t)(2 * d), &full[s], pol);
-    bulk_g2s(st + 2 * d, es.down + roff, (uint32_t)(2 * d), &full[s], pol);
-  }
-}
-
 template <int B>
 __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t gsm[];
   const int d = p.d, SR = p.sr, P = gridDim.x;
   const GaLayoutD L = ga_layout_d(d, SR, p.list_cap, P);
   uint64_t* full = reinterpret_cast<uint64_t*>(gsm + L.off_bar);
+  uint64_t* empty = full + kDecMaxSr;
   GaMisc* m = reinterpret_cast<GaMisc*>(gsm + L.off_misc);
   uint8_t* ring = gsm + L.off_ring;
   GaRow* list = reinterpret_cast<GaRow*>(gsm + L.off_list);
@@ -747,9 +725,12 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
   int* scan = reinterpret_cast<int*>(gsm + L.off_scan);
   GroupDesc* grp = reinterpret_cast<GroupDesc*>(gsm + L.off_grp);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ngw = L.ngw, nthreads = ngw * 32;
+  const int ngw = L.ngw, nct = ngw * 32, nthreads = nct + 32;
   if (tid == 0) {
-    for (int s = 0; s < SR; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < SR; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], ngw);
+    }
     fence_barrier_init();
     m->abort = 0;
     m->issued = 0;
@@ -760,7 +741,8 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
   float xf[B][8];
 #pragma unroll
   for (int b = 0; b < B; ++b) {
-    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)b * d) + tid);
+    const uint4 xv = tid < nct ? __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)b * d) + tid)
+                               : make_uint4(0, 0, 0, 0);
     const __half2* h2 = reinterpret_cast<const __half2*>(&xv);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -865,13 +847,37 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
     }
   }
   __syncthreads();
-  const uint64_t pol = policy_evict_first();
-  if (tid == 0) {
-    const int n0 = min(nrows, SR);
-    for (int i = 0; i < n0; ++i) ga_issue(p, list, grp, ring, full, i, SR, L.row, d, pol);
-    m->issued = n0;
-  }
-
+  if (warp == ngw) {
+    // ---- producer warp: the kept rows, in order
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int s = 0, ph = 0;
+      for (int i = 0; i < nrows; ++i) {
+        if (i >= SR && !mbar_wait(&empty[s], ph ^ 1)) {
+          dec_fail(p, &m->abort);
+          break;
+        }
+        if (vload(&m->abort)) break;
+        const GaRow gr = list[i];
+        int el;
+        const ExpertSet& es = dec_set(p, grp[gr.g].expert, el);
+        const size_t roff = ((size_t)el * es.f + gr.col) * es.rs;
+        uint8_t* st = ring + (size_t)s * L.row;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)L.row);
+        if (es.rs == 2 * d) {
+          bulk_g2s(st, es.gate_t + roff, (uint32_t)(4 * d), &full[s], pol);
+        } else {
+          bulk_g2s(st, es.gate_t + roff, (uint32_t)(2 * d), &full[s], pol);
+          bulk_g2s(st + 2 * d, es.down + roff, (uint32_t)(2 * d), &full[s], pol);
+        }
+        m->issued = i + 1;
+        if (++s == SR) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  } else {
   // ---- batches of up to kDecRows rows, one barrier per batch
   float acc[B][8];
 #pragma unroll
@@ -931,18 +937,20 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
 #pragma unroll
         for (int b = 0; b < B; ++b) rb[(q * 2 + b) * kDecMaxGw + warp] = dot[q][b];
     }
-    if (__syncthreads_or(!ok)) {
+    int fail;
+    asm volatile(
+        "{\n\t.reg .pred pin, pout;\n\t"
+        "setp.ne.u32 pin, %1, 0;\n\t"
+        "barrier.red.or.pred pout, 1, %2, pin;\n\t"
+        "selp.u32 %0, 1, 0, pout;\n\t}"
+        : "=r"(fail)
+        : "r"((unsigned)!ok), "r"(nct)
+        : "memory");
+    if (fail) {
       if (tid == 0) dec_fail(p, &m->abort);
       break;
     }
-    if (tid == 0) {
-      // every warp is done with the previous batch: refill its stages
-      m->consumed = i0;
-      fence_proxy_async_smem();
-      const int hi = min(nrows, i0 + SR);
-      for (int i = m->issued; i < hi; ++i) ga_issue(p, list, grp, ring, full, i, SR, L.row, d, pol);
-      if (hi > m->issued) m->issued = hi;
-    }
+    if (tid == 0) m->consumed = i0;
     float h[kDecRows][B];
 #pragma unroll
     for (int q = 0; q < kDecRows; ++q) {
@@ -976,6 +984,9 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
         }
       }
     }
+    __syncwarp();
+    if (lane == 0)
+      for (int q = 0; q < nb; ++q) mbar_arrive(&empty[st[q]]);
   }
   // this CTA's partial output (every CTA writes one, zeros if it had no rows)
 #pragma unroll
@@ -983,6 +994,7 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
     float4* dst = reinterpret_cast<float4*>(p.part + ((size_t)blockIdx.x * B + b) * d + tid * 8);
     dst[0] = make_float4(acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
     dst[1] = make_float4(acc[b][4], acc[b][5], acc[b][6], acc[b][7]);
+  }
   }
   __syncthreads();
   if (m->abort && tid == 0) {
