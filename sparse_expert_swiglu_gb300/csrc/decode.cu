@@ -10,9 +10,9 @@
 //                         fixed, equal share of the work units (16 output columns of
 //                         one expert): packed INT2 strips stream through a TMA ring;
 //                         16 warps, one 512-input superblock each, two units in
-//                         flight; the last warp of a unit to finish adds the
-//                         superblock partials, applies mask = |v| > t and writes the
-//                         unit's kept columns.
+//                         flight; a finalize warp adds each unit's superblock
+//                         partials in a fixed order, applies mask = |v| > t and writes
+//                         the unit's kept columns.
 //   decode_gather_kernel  one CTA per SM.  An equal share of all kept columns, in
 //                         (group, column) order: their gate and down rows stream
 //                         through a TMA ring; 16 warps form x . gate for a batch of
@@ -39,7 +39,7 @@ constexpr int kDecMaxSr = 16;    // row-ring stages
 constexpr int kDecMaxUnits = 128;  // units per CTA
 constexpr int kDecRows = 4;      // kept rows per gather batch
 constexpr int kDecMaxGw = 16;    // gather warps
-constexpr int kUpThreads = (2 * kDecMaxSb + 1) * 32;  // up warps + the strip producer warp
+constexpr int kUpThreads = (2 * kDecMaxSb + 2) * 32;  // up warps, strip producer, finalize warp
 constexpr int kGaThreads = (kDecMaxGw + 1) * 32;      // gather warps + the row producer warp
 constexpr int kDecMaxD = 4096;
 constexpr int kCombCols = 32;    // hidden elements per combine CTA
@@ -51,7 +51,6 @@ __host__ __device__ inline size_t al16(size_t o) { return (o + 15) & ~(size_t)15
 struct UpMisc {
   int abort;
   int G;
-  int ucnt[kDecNV];            // superblock partials written for the unit in the slot
   int pend[kDecMaxSu];         // strip in flight in the stage (issue index + 1) or 0
   int scnt[kDecMaxUnits];      // kept columns of this CTA's units
   float logits[2][kDecMaxE];
@@ -70,7 +69,7 @@ struct UpLayoutD {
 __host__ __device__ inline UpLayoutD up_layout_d(int d, int B, int E, int su) {
   UpLayoutD L;
   L.nsb = n_superblocks(d);
-  L.nwarps = 2 * L.nsb + 1;
+  L.nwarps = 2 * L.nsb + 2;
   L.su = su;
   L.strip = (size_t)L.nsb * kBlkBytes;
   L.wr_bytes = (size_t)d * E * 2;
@@ -78,7 +77,7 @@ __host__ __device__ inline UpLayoutD up_layout_d(int d, int B, int E, int su) {
   if (L.ring < L.wr_bytes) L.ring = L.wr_bytes;
   size_t o = 0;
   L.off_bar = o;
-  o += 8 * (size_t)(2 * kDecMaxSu + kDecNV + 1);
+  o += 8 * (size_t)(2 * kDecMaxSu + 2 * kDecNV + 1);
   o = al16(o);
   L.off_misc = o;
   o += al16(sizeof(UpMisc));
@@ -222,7 +221,9 @@ __device__ void dec_route(const DecodeParams& p, int nthreads, const __half* wr,
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       float v = acc[b][i];
-      for (int off = 16; off >= nchunk; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        if (off >= nchunk) v += __shfl_xor_sync(0xffffffffu, v, off);
       if (lane < nchunk) lred[(warp * B + b) * kDecMaxE + lane * 8 + i] = v;
     }
   __syncthreads();
@@ -532,7 +533,8 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
   const UpLayoutD L = up_layout_d(d, B, p.routed.E, SU);
   uint64_t* full = reinterpret_cast<uint64_t*>(usm + L.off_bar);
   uint64_t* empty = full + kDecMaxSu;
-  uint64_t* vfree = empty + kDecMaxSu;
+  uint64_t* vfull = empty + kDecMaxSu;
+  uint64_t* vfree = vfull + kDecNV;
   uint64_t* wbar = vfree + kDecNV;
   UpMisc* m = reinterpret_cast<UpMisc*>(usm + L.off_misc);
   uint8_t* ring = usm + L.off_ring;
@@ -548,7 +550,10 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], nsb);
     }
-    for (int v = 0; v < kDecNV; ++v) mbar_init(&vfree[v], 1);
+    for (int v = 0; v < kDecNV; ++v) {
+      mbar_init(&vfull[v], nsb);
+      mbar_init(&vfree[v], 1);
+    }
     mbar_init(wbar, 1);
     fence_barrier_init();
     // the router weight is not written by the previous kernel: fetch it before waiting
@@ -559,7 +564,6 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
                policy_evict_last());
     }
     m->abort = 0;
-    for (int v = 0; v < kDecNV; ++v) m->ucnt[v] = 0;
     for (int s = 0; s < kDecMaxSu; ++s) m->pend[s] = 0;
   }
   __syncthreads();
@@ -590,7 +594,33 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
   const int u0 = (int)muldiv(U, blockIdx.x, gridDim.x), u1 = (int)muldiv(U, blockIdx.x + 1, gridDim.x);
   const int n = u1 - u0;
 
-  if (warp == 2 * nsb) {
+  if (warp == 2 * nsb + 1) {
+    // ---- finalize warp: every unit in order, once all its superblock partials are in
+    int g = u0 / MT, mt = u0 - g * MT, cur_g = -1;
+    float thr = 0.f;
+    for (int j = 0; j < n; ++j) {
+      const int slot = j & (kDecNV - 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(&vfull[slot], (j >> 2) & 1))) {
+        if (lane == 0) dec_fail(p, &m->abort);
+        break;
+      }
+      if (g != cur_g) {
+        int el;
+        const ExpertSet& es = dec_set(p, grp[g].expert, el);
+        thr = es.thr[el];
+        cur_g = g;
+      }
+      const int cnt = dec_finalize<B>(p, vpart + (size_t)slot * nsb * 32, nsb, grp[g], u0 + j, mt,
+                                      thr, m->vbuf[slot]);
+      if (lane == 0) m->scnt[j] = cnt;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&vfree[slot]);
+      if (++mt == MT) {
+        mt = 0;
+        ++g;
+      }
+    }
+  } else if (warp == 2 * nsb) {
     // ---- producer warp: the strips of this CTA's units, in order
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
@@ -624,7 +654,6 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
     float* xgw = xg + uw * 16;
     uint32_t xr[B][4][2];
     int cur_g = -1;
-    float thr = 0.f;
     // stage s = j % SU with full-barrier parity ph = (j / SU) & 1, and unit u = u0 + j as
     // (group g, M-tile mt), all advanced by 2 units per iteration without divisions
     int s = ug % SU, ph = (ug / SU) & 1;
@@ -637,11 +666,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
         if (!ab && lane == 0) dec_fail(p, &m->abort);
         break;
       }
-      const int u = u0 + j;
       if (g != cur_g) {
-        int el;
-        const ExpertSet& es = dec_set(p, grp[g].expert, el);
-        thr = es.thr[el];
         dec_up_setup<B>(xs, d, grp[g], sb, ng, xr, xgw);
         cur_g = g;
       }
@@ -660,23 +685,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
       }
       vpart[((size_t)slot * nsb + sb) * 32 + lane] = make_float4(vacc[0][0], vacc[0][1], vacc[1][0], vacc[1][1]);
       __syncwarp();
-      int prev = 0;
-      if (lane == 0) {
-        __threadfence_block();
-        prev = atomicAdd(&m->ucnt[slot], 1);
-      }
-      prev = __shfl_sync(0xffffffffu, prev, 0);
-      __syncwarp();
-      if (prev == nsb - 1) {
-        // last superblock of the unit: this warp finalizes it
-        __threadfence_block();
-        if (lane == 0) m->ucnt[slot] = 0;
-        const int cnt = dec_finalize<B>(p, vpart + (size_t)slot * nsb * 32, nsb, grp[g], u, mt,
-                                        thr, m->vbuf[slot]);
-        if (lane == 0) m->scnt[j] = cnt;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&vfree[slot]);
-      }
+      if (lane == 0) mbar_arrive(&vfull[slot]);
       s += 2;
       if (s >= SU) {
         s -= SU;
