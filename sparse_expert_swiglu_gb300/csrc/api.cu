@@ -44,7 +44,7 @@ int groups_max_routed(int B, int E, int k, int gcap) {
 // Workspace carving shared by every entry point.
 struct WsLayout {
   size_t ctrl, groups, tok_groups, topk_idx, topk_w, group_total, unit_cnt, item_col, item_v,
-      part, sumsq, tok_ctr, cta_total, total;
+      part, sumsq, tok_ctr, cta_total, klist, total;
   int G_max, P3, list_cap;
 };
 
@@ -74,6 +74,8 @@ WsLayout ws_layout(int B, int npairs, int G_max, int d, int f, int P3) {
   L.sumsq = take(sizeof(float) * (size_t)B * (d / 32));
   L.tok_ctr = take(sizeof(int) * (size_t)2 * B);
   L.cta_total = take(sizeof(int) * (size_t)P3);
+  // decode path: per up CTA, 16 entries of 16 bytes for each of its units
+  L.klist = take((size_t)P3 * (((size_t)G_max * MT + P3 - 1) / P3) * 16 * 16);
   L.total = o;
   return L;
 }
@@ -359,9 +361,8 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
     if (layer->shared.E > 0) dp.shared = to_set(layer->shared);
     dp.ctrl = at<Ctrl>(ws, L.ctrl);
     dp.groups = at<GroupDesc>(ws, L.groups);
-    dp.kcol = at<int>(ws, L.item_col);
-    dp.kv = at<float>(ws, L.item_v);
-    dp.ucnt = at<uint8_t>(ws, L.unit_cnt);
+    dp.klist = at<int4>(ws, L.klist);
+    dp.kcap = (int)((((long long)L.G_max * (layer->routed.f / kMTile)) + P - 1) / P) * 16;
     dp.cta_total = at<int>(ws, L.cta_total);
     dp.part = at<float>(ws, L.part);
     dp.P = P;

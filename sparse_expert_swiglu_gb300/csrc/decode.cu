@@ -52,7 +52,7 @@ struct UpMisc {
   int abort;
   int G;
   int pend[kDecMaxSu];         // strip in flight in the stage (issue index + 1) or 0
-  int scnt[kDecMaxUnits];      // kept columns of this CTA's units
+  int total;                   // kept columns of this CTA's units
   float logits[2][kDecMaxE];
   int tidx[2][kMaxTok];
   float tlog[2][kMaxTok];
@@ -108,7 +108,7 @@ struct GaRow {
 struct GaMisc {
   int abort;
   int G;
-  int c0, c1;                  // up CTAs whose units hold this CTA's rows
+  int c0;                      // up CTA whose list holds this CTA's first row
   int issued;                  // rows issued (0 .. issued-1)
   int consumed;                // rows whose stages are free again
   int tmap[kDecMaxG][2];       // group token of batch token b, -1 if none
@@ -118,7 +118,7 @@ struct GaMisc {
 struct GaLayoutD {
   int ngw, nwarps, sr, cap;
   size_t row;
-  size_t off_bar, off_misc, off_ring, off_list, off_red, off_pre, off_scan, off_grp, total;
+  size_t off_bar, off_misc, off_ring, off_list, off_red, off_pre, off_grp, total;
 };
 
 __host__ __device__ inline GaLayoutD ga_layout_d(int d, int sr, int cap, int P) {
@@ -143,8 +143,6 @@ __host__ __device__ inline GaLayoutD ga_layout_d(int d, int sr, int cap, int P) 
   o += (size_t)2 * kDecRows * 2 * kDecMaxGw * 4;
   L.off_pre = o;
   o += al16(4 * ((size_t)P + 1));
-  L.off_scan = o;
-  o += al16(4 * ((size_t)kGaThreads + 1));
   L.off_grp = o;
   o += al16(sizeof(GroupDesc) * kDecMaxG);
   L.total = o;
@@ -451,12 +449,12 @@ __device__ __forceinline__ void dec_superblock(const uint8_t* __restrict__ blk,
 }
 
 // The superblock partials of one unit added in a fixed order, per-token v of its 16
-// columns, mask = |v| > t (union over the group's tokens) and the unit's kept list:
-// kcol[u][rank] (ascending columns), kv[u][rank][t] (0 for a token that drops the
-// column), ucnt[u].  Returns the number of kept columns.
+// columns, mask = |v| > t (union over the group's tokens) and the unit's kept columns,
+// appended at out in ascending order: {column | group << 16, v per group token (0 for a
+// token that drops the column)}.  Returns the number of kept columns.
 template <int T>
 __device__ int dec_finalize(const DecodeParams& p, const float4* vpart, int nsb, const GroupDesc& gd,
-                            int u, int mt, float thr, float* vbuf) {
+                            int g, int mt, float thr, float* vbuf, int4* out) {
   constexpr int G = 8 / T;
   const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
   float v00 = 0.f, v01 = 0.f, v10 = 0.f, v11 = 0.f;
@@ -496,15 +494,11 @@ __device__ int dec_finalize(const DecodeParams& p, const float4* vpart, int nsb,
   const uint32_t bal = __ballot_sync(0xffffffffu, mbits != 0);
   if (mbits) {
     const int rank = __popc(bal & ((1u << lane) - 1u));
-    const size_t e = (size_t)u * 16 + rank;
-    p.kcol[e] = mt * kMTile + lane;
-    float2 kv;
-    kv.x = (mbits & 1u) ? vv[0] : 0.f;
-    kv.y = (T > 1 && ((mbits >> 1) & 1u)) ? vv[T > 1 ? 1 : 0] : 0.f;
-    reinterpret_cast<float2*>(p.kv)[e] = kv;
+    const float v0 = (mbits & 1u) ? vv[0] : 0.f;
+    const float v1 = (T > 1 && ((mbits >> 1) & 1u)) ? vv[T > 1 ? 1 : 0] : 0.f;
+    out[rank] = make_int4((mt * kMTile + lane) | (g << 16), __float_as_int(v0), __float_as_int(v1), 0);
   }
   const int cnt = __popc(bal);
-  if (lane == 0) p.ucnt[u] = (uint8_t)cnt;
   if (p.dbg_v || p.dbg_mask) {
 #pragma unroll
     for (int t = 0; t < T; ++t) {
@@ -564,6 +558,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
                policy_evict_last());
     }
     m->abort = 0;
+    m->total = 0;
     for (int s = 0; s < kDecMaxSu; ++s) m->pend[s] = 0;
   }
   __syncthreads();
@@ -596,8 +591,9 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
 
   if (warp == 2 * nsb + 1) {
     // ---- finalize warp: every unit in order, once all its superblock partials are in
-    int g = u0 / MT, mt = u0 - g * MT, cur_g = -1;
+    int g = u0 / MT, mt = u0 - g * MT, cur_g = -1, off = 0;
     float thr = 0.f;
+    int4* out = p.klist + (size_t)blockIdx.x * p.kcap;
     for (int j = 0; j < n; ++j) {
       const int slot = j & (kDecNV - 1);
       if (!__all_sync(0xffffffffu, mbar_wait(&vfull[slot], (j >> 2) & 1))) {
@@ -610,9 +606,8 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
         thr = es.thr[el];
         cur_g = g;
       }
-      const int cnt = dec_finalize<B>(p, vpart + (size_t)slot * nsb * 32, nsb, grp[g], u0 + j, mt,
-                                      thr, m->vbuf[slot]);
-      if (lane == 0) m->scnt[j] = cnt;
+      off += dec_finalize<B>(p, vpart + (size_t)slot * nsb * 32, nsb, grp[g], g, mt, thr,
+                             m->vbuf[slot], out + off);
       __syncwarp();
       if (lane == 0) mbar_arrive(&vfree[slot]);
       if (++mt == MT) {
@@ -620,6 +615,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
         ++g;
       }
     }
+    if (lane == 0) m->total = off;
   } else if (warp == 2 * nsb) {
     // ---- producer warp: the strips of this CTA's units, in order
     if (lane == 0) {
@@ -707,9 +703,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
         if (q > 0) (void)mbar_wait(&full[s], ((q - 1) / SU) & 1);
       }
     }
-    int tot = 0;
-    for (int j = 0; j < n; ++j) tot += m->scnt[j];
-    p.cta_total[blockIdx.x] = tot;
+    p.cta_total[blockIdx.x] = m->total;
   }
 }
 
@@ -731,7 +725,6 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
   GaRow* list = reinterpret_cast<GaRow*>(gsm + L.off_list);
   float* red = reinterpret_cast<float*>(gsm + L.off_red);
   int* pre = reinterpret_cast<int*>(gsm + L.off_pre);
-  int* scan = reinterpret_cast<int*>(gsm + L.off_scan);
   GroupDesc* grp = reinterpret_cast<GroupDesc*>(gsm + L.off_grp);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ngw = L.ngw, nct = ngw * 32, nthreads = nct + 32;
@@ -787,14 +780,11 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
   const int N = pre[P], G = m->G;
   for (int i = tid; i < G * (int)(sizeof(GroupDesc) / 4); i += nthreads)
     reinterpret_cast<int*>(grp)[i] = __ldcg(reinterpret_cast<const int*>(p.groups) + i);
-  const int MT = p.f / kMTile, U = G * MT;
   const int a = (int)muldiv(N, blockIdx.x, P), bnd = (int)muldiv(N, blockIdx.x + 1, P);
   const int nrows = bnd - a;
-  // up CTAs whose units hold rows [a, bnd): the last c with pre[c] <= a, the last with pre[c] < bnd
-  for (int c = tid; c < P; c += nthreads) {
+  // the up CTA whose list holds row a: the last c with pre[c] <= a
+  for (int c = tid; c < P; c += nthreads)
     if (pre[c] <= a && (c + 1 == P || pre[c + 1] > a)) m->c0 = c;
-    if (pre[c] < bnd && (c + 1 == P || pre[c + 1] >= bnd)) m->c1 = c;
-  }
   __syncthreads();
   if (tid < G * 2) {
     const int g = tid >> 1, b = tid & 1;
@@ -809,50 +799,19 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
     m->tmap[g][b] = t_of_b;
     m->tw[g][b] = w;
   }
-  if (nrows > 0) {
-    // candidate units, nthreads at a time: counts, prefix, then 16 lanes per unit copy
-    // the unit's rows that fall in [a, bnd)
-    const int c0 = m->c0, c1 = max(m->c0, m->c1);
-    const int v0 = (int)muldiv(U, c0, P), v1 = (int)muldiv(U, c1 + 1, P);
-    int run = pre[c0];
-    for (int base = v0; base < v1; base += nthreads) {
-      const int u = base + tid;
-      scan[tid] = u < v1 ? (int)__ldcg(p.ucnt + u) : 0;
-      __syncthreads();
-      if (tid < 32) {
-        int carry = 0;
-        for (int o = 0; o < nthreads; o += 32) {
-          const int v = scan[o + lane];
-          int incl = v;
-#pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += t;
-          }
-          scan[o + lane] = carry + incl - v;
-          carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) scan[nthreads] = carry;
-      }
-      __syncthreads();
-      const int nu = min(nthreads, v1 - base);
-      for (int q = tid; q < nu * 16; q += nthreads) {
-        const int k = q >> 4, r = q & 15;
-        const int cnt = scan[k + 1] - scan[k];
-        const int row = run + scan[k] + r;
-        if (r < cnt && row >= a && row < bnd) {
-          const size_t e = (size_t)(base + k) * 16 + r;
-          GaRow gr;
-          gr.col = __ldcg(p.kcol + e);
-          gr.g = (base + k) / MT;
-          const float2 kv = __ldcg(reinterpret_cast<const float2*>(p.kv) + e);
-          gr.v[0] = kv.x;
-          gr.v[1] = kv.y;
-          list[row - a] = gr;
-        }
-      }
-      run += scan[nthreads];
-      __syncthreads();
+  // rows [a, bnd): entries of up CTAs c0..c1, each list in unit order
+  {
+    const int c0 = m->c0;
+    for (int r = a + tid; r < bnd; r += nthreads) {
+      int cc = c0;
+      while (cc + 1 < P && pre[cc + 1] <= r) ++cc;
+      const int4 e = __ldcg(p.klist + (size_t)cc * p.kcap + (r - pre[cc]));
+      GaRow gr;
+      gr.col = e.x & 0xffff;
+      gr.g = e.x >> 16;
+      gr.v[0] = __int_as_float(e.y);
+      gr.v[1] = __int_as_float(e.z);
+      list[r - a] = gr;
     }
   }
   __syncthreads();

@@ -57,9 +57,9 @@ struct DecodeParams {
   ExpertSet routed, shared;
   Ctrl* ctrl;
   GroupDesc* groups;        // [<= 24] written by CTA 0 of the up kernel
-  int* kcol;                // [units][16] kept columns of every unit
-  float* kv;                // [units][16][2] their v per group token
-  uint8_t* ucnt;            // [units] kept columns per unit
+  int4* klist;              // [P][kcap] kept columns of every up CTA, in unit order:
+                            // {column | group << 16, v of group token 0, 1 (float bits), 0}
+  int kcap;                 // entries per up CTA
   int* cta_total;           // [P] kept columns per up CTA
   float* part;              // [P][B][d] per-CTA partial outputs of the gather kernel
   int P;                    // CTAs of the up and gather kernels (one per SM)
