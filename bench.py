@@ -41,8 +41,8 @@ METRIC = "MoE decode layer expert-tokens/s (Mixtral-8x7B-shaped layer, 1 token, 
 # ncu DRAM bytes per launch of the dominant kernel, keyed by the source file hash it was
 # taken on; reported only while the kernel source is unchanged.
 NCU_TRAFFIC = {
-    # gather_kernel, layer copy 0 at 70% (1-copy small case): 144.54 MB read + 3.10 MB written
-    ("gather", "dbf6946cb4876587"): 147.64e6,
+    # decode_gather_kernel, layer copy 0 at 70% (1-copy small case): 144.16 MB read + 3.36 MB written
+    ("decode_gather_kernel", "88743459a6449cfe"): 147.52e6,
 }
 
 
@@ -281,9 +281,11 @@ def time_steps(graphs, stream, steps, warmup, world, dev):
     return start.elapsed_time(end) / 1e3  # seconds
 
 
-def per_kernel_times(prof_graphs, events_list, stream, steps):
+def per_kernel_times(prof_graphs, events_list, stream, steps, path):
     """Average device time of each kernel, from events recorded around it inside the
-    graphs (replayed R at a time, read back before the events are re-recorded)."""
+    graphs (replayed R at a time, read back before the events are re-recorded).  On the
+    decode path the router runs inside the up kernel: events 0 and 1 are back to back,
+    and their interval is the cost of an event pair, reported as event_pair_us."""
     R = len(prof_graphs)
     acc = np.zeros(4)
     n = 0
@@ -297,14 +299,17 @@ def per_kernel_times(prof_graphs, events_list, stream, steps):
             for j in range(4):
                 acc[j] += evs[j].elapsed_time(evs[j + 1])
             n += 1
-    names = ["route", "up", "gather", "combine"]
-    return {nm: acc[j] / n * 1e3 for j, nm in enumerate(names)}  # microseconds
+    t = [acc[j] / n * 1e3 for j in range(4)]  # microseconds
+    if path == "decode":
+        return {"decode_up_kernel": t[1], "decode_gather_kernel": t[2],
+                "decode_combine_kernel": t[3], "event_pair_us": t[0]}
+    return {"route_kernel": t[0], "up_kernel": t[1], "gather_kernel": t[2], "combine_kernel": t[3]}
 
 
 def source_hash():
     import hashlib
     h = hashlib.sha256()
-    for fn in ["up.cu", "gather.cu", "combine.cu", "common.cuh", "params.cuh"]:
+    for fn in ["up.cu", "gather.cu", "combine.cu", "decode.cu", "common.cuh", "params.cuh"]:
         with open(os.path.join(ROOT, "sparse_expert_swiglu_gb300", "csrc", fn), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -461,12 +466,18 @@ def run_ours(args, world, rank, local):
         for ev in evs:
             ev.record()
     torch.cuda.synchronize()
+    path = ses.layer_path(layers[0], B)
     prof_graphs, pstream = capture_graphs(layers, xs, ys, ws_list, events_list)
-    kt = per_kernel_times(prof_graphs, events_list, pstream, max(R * 50, args.steps // 10))
-    kernel_bytes = {"up": float(np.mean([b["up"] for b in byts])),
-                    "gather": float(np.mean([b["gather"] for b in byts])),
-                    "route": float(np.mean([b["route"] for b in byts]))}
-    dominant = max(("up", "gather"), key=lambda kname: kt[kname])
+    kt = per_kernel_times(prof_graphs, events_list, pstream, max(R * 50, args.steps // 10), path)
+    up_b = float(np.mean([b["up"] for b in byts]))
+    ga_b = float(np.mean([b["gather"] for b in byts]))
+    rt_b = float(np.mean([b["route"] for b in byts]))
+    if path == "decode":
+        # the up kernel also reads the router weight and the tokens
+        kernel_bytes = {"decode_up_kernel": up_b + rt_b, "decode_gather_kernel": ga_b}
+    else:
+        kernel_bytes = {"up_kernel": up_b, "gather_kernel": ga_b, "route_kernel": rt_b}
+    dominant = max((k for k in kernel_bytes if k in kt and k != "route_kernel"), key=lambda kname: kt[kname])
     achieved = kernel_bytes[dominant] / (kt[dominant] * 1e-6) / 1e9
     traffic = NCU_TRAFFIC.get((dominant, source_hash()))
 
@@ -521,14 +532,15 @@ def run_ours(args, world, rank, local):
         "layer_roofline": {"bytes_per_step": mean_bytes, "hbm_gbs": mean_bytes / (ms_per_step * 1e-3) / 1e9,
                            "peak": peak, "frac": mean_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
                            "peak_kind": peak_kind},
-        "roofline": {"bound": "hbm", "kernel": f"{dominant}_kernel", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "bytes_per_launch": kernel_bytes[dominant], "peak_kind": peak_kind},
         "kernel_us": kt,
         "sweep": sweep,
         "e2e": {"value": e2e_value, "unit": "expert-tokens/s", "h2d_bytes_per_step": B * d * 2,
                 "d2h_bytes_per_step": B * d * 2},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (3 if path == "decode" else 4) * args.steps,
+        "path": path,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
     }

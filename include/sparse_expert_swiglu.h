@@ -209,6 +209,15 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
                               int32_t rmsnorm_out, const moe_debug_t* dbg, void* ws,
                               size_t ws_bytes, void* stream);
 
+/*
+ * moe_layer_path -- which kernels moe_layer_decode runs for this layer and B tokens on
+ * the current device: 1 = the decode path (one or two tokens, 8/16/32 routed experts,
+ * d <= 4096: an up-projection kernel that also routes, a gather kernel and a combine
+ * kernel), 0 = the general path (router, up-projection, gather and combine kernels),
+ * or a negative moe_status_t for an invalid layer.  Both paths compute the same layer.
+ */
+int32_t moe_layer_path(const moe_layer_t* layer, int32_t B);
+
 /* ---------------- workspace and status ---------------- */
 
 /* Zero-fills `ws` on `stream` (required once after allocating a workspace). */

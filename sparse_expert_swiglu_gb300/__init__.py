@@ -14,6 +14,7 @@ from ._lib import (  # noqa: F401
     expert_sparse_swiglu,
     expert_workspace_bytes,
     layer_decode,
+    layer_path,
     layer_workspace_bytes,
     lib,
     lib_path,

@@ -75,6 +75,7 @@ _SIGS = {
     "moe_layer_decode": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(_Layer),
                                         ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(_Debug),
                                         ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_layer_path": (ctypes.c_int32, [ctypes.POINTER(_Layer), ctypes.c_int32]),
     "moe_workspace_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_get_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -361,6 +362,14 @@ def expert_sparse_swiglu(x: torch.Tensor, experts: Experts, expert: int,
 def layer_workspace_bytes(layer: Layer, B: int) -> int:
     c = layer.c_struct()
     return int(lib().moe_layer_workspace_bytes(ctypes.byref(c), B))
+
+
+def layer_path(layer: Layer, B: int) -> str:
+    """'decode' (one or two tokens: up, gather, combine kernels) or 'general'."""
+    r = int(lib().moe_layer_path(ctypes.byref(layer.c_struct()), B))
+    if r < 0:
+        raise MoeError("moe_layer_path", r)
+    return "decode" if r == 1 else "general"
 
 
 def layer_decode(x: torch.Tensor, layer: Layer, rmsnorm: bool = False,

@@ -327,6 +327,24 @@ size_t moe_layer_workspace_bytes(const moe_layer_t* layer, int32_t B) {
   return layer_layout(layer, B, di.sms).total;
 }
 
+// The decode path applies: shapes it handles and a shared-memory plan that fits.
+static bool use_decode_path(const moe_layer_t* layer, int B, const DeviceInfo& di, int& su, int& sr,
+                            int& cap) {
+  const int k = layer->k, P = di.sms;
+  cap = decode_list_cap(B, layer->routed.f, k, layer->shared.E, P);
+  return decode_supported(B, layer->routed.d, layer->routed.f, layer->routed.E, k, layer->shared.E, P) &&
+         decode_plan(B, layer->routed.d, layer->routed.E, cap, P, di.smem_optin, su, sr);
+}
+
+int32_t moe_layer_path(const moe_layer_t* layer, int32_t B) {
+  moe_status_t s = check_layer(layer, B);
+  if (s != MOE_OK) return s;
+  DeviceInfo di;
+  if (device_info(di) != cudaSuccess) return MOE_ERR_CUDA;
+  int su = 0, sr = 0, cap = 0;
+  return B >= 1 && use_decode_path(layer, B, di, su, sr, cap) ? 1 : 0;
+}
+
 moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* layer, uint16_t* y,
                               int32_t rmsnorm_out, const moe_debug_t* dbg, void* ws,
                               size_t ws_bytes, void* stream) {
@@ -343,10 +361,8 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
   cudaStream_t st = (cudaStream_t)stream;
   const int k = layer->k;
   const int P = di.sms;
-  int su = 0, sr = 0;
-  const int cap = decode_list_cap(B, layer->routed.f, k, layer->shared.E, P);
-  if (decode_supported(B, layer->routed.d, layer->routed.f, layer->routed.E, k, layer->shared.E, P) &&
-      decode_plan(B, layer->routed.d, layer->routed.E, cap, P, di.smem_optin, su, sr)) {
+  int su = 0, sr = 0, cap = 0;
+  if (use_decode_path(layer, B, di, su, sr, cap)) {
     // one or two tokens: up kernel, gather kernel, combine kernel
     DecodeParams dp = {};
     dp.x = reinterpret_cast<const __half*>(x);

@@ -359,6 +359,22 @@ def test_layer_interleaved_gate_down(B):
     run_layer_case(1024, 352, 8, 2, B, 1, [0, 70], seed=40 + B, interleave=True)
 
 
+def test_layer_path_selection():
+    """One or two tokens with 8/16/32 routed experts and d <= 4096 take the decode
+    kernels; other shapes take the general path."""
+    def layer(d, f, E):
+        de = synth.experts(E, d, f, 50)
+        ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(),
+                                    torch.zeros(E, dtype=torch.float32).cuda())
+        return ses.Layer(synth.router(d, E, 50).cuda(), ex, 2)
+    small = layer(1024, 256, 8)
+    assert ses.layer_path(small, 1) == "decode"
+    assert ses.layer_path(small, 2) == "decode"
+    assert ses.layer_path(small, 3) == "general"
+    assert ses.layer_path(layer(1024, 256, 64), 1) == "general"
+    assert ses.layer_path(layer(6144, 256, 8), 1) == "general"
+
+
 def test_decode_repeated_calls_share_the_workspace():
     """The unit counter of the decode kernel is reset by the kernel itself: many calls
     in a row on one workspace give the same output up to fp32 summation order."""
