@@ -177,7 +177,7 @@ __device__ __forceinline__ long long muldiv(long long a, long long b, long long 
 // wr: the router weight [d][E], in shared memory.
 // ---------------------------------------------------------------------------
 template <int B>
-__device__ void dec_route(const DecodeParams& p, int nthreads, const __half* wr, const __half* xs,
+__device__ __forceinline__ void dec_route(const DecodeParams& p, int nthreads, const __half* wr, const __half* xs,
                           float* lred, UpMisc* m, GroupDesc* grp) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = nthreads / 32;
   const int E = p.routed.E, d = p.d, k = p.k;
@@ -214,28 +214,38 @@ __device__ void dec_route(const DecodeParams& p, int nthreads, const __half* wr,
       }
     }
   }
+  // warp sums by recursive halving: across lane bits 4, 3, 2 every lane keeps half of
+  // its experts and adds its partner's copy of them (8 values -> 1), then the lanes
+  // that still share an expert (bits 1 and 0 not used by the expert chunk) add up.
+  const bool u16 = (lane & 16) != 0, u8 = (lane & 8) != 0, u4 = (lane & 4) != 0;
+  const int e_in = (u16 ? 4 : 0) + (u8 ? 2 : 0) + (u4 ? 1 : 0);
 #pragma unroll
-  for (int b = 0; b < B; ++b)
+  for (int b = 0; b < B; ++b) {
+    float w4[4], w2[2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float v = acc[b][i];
+    for (int i = 0; i < 4; ++i)
+      w4[i] = (u16 ? acc[b][i + 4] : acc[b][i]) + __shfl_xor_sync(0xffffffffu, u16 ? acc[b][i] : acc[b][i + 4], 16);
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-        if (off >= nchunk) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane < nchunk) lred[(warp * B + b) * kDecMaxE + lane * 8 + i] = v;
-    }
+    for (int i = 0; i < 2; ++i)
+      w2[i] = (u8 ? w4[i + 2] : w4[i]) + __shfl_xor_sync(0xffffffffu, u8 ? w4[i] : w4[i + 2], 8);
+    float v = (u4 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, u4 ? w2[0] : w2[1], 4);
+    if (nchunk <= 2) v += __shfl_xor_sync(0xffffffffu, v, 2);
+    if (nchunk == 1) v += __shfl_xor_sync(0xffffffffu, v, 1);
+    if ((lane & 3) < nchunk) lred[(warp * B + b) * kDecMaxE + (lane % nchunk) * 8 + e_in] = v;
+  }
   __syncthreads();
   for (int t = tid; t < B * E; t += nthreads) {
     const int b = t / E, e = t % E;
     float s = 0.f;
+#pragma unroll 6
     for (int w = 0; w < nw; ++w) s += lred[(w * B + b) * kDecMaxE + e];
     m->logits[b][e] = s;
   }
   __syncthreads();
-  if (warp < B) {
+  if (warp == 0) {
+  for (int b = 0; b < B; ++b) {
     // top-k by rank: an expert's rank counts the experts with a larger logit, or an
     // equal one and a lower index; ranks 0..k-1 are chosen, listed by rank
-    const int b = warp;
     const float l = lane < E ? m->logits[b][lane] : -INFINITY;
     int rank = 0;
     for (int e = 0; e < E; ++e) {
@@ -266,9 +276,9 @@ __device__ void dec_route(const DecodeParams& p, int nthreads, const __half* wr,
         }
       }
     }
+    __syncwarp();
   }
-  __syncthreads();
-  if (warp == 0) {
+    // groups
     const int np = B * k;
     int e = -1, bb = 0, jj = 0;
     float ww = 0.f;
@@ -453,7 +463,7 @@ __device__ __forceinline__ void dec_superblock(const uint8_t* __restrict__ blk,
 // appended at out in ascending order: {column | group << 16, v per group token (0 for a
 // token that drops the column)}.  Returns the number of kept columns.
 template <int T>
-__device__ int dec_finalize(const DecodeParams& p, const float4* vpart, int nsb, const GroupDesc& gd,
+__device__ __forceinline__ int dec_finalize(const DecodeParams& p, const float4* vpart, int nsb, const GroupDesc& gd,
                             int g, int mt, float thr, float* vbuf, int4* out) {
   constexpr int G = 8 / T;
   const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
