@@ -418,7 +418,7 @@ __device__ __forceinline__ void dec_groups(const uint4 (&w)[4], const uint32_t (
 
 template <int T, int PH>
 __device__ __forceinline__ void dec_phases(const uint4 (&w)[4], const uint32_t (&xr)[T][4][2],
-                                           const uint8_t* __restrict__ szt, const float* xgw,
+                                           const uint32_t (&sz)[T][2][2], const float* xgw,
                                            int ng, float (&vacc)[2][2]) {
   if constexpr (PH < T) {
     constexpr int G = 8 / T;
@@ -436,26 +436,35 @@ __device__ __forceinline__ void dec_phases(const uint4 (&w)[4], const uint32_t (
         const float X = xgw[tau * 8 + gi];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const __half2 h = *reinterpret_cast<const __half2*>(szt + ((gl + 8 * r) * 8 + gi) * 4);
+          const __half2 h = *reinterpret_cast<const __half2*>(&sz[PH][s][r]);
           const float sf = __low2float(h), zf = __high2float(h);
           const float acc = (D[0][2 * r + s] + D[1][2 * r + s]) + (D[2][2 * r + s] + D[3][2 * r + s]);
           vacc[r][s] = fmaf(sf, fmaf(-zf, X, acc * cs), vacc[r][s]);
         }
       }
     }
-    dec_phases<T, PH + 1>(w, xr, szt, xgw, ng, vacc);
+    dec_phases<T, PH + 1>(w, xr, sz, xgw, ng, vacc);
   }
 }
 
+// This lane's codes and (scale, zero) pairs of one superblock block, copied out of the
+// stage so that the stage can be refilled while the dot products run.
 template <int T>
-__device__ __forceinline__ void dec_superblock(const uint8_t* __restrict__ blk,
-                                               const uint32_t (&xr)[T][4][2], const float* xgw,
-                                               int ng, float (&vacc)[2][2]) {
-  const int lane = threadIdx.x & 31;
-  uint4 w[4];
+__device__ __forceinline__ void dec_load_block(const uint8_t* __restrict__ blk, uint4 (&w)[4],
+                                               uint32_t (&sz)[T][2][2]) {
+  constexpr int G = 8 / T;
+  const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
 #pragma unroll
   for (int q = 0; q < 4; ++q) w[q] = reinterpret_cast<const uint4*>(blk)[q * 32 + lane];
-  dec_phases<T, 0>(w, xr, blk + kBlkCodeBytes, xgw, ng, vacc);
+  const uint8_t* szt = blk + kBlkCodeBytes;
+  const int gi_lane = (2 * c) % G;
+#pragma unroll
+  for (int ph = 0; ph < T; ++ph)
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        sz[ph][s][r] = *reinterpret_cast<const uint32_t*>(szt + ((gl + 8 * r) * 8 + ph * G + gi_lane + s) * 4);
 }
 
 // The superblock partials of one unit added in a fixed order, per-token v of its 16
@@ -676,13 +685,16 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
         dec_up_setup<B>(xs, d, grp[g], sb, ng, xr, xgw);
         cur_g = g;
       }
-      float vacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-      dec_superblock<B>(ring + (size_t)s * L.strip + (size_t)sb * kBlkBytes, xr, xgw, ng, vacc);
+      uint4 w[4];
+      uint32_t sz[B][2][2];
+      dec_load_block<B>(ring + (size_t)s * L.strip + (size_t)sb * kBlkBytes, w, sz);
       __syncwarp();
       if (lane == 0) {
         if (sb == 0) m->pend[s] = 0;
-        mbar_arrive(&empty[s]);
+        mbar_arrive(&empty[s]);  // release: the copies above are done before the stage is reused
       }
+      float vacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      dec_phases<B, 0>(w, xr, sz, xgw, ng, vacc);
       // the slot's previous unit must have been finalized
       if (j >= kDecNV &&
           !__all_sync(0xffffffffu, mbar_wait(&vfree[slot], ((j >> 2) - 1) & 1))) {
@@ -902,6 +914,15 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
         }
       }
     }
+    // this thread's slice of every down row, then the stages can be refilled at once
+    uint4 dn[kDecRows];
+#pragma unroll
+    for (int q = 0; q < kDecRows; ++q)
+      dn[q] = (q < nb && ok) ? reinterpret_cast<const uint4*>(ring + (size_t)st[q] * L.row + 2 * d)[tid]
+                             : make_uint4(0, 0, 0, 0);
+    __syncwarp();
+    if (lane == 0)
+      for (int q = 0; q < nb; ++q) mbar_arrive(&empty[st[q]]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
@@ -949,8 +970,7 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
 #pragma unroll
     for (int q = 0; q < kDecRows; ++q) {
       if (q < nb) {
-        const uint4 dr = reinterpret_cast<const uint4*>(ring + (size_t)st[q] * L.row + 2 * d)[tid];
-        const __half2* dh = reinterpret_cast<const __half2*>(&dr);
+        const __half2* dh = reinterpret_cast<const __half2*>(&dn[q]);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 df = __half22float2(dh[e]);
@@ -962,9 +982,6 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
         }
       }
     }
-    __syncwarp();
-    if (lane == 0)
-      for (int q = 0; q < nb; ++q) mbar_arrive(&empty[st[q]]);
   }
   // this CTA's partial output (every CTA writes one, zeros if it had no rows)
 #pragma unroll
