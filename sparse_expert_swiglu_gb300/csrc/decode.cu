@@ -140,7 +140,7 @@ __host__ __device__ inline GaLayoutD ga_layout_d(int d, int sr, int cap, int P) 
   L.off_list = o;
   o += sizeof(GaRow) * (size_t)cap;
   L.off_red = o;
-  o += (size_t)2 * kDecRows * 2 * kDecMaxGw * 4;
+  o += (size_t)2 * kDecRows * 2 * kDecMaxGw * 4 + (size_t)2 * kDecRows * 2 * 4;
   L.off_pre = o;
   o += al16(4 * ((size_t)P + 1));
   L.off_grp = o;
@@ -868,15 +868,53 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
       }
     }
   } else {
-  // ---- batches of up to kDecRows rows, one barrier per batch
+  // ---- batches of up to kDecRows rows, one barrier per batch, software-pipelined:
+  // all warps form the dot products of batch k and publish per-warp sums; after the
+  // barrier warp 0 alone turns them into h = SiLU(.) * v * w for batch k while every
+  // warp applies batch k-1 (whose h warp 0 wrote before the barrier) to its rows.
   float acc[B][8];
 #pragma unroll
   for (int b = 0; b < B; ++b)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[b][e] = 0.f;
-  int batch = 0;
+  float* hbuf = red + 2 * kDecRows * 2 * kDecMaxGw;  // [2][kDecRows][2]
   int s0 = 0, ph0 = 0;  // stage and full-barrier parity of row i0
-  for (int i0 = 0; i0 < nrows; i0 += kDecRows, ++batch) {
+  int prev_nb = 0;      // rows of the batch whose h warp 0 computed last
+  bool stop = false;
+  auto bar_or = [&](bool bad) -> bool {
+    int fail;
+    asm volatile(
+        "{\n\t.reg .pred pin, pout;\n\t"
+        "setp.ne.u32 pin, %1, 0;\n\t"
+        "barrier.red.or.pred pout, 1, %2, pin;\n\t"
+        "selp.u32 %0, 1, 0, pout;\n\t}"
+        : "=r"(fail)
+        : "r"((unsigned)bad), "r"(nct)
+        : "memory");
+    return fail != 0;
+  };
+  // acc += h (batch in parity slot par) * this thread's down slices
+  auto apply = [&](int par, int nbq, const uint4 (&dn)[kDecRows]) {
+    const float* hb = hbuf + par * kDecRows * 2;
+#pragma unroll
+    for (int q = 0; q < kDecRows; ++q) {
+      if (q < nbq) {
+        const float2 hq = *reinterpret_cast<const float2*>(hb + q * 2);
+        const float hv[2] = {hq.x, hq.y};
+        const __half2* dh = reinterpret_cast<const __half2*>(&dn[q]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 df = __half22float2(dh[e]);
+#pragma unroll
+          for (int b = 0; b < B; ++b) {
+            acc[b][2 * e] = fmaf(hv[b], df.x, acc[b][2 * e]);
+            acc[b][2 * e + 1] = fmaf(hv[b], df.y, acc[b][2 * e + 1]);
+          }
+        }
+      }
+    }
+  };
+  auto step = [&](int i0, int bt, uint4 (&dcur)[kDecRows], const uint4 (&dprev)[kDecRows]) {
     const int nb = min(kDecRows, nrows - i0);
     int st[kDecRows];
     bool ok = !vload(&m->abort);
@@ -915,11 +953,10 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
       }
     }
     // this thread's slice of every down row, then the stages can be refilled at once
-    uint4 dn[kDecRows];
 #pragma unroll
     for (int q = 0; q < kDecRows; ++q)
-      dn[q] = (q < nb && ok) ? reinterpret_cast<const uint4*>(ring + (size_t)st[q] * L.row + 2 * d)[tid]
-                             : make_uint4(0, 0, 0, 0);
+      dcur[q] = (q < nb && ok) ? reinterpret_cast<const uint4*>(ring + (size_t)st[q] * L.row + 2 * d)[tid]
+                               : make_uint4(0, 0, 0, 0);
     __syncwarp();
     if (lane == 0)
       for (int q = 0; q < nb; ++q) mbar_arrive(&empty[st[q]]);
@@ -929,60 +966,51 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
       for (int q = 0; q < kDecRows; ++q)
 #pragma unroll
         for (int b = 0; b < B; ++b) dot[q][b] += __shfl_xor_sync(0xffffffffu, dot[q][b], off);
-    float* rb = red + (size_t)(batch & 1) * kDecRows * 2 * kDecMaxGw;
+    float* rb = red + (size_t)(bt & 1) * kDecRows * 2 * kDecMaxGw;
     if (lane == 0) {
 #pragma unroll
       for (int q = 0; q < kDecRows; ++q)
 #pragma unroll
         for (int b = 0; b < B; ++b) rb[(q * 2 + b) * kDecMaxGw + warp] = dot[q][b];
     }
-    int fail;
-    asm volatile(
-        "{\n\t.reg .pred pin, pout;\n\t"
-        "setp.ne.u32 pin, %1, 0;\n\t"
-        "barrier.red.or.pred pout, 1, %2, pin;\n\t"
-        "selp.u32 %0, 1, 0, pout;\n\t}"
-        : "=r"(fail)
-        : "r"((unsigned)!ok), "r"(nct)
-        : "memory");
-    if (fail) {
+    if (bar_or(!ok)) {
       if (tid == 0) dec_fail(p, &m->abort);
-      break;
+      stop = true;
+      return;
     }
-    if (tid == 0) m->consumed = i0;
-    float h[kDecRows][B];
-#pragma unroll
-    for (int q = 0; q < kDecRows; ++q) {
-      const GaRow gr = list[min(i0 + q, nrows - 1)];
-#pragma unroll
-      for (int b = 0; b < B; ++b) {
-        h[q][b] = 0.f;
-        const int t = m->tmap[gr.g][b];
-        if (q < nb && t >= 0) {
-          const float4* pr = reinterpret_cast<const float4*>(rb + (q * 2 + b) * kDecMaxGw);
-          const float4 p0 = pr[0], p1 = pr[1], p2 = pr[2], p3 = pr[3];  // unused slots hold 0
-          const float gs = (((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w))) +
-                           (((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w)));
-          h[q][b] = silu_fast(gs) * (t == 0 ? gr.v[0] : gr.v[1]) * m->tw[gr.g][b];
-        }
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < kDecRows; ++q) {
-      if (q < nb) {
-        const __half2* dh = reinterpret_cast<const __half2*>(&dn[q]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 df = __half22float2(dh[e]);
-#pragma unroll
-          for (int b = 0; b < B; ++b) {
-            acc[b][2 * e] = fmaf(h[q][b], df.x, acc[b][2 * e]);
-            acc[b][2 * e + 1] = fmaf(h[q][b], df.y, acc[b][2 * e + 1]);
+    if (tid == 0) m->consumed = i0 + nb;
+    // the previous batch, with the h warp 0 wrote before this barrier
+    if (bt > 0) apply((bt - 1) & 1, prev_nb, dprev);
+    if (warp == 0) {
+      // h of this batch: lane q * 2 + b
+      if (lane < kDecRows * 2) {
+        const int q = lane >> 1, b = lane & 1;
+        float hq = 0.f;
+        if (q < nb && b < B) {
+          const GaRow gr = list[i0 + q];
+          const int t = m->tmap[gr.g][b];
+          if (t >= 0) {
+            const float4* pr = reinterpret_cast<const float4*>(rb + (q * 2 + b) * kDecMaxGw);
+            const float4 p0 = pr[0], p1 = pr[1], p2 = pr[2], p3 = pr[3];  // unused slots hold 0
+            const float gs = (((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w))) +
+                             (((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w)));
+            hq = silu_fast(gs) * (t == 0 ? gr.v[0] : gr.v[1]) * m->tw[gr.g][b];
           }
         }
+        hbuf[(bt & 1) * kDecRows * 2 + lane] = hq;
       }
+      __syncwarp();
     }
+    prev_nb = nb;
+  };
+  uint4 dA[kDecRows], dB[kDecRows];
+  int bt = 0;
+  for (int i0 = 0; i0 < nrows && !stop; i0 += 2 * kDecRows) {
+    step(i0, bt++, dA, dB);
+    if (!stop && i0 + kDecRows < nrows) step(i0 + kDecRows, bt++, dB, dA);
   }
+  // the last batch: its h is written once warp 0 reaches the barrier
+  if (!stop && bt > 0 && !bar_or(false)) apply((bt - 1) & 1, prev_nb, (bt & 1) ? dA : dB);
   // this CTA's partial output (every CTA writes one, zeros if it had no rows)
 #pragma unroll
   for (int b = 0; b < B; ++b) {
