@@ -1099,12 +1099,12 @@ __global__ void __launch_bounds__(kCombThr) decode_combine_kernel(DecodeParams p
   if constexpr (RMS) {
     if (tid == 0) {
       p.sumsq[(size_t)b * ns + slice] = ss;
-      __threadfence();
-      atomicAdd(&p.tok_ctr[b], 1);
+      // release: the sum above is visible to whoever sees the count
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.tok_ctr[b]) : "memory");
       bool done = false;
-      for (int it = 0; it < (1 << 26) && !done; ++it) {
+      for (int it = 0; it < (1 << 27) && !done; ++it) {
         done = ld_acquire(&p.tok_ctr[b]) >= ns;
-        if (!done) __nanosleep(64);
+        if (!done) __nanosleep(32);
       }
       if (!done) set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
     }
@@ -1118,16 +1118,16 @@ __global__ void __launch_bounds__(kCombThr) decode_combine_kernel(DecodeParams p
     }
     __syncthreads();
     rinv = s_rinv;
-    // the last CTA of the token to have read the sums resets both counters
-    if (tid == 0 && atomicAdd(&p.tok_ctr[p.B + b], 1) == ns - 1) {
-      p.tok_ctr[b] = 0;
-      p.tok_ctr[p.B + b] = 0;
-    }
   }
   if (tid < 8) {
     __half2* yo = reinterpret_cast<__half2*>(p.y + (size_t)b * d + col);
     yo[0] = __floats2half2_rn(y.x * rinv, y.y * rinv);
     yo[1] = __floats2half2_rn(y.z * rinv, y.w * rinv);
+  }
+  // the last CTA of the token to have read the sums resets both counters
+  if (RMS && tid == 0 && atomicAdd(&p.tok_ctr[p.B + b], 1) == ns - 1) {
+    p.tok_ctr[b] = 0;
+    p.tok_ctr[p.B + b] = 0;
   }
 }
 
