@@ -101,8 +101,9 @@ typedef struct {
                           before the gather kernel, before the combine kernel and after it;
                           for per-kernel timing.  Recording them serialises the kernels.
                           On the decode path (moe_layer_decode with 1 or 2 tokens) the
-                          router runs inside the up-projection kernel: events 0 and 1 are
-                          recorded back to back. */
+                          router runs inside the up-projection kernel and the combination
+                          inside the gather kernel: events 0 and 1, and events 3 and 4,
+                          are recorded back to back. */
 } moe_debug_t;
 
 /* ---------------- INT2 up projection ---------------- */
@@ -212,9 +213,12 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
 /*
  * moe_layer_path -- which kernels moe_layer_decode runs for this layer and B tokens on
  * the current device: 1 = the decode path (one or two tokens, 8/16/32 routed experts,
- * d <= 4096: an up-projection kernel that also routes, a gather kernel and a combine
- * kernel), 0 = the general path (router, up-projection, gather and combine kernels),
+ * d <= 4096: an up-projection kernel that also routes and a gather kernel that also
+ * combines), 0 = the general path (router, up-projection, gather and combine kernels),
  * or a negative moe_status_t for an invalid layer.  Both paths compute the same layer.
+ * The general path is bitwise reproducible; on the decode path the experts' shares
+ * reach the fp32 sum of y in a varying order, so two calls can differ in the last
+ * bits of that sum (at most one fp16 ulp of y).
  */
 int32_t moe_layer_path(const moe_layer_t* layer, int32_t B);
 

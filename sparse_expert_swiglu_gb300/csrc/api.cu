@@ -44,7 +44,7 @@ int groups_max_routed(int B, int E, int k, int gcap) {
 // Workspace carving shared by every entry point.
 struct WsLayout {
   size_t ctrl, groups, tok_groups, topk_idx, topk_w, group_total, unit_cnt, item_col, item_v,
-      part, sumsq, tok_ctr, cta_total, klist, total;
+      part, yacc, cta_total, klist, total;
   int G_max, P3, list_cap;
 };
 
@@ -71,8 +71,7 @@ WsLayout ws_layout(int B, int npairs, int G_max, int d, int f, int P3) {
   L.item_col = take(sizeof(int) * (size_t)G_max * MT * 16);
   L.item_v = take(sizeof(float) * (size_t)G_max * MT * 16 * 8);
   L.part = take(sizeof(float) * (size_t)(P3 + G_max) * kMaxTok * d);
-  L.sumsq = take(sizeof(float) * (size_t)B * (d / 32));
-  L.tok_ctr = take(sizeof(int) * (size_t)2 * B);
+  L.yacc = take(sizeof(float) * (size_t)B * d);
   L.cta_total = take(sizeof(int) * (size_t)P3);
   // decode path: per up CTA, 16 entries of 16 bytes for each of its units
   L.klist = take((size_t)P3 * (((size_t)G_max * MT + P3 - 1) / P3) * 16 * 16);
@@ -363,7 +362,7 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
   const int P = di.sms;
   int su = 0, sr = 0, cap = 0;
   if (use_decode_path(layer, B, di, su, sr, cap)) {
-    // one or two tokens: up kernel, gather kernel, combine kernel
+    // one or two tokens: up kernel, gather kernel
     DecodeParams dp = {};
     dp.x = reinterpret_cast<const __half*>(x);
     dp.w_router = reinterpret_cast<const __half*>(layer->w_router);
@@ -380,7 +379,7 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
     dp.klist = at<int4>(ws, L.klist);
     dp.kcap = (int)((((long long)L.G_max * (layer->routed.f / kMTile)) + P - 1) / P) * 16;
     dp.cta_total = at<int>(ws, L.cta_total);
-    dp.part = at<float>(ws, L.part);
+    dp.yacc = at<float>(ws, L.yacc);
     dp.P = P;
     dp.list_cap = cap;
     dp.topk_idx = at<int32_t>(ws, L.topk_idx);
@@ -394,16 +393,14 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
     dp.sr = sr;
     dp.y = reinterpret_cast<__half*>(y);
     dp.rmsnorm = rmsnorm_out ? 1 : 0;
-    dp.sumsq = at<float>(ws, L.sumsq);
-    dp.tok_ctr = at<int>(ws, L.tok_ctr);
-    // the router runs inside the up kernel: events 0 and 1 mark the same point
+    // the router runs inside the up kernel and the combination inside the gather kernel:
+    // events 0 and 1, and 3 and 4, mark the same points
     cudaError_t e = record(dbg, 0, st);
     if (e == cudaSuccess) e = record(dbg, 1, st);
     if (e == cudaSuccess) e = launch_decode_up(dp, st, true);
     if (e == cudaSuccess) e = record(dbg, 2, st);
     if (e == cudaSuccess) e = launch_decode_gather(dp, st, true);
     if (e == cudaSuccess) e = record(dbg, 3, st);
-    if (e == cudaSuccess) e = launch_decode_combine(dp, st, true);
     if (e == cudaSuccess) e = record(dbg, 4, st);
     return cuda_status(e);
   }

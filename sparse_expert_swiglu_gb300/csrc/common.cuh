@@ -88,7 +88,8 @@ struct Ctrl {
   int work;          // next unclaimed unit of the decode kernel
   int N;             // total kept items of the current call (written by the gather kernel)
   int work_done;     // decode CTAs that have claimed their last unit
-  int pad1[2];
+  int gdone;         // decode gather CTAs that have added their share of y
+  int pad1;
 };
 
 __device__ inline void set_status(int* status, int code) { atomicCAS(status, 0, code); }

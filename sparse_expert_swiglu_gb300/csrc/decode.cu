@@ -1,6 +1,6 @@
 // Decode path for one or two tokens: the MoE layer of "FloE: On-the-Fly MoE
 // Inference on Memory-constrained GPU" (sec. 三 "系统协同优化", Algorithm 1
-// "Efficient Sparse Kernel" for every chosen expert) as three kernels chained by
+// "Efficient Sparse Kernel" for every chosen expert) as two kernels chained by
 // programmatic dependent launch:
 //
 //   decode_up_kernel      one CTA per SM.  Routes the tokens (router GEMV from a copy
@@ -17,13 +17,17 @@
 //                         (group, column) order: their gate and down rows stream
 //                         through a TMA ring; 16 warps form x . gate for a batch of
 //                         rows (one barrier per batch), h = SiLU(.) * v * router
-//                         weight, acc += h * down, and write the CTA's partial sum.
-//   decode_combine_kernel adds the partial sums in a fixed order, rounds to fp16 once
-//                         and applies the RMSNorm of stacked layers.
+//                         weight, acc += h * down; each CTA adds its share of y to an
+//                         fp32 accumulator with vector atomics and the last CTA to
+//                         finish rounds y to fp16 once, after the RMSNorm of stacked
+//                         layers.
 //
-// Shares and orders are fixed, so the result is bitwise reproducible.  Every wait is
-// bounded; on expiry a CTA records MOE_ERR_TIMEOUT, stops, and waits (bounded) for
-// its copies in flight before it exits.
+// Every CTA's share and every order inside a CTA are fixed; only the order in which
+// the CTAs' shares reach the fp32 accumulator varies, so y can differ between calls
+// in the last bits of the fp32 sum (and by one fp16 ulp where that sum sits on a
+// rounding boundary).  Every wait is bounded; on expiry a CTA records
+// MOE_ERR_TIMEOUT, stops, and waits (bounded) for its copies in flight before it
+// exits.
 #include "params.cuh"
 
 namespace sesg {
@@ -42,8 +46,6 @@ constexpr int kDecMaxGw = 16;    // gather warps
 constexpr int kUpThreads = (2 * kDecMaxSb + 2) * 32;  // up warps, strip producer, finalize warp
 constexpr int kGaThreads = (kDecMaxGw + 1) * 32;      // gather warps + the row producer warp
 constexpr int kDecMaxD = 4096;
-constexpr int kCombCols = 32;    // hidden elements per combine CTA
-constexpr int kCombThr = 256;
 
 __host__ __device__ inline size_t al16(size_t o) { return (o + 15) & ~(size_t)15; }
 
@@ -107,6 +109,7 @@ struct GaRow {
 
 struct GaMisc {
   int abort;
+  int last;                    // this CTA finished last
   int G;
   int c0;                      // up CTA whose list holds this CTA's first row
   int issued;                  // rows issued (0 .. issued-1)
@@ -163,6 +166,11 @@ __device__ __forceinline__ int vload(const int* p) { return *reinterpret_cast<co
 __device__ __forceinline__ void dec_fail(const DecodeParams& p, int* abort_flag) {
   set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
   atomicExch(abort_flag, 1);
+}
+
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
 }
 
 // SiLU with the fast division (2 ulp): g / (1 + e^-g)
@@ -583,6 +591,11 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
   __syncthreads();
   griddep_wait();
   griddep_launch_dependents();
+  // the gather kernel's fp32 accumulator of y and its finish counter start at zero
+  // (the previous kernel, which may be the last call's gather kernel, has finished)
+  for (int i = blockIdx.x * nthreads + tid; i < p.B * p.d / 4; i += gridDim.x * nthreads)
+    reinterpret_cast<float4*>(p.yacc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (blockIdx.x == 0 && tid == 0) p.ctrl->gdone = 0;
   for (int i = tid; i < B * d / 8; i += nthreads)
     reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
   const bool wok = mbar_wait(wbar, 0);
@@ -1011,126 +1024,59 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
   }
   // the last batch: its h is written once warp 0 reaches the barrier
   if (!stop && bt > 0 && !bar_or(false)) apply((bt - 1) & 1, prev_nb, (bt & 1) ? dA : dB);
-  // this CTA's partial output (every CTA writes one, zeros if it had no rows)
+  // this CTA's share of y, added in fp32 (the order of the CTAs' additions varies)
 #pragma unroll
   for (int b = 0; b < B; ++b) {
-    float4* dst = reinterpret_cast<float4*>(p.part + ((size_t)blockIdx.x * B + b) * d + tid * 8);
-    dst[0] = make_float4(acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
-    dst[1] = make_float4(acc[b][4], acc[b][5], acc[b][6], acc[b][7]);
+    float* dst = p.yacc + (size_t)b * d + tid * 8;
+    red_add_v4(dst, acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
+    red_add_v4(dst + 4, acc[b][4], acc[b][5], acc[b][6], acc[b][7]);
   }
+  __threadfence();
   }
   __syncthreads();
+  // the last CTA to finish: y = fp16(sum) or, for stacked layers, the RMSNorm
+  // y / sqrt(mean(y^2) + 1e-6) of it
+  if (tid == 0) m->last = atomicAdd(&p.ctrl->gdone, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (m->last) {
+    __threadfence();
+    float* ss = red;  // [B][warps]
+    for (int b = 0; b < B; ++b) {
+      float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+      float sq = 0.f;
+      if (tid < d / 8) {
+        const float4* src = reinterpret_cast<const float4*>(p.yacc + (size_t)b * d + tid * 8);
+        v0 = __ldcg(src);
+        v1 = __ldcg(src + 1);
+        sq = ((v0.x * v0.x + v0.y * v0.y) + (v0.z * v0.z + v0.w * v0.w)) +
+             ((v1.x * v1.x + v1.y * v1.y) + (v1.z * v1.z + v1.w * v1.w));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+      if (lane == 0) ss[warp] = sq;
+      __syncthreads();
+      float rinv = 1.f;
+      if (p.rmsnorm) {
+        float t = 0.f;
+        for (int w = 0; w < L.nwarps; ++w) t += ss[w];
+        rinv = rsqrtf(t / (float)d + 1e-6f);
+      }
+      if (tid < d / 8) {
+        __half2* yo = reinterpret_cast<__half2*>(p.y + (size_t)b * d + tid * 8);
+        yo[0] = __floats2half2_rn(v0.x * rinv, v0.y * rinv);
+        yo[1] = __floats2half2_rn(v0.z * rinv, v0.w * rinv);
+        yo[2] = __floats2half2_rn(v1.x * rinv, v1.y * rinv);
+        yo[3] = __floats2half2_rn(v1.z * rinv, v1.w * rinv);
+      }
+      __syncthreads();
+    }
+  }
   if (m->abort && tid == 0) {
     // wait (bounded) for the rows still in flight before the CTA exits
     for (int i = max(m->consumed, m->issued - SR); i < m->issued; ++i)
       (void)mbar_wait(&full[i % SR], (i / SR) & 1);
   }
 }
-
-// ---------------------------------------------------------------------------
-// Sum of the per-CTA partials (fixed order), the single fp16 rounding and, for
-// stacked layers, y / sqrt(mean(y^2) + 1e-6).  Every CTA owns 32 hidden elements of
-// one token.  With RMSNorm the CTAs of a token publish their sums of squares, wait
-// (bounded) until all of them have, and scale their own elements: all CTAs of the
-// grid are resident together (a few small CTAs per SM), so the wait always ends.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-template <bool RMS>
-__global__ void __launch_bounds__(kCombThr) decode_combine_kernel(DecodeParams p) {
-  __shared__ float4 s_red[kCombThr / 32][8];
-  __shared__ float s_rinv;
-  griddep_wait();
-  griddep_launch_dependents();
-  const int slice = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int d = p.d, ns = d / kCombCols;
-  constexpr int NSUB = kCombThr / 8;  // subsets of the partial rows: 8 float4 columns per row
-  const int f4 = tid & 7, sub = tid >> 3;
-  const int col = slice * kCombCols + f4 * 4;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  constexpr int LU = 8;
-  for (int c0 = sub; c0 < p.P; c0 += NSUB * LU) {
-    float4 v[LU];
-#pragma unroll
-    for (int u = 0; u < LU; ++u) {
-      const int c = c0 + u * NSUB;
-      v[u] = c < p.P ? __ldcg(reinterpret_cast<const float4*>(p.part + ((size_t)c * p.B + b) * d + col))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < LU; ++u) {
-      acc.x += v[u].x;
-      acc.y += v[u].y;
-      acc.z += v[u].z;
-      acc.w += v[u].w;
-    }
-  }
-  // the warp's 4 subsets of every column, then the 8 warps, in a fixed order
-#pragma unroll
-  for (int off = 8; off < 32; off <<= 1) {
-    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
-    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
-    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
-    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
-  }
-  if (lane < 8) s_red[warp][lane] = acc;
-  __syncthreads();
-  float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-  float ss = 0.f;
-  if (tid < 8) {
-    y = s_red[0][tid];
-#pragma unroll
-    for (int w = 1; w < kCombThr / 32; ++w) {
-      const float4 v = s_red[w][tid];
-      y.x += v.x;
-      y.y += v.y;
-      y.z += v.z;
-      y.w += v.w;
-    }
-    ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
-#pragma unroll
-    for (int off = 4; off > 0; off >>= 1) ss += __shfl_xor_sync(0x000000ffu, ss, off);
-  }
-  float rinv = 1.f;
-  if constexpr (RMS) {
-    if (tid == 0) {
-      p.sumsq[(size_t)b * ns + slice] = ss;
-      // release: the sum above is visible to whoever sees the count
-      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.tok_ctr[b]) : "memory");
-      bool done = false;
-      for (int it = 0; it < (1 << 27) && !done; ++it) {
-        done = ld_acquire(&p.tok_ctr[b]) >= ns;
-        if (!done) __nanosleep(32);
-      }
-      if (!done) set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      float t = 0.f;
-      for (int s = lane; s < ns; s += 32) t += __ldcg(p.sumsq + (size_t)b * ns + s);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-      if (lane == 0) s_rinv = rsqrtf(t / (float)d + 1e-6f);
-    }
-    __syncthreads();
-    rinv = s_rinv;
-  }
-  if (tid < 8) {
-    __half2* yo = reinterpret_cast<__half2*>(p.y + (size_t)b * d + col);
-    yo[0] = __floats2half2_rn(y.x * rinv, y.y * rinv);
-    yo[1] = __floats2half2_rn(y.z * rinv, y.w * rinv);
-  }
-  // the last CTA of the token to have read the sums resets both counters
-  if (RMS && tid == 0 && atomicAdd(&p.tok_ctr[p.B + b], 1) == ns - 1) {
-    p.tok_ctr[b] = 0;
-    p.tok_ctr[p.B + b] = 0;
-  }
-}
-
 
 bool decode_supported(int B, int d, int f, int E, int k, int n_shared, int P) {
   // the in-kernel router splits the experts into 1, 2 or 4 chunks of 8
@@ -1200,13 +1146,6 @@ cudaError_t launch_decode_gather(const DecodeParams& p, cudaStream_t st, bool pd
   if (e != cudaSuccess) return e;
   if (p.B == 1) return cudaLaunchKernelEx(&cfg, decode_gather_kernel<1>, p);
   return cudaLaunchKernelEx(&cfg, decode_gather_kernel<2>, p);
-}
-
-cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t st, bool pdl) {
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_cfg(dim3(p.d / kCombCols, p.B), dim3(kCombThr), 0, st, attr, pdl);
-  if (p.rmsnorm) return cudaLaunchKernelEx(&cfg, decode_combine_kernel<true>, p);
-  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<false>, p);
 }
 
 }  // namespace sesg

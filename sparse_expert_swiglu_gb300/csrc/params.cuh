@@ -49,7 +49,7 @@ struct ExpertParams {
 };
 
 // The decode path (one or two tokens): up kernel (routing, up projection, mask, kept
-// lists), gather kernel (kept gate/down rows, per-CTA partial sums), combine kernel.
+// lists) and gather kernel (kept gate/down rows, the weighted sum and RMSNorm).
 struct DecodeParams {
   const __half* x;          // [B][d]
   const __half* w_router;   // [d][E]
@@ -61,7 +61,7 @@ struct DecodeParams {
                             // {column | group << 16, v of group token 0, 1 (float bits), 0}
   int kcap;                 // entries per up CTA
   int* cta_total;           // [P] kept columns per up CTA
-  float* part;              // [P][B][d] per-CTA partial outputs of the gather kernel
+  float* yacc;              // [B][d] fp32 sum of the gather CTAs' shares (zero between calls)
   int P;                    // CTAs of the up and gather kernels (one per SM)
   int list_cap;             // rows per gather CTA, at most
   int32_t* topk_idx;        // [B][k] workspace copies (written by CTA 0)
@@ -74,8 +74,6 @@ struct DecodeParams {
   int su, sr;               // depths of the up-strip ring and of the row ring
   __half* y;                // [B][d]
   int rmsnorm;
-  float* sumsq;             // [B][d/32] (RMSNorm: per-slice sums of squares)
-  int* tok_ctr;             // [2][B] (RMSNorm: slices published, slices done reading)
 };
 
 __device__ __forceinline__ const ExpertSet& expert_set(const ExpertParams& p, int expert,
@@ -113,6 +111,5 @@ int decode_list_cap(int B, int f, int k, int n_shared, int P);
 int decode_plan(int B, int d, int E, int list_cap, int P, int smem_optin, int& su, int& sr);
 cudaError_t launch_decode_up(const DecodeParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_decode_gather(const DecodeParams& p, cudaStream_t st, bool pdl);
-cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t st, bool pdl);
 
 }  // namespace sesg
