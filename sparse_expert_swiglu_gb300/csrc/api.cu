@@ -328,11 +328,12 @@ size_t moe_layer_workspace_bytes(const moe_layer_t* layer, int32_t B) {
 
 // The decode path applies: shapes it handles and a shared-memory plan that fits.
 static bool use_decode_path(const moe_layer_t* layer, int B, const DeviceInfo& di, int& su, int& sr,
-                            int& cap) {
+                            int& cap, int& umax) {
   const int k = layer->k, P = di.sms;
   cap = decode_list_cap(B, layer->routed.f, k, layer->shared.E, P);
+  umax = decode_units_max(B, layer->routed.f, k, layer->shared.E, P);
   return decode_supported(B, layer->routed.d, layer->routed.f, layer->routed.E, k, layer->shared.E, P) &&
-         decode_plan(B, layer->routed.d, layer->routed.E, cap, P, di.smem_optin, su, sr);
+         decode_plan(B, layer->routed.d, layer->routed.E, umax, cap, P, di.smem_optin, su, sr);
 }
 
 int32_t moe_layer_path(const moe_layer_t* layer, int32_t B) {
@@ -340,8 +341,8 @@ int32_t moe_layer_path(const moe_layer_t* layer, int32_t B) {
   if (s != MOE_OK) return s;
   DeviceInfo di;
   if (device_info(di) != cudaSuccess) return MOE_ERR_CUDA;
-  int su = 0, sr = 0, cap = 0;
-  return B >= 1 && use_decode_path(layer, B, di, su, sr, cap) ? 1 : 0;
+  int su = 0, sr = 0, cap = 0, umax = 0;
+  return B >= 1 && use_decode_path(layer, B, di, su, sr, cap, umax) ? 1 : 0;
 }
 
 moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* layer, uint16_t* y,
@@ -360,8 +361,8 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
   cudaStream_t st = (cudaStream_t)stream;
   const int k = layer->k;
   const int P = di.sms;
-  int su = 0, sr = 0, cap = 0;
-  if (use_decode_path(layer, B, di, su, sr, cap)) {
+  int su = 0, sr = 0, cap = 0, umax = 0;
+  if (use_decode_path(layer, B, di, su, sr, cap, umax)) {
     // one or two tokens: up kernel, gather kernel
     DecodeParams dp = {};
     dp.x = reinterpret_cast<const __half*>(x);
@@ -376,6 +377,8 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
     if (layer->shared.E > 0) dp.shared = to_set(layer->shared);
     dp.ctrl = at<Ctrl>(ws, L.ctrl);
     dp.groups = at<GroupDesc>(ws, L.groups);
+    dp.gmax = L.G_max;
+    dp.umax = umax;
     dp.klist = at<int4>(ws, L.klist);
     dp.kcap = (int)((((long long)L.G_max * (layer->routed.f / kMTile)) + P - 1) / P) * 16;
     dp.cta_total = at<int>(ws, L.cta_total);

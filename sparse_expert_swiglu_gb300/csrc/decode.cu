@@ -3,16 +3,17 @@
 // "Efficient Sparse Kernel" for every chosen expert) as two kernels chained by
 // programmatic dependent launch:
 //
-//   decode_up_kernel      one CTA per SM.  Routes the tokens (router GEMV from a copy
-//                         of the router weight fetched before the previous kernel
+//   decode_up_kernel      one CTA per SM.  Routes the tokens (router GEMV on router
+//                         rows loaded into registers before the previous kernel
 //                         ends, softmax top-k, expert groups; every CTA redundantly,
 //                         the result is identical), then steps 1-2 of Algorithm 1 on a
 //                         fixed, equal share of the work units (16 output columns of
 //                         one expert): packed INT2 strips stream through a TMA ring;
 //                         16 warps, one 512-input superblock each, two units in
-//                         flight; a finalize warp adds each unit's superblock
-//                         partials in a fixed order, applies mask = |v| > t and writes
-//                         the unit's kept columns.
+//                         flight; per unit lane a finalize warp adds each unit's
+//                         superblock partials in a fixed order, applies
+//                         mask = |v| > t and stages the unit's kept columns; at the
+//                         end the CTA writes them as one list in unit order.
 //   decode_gather_kernel  one CTA per SM.  An equal share of all kept columns, in
 //                         (group, column) order: their gate and down rows stream
 //                         through a TMA ring; 16 warps form x . gate for a batch of
@@ -43,7 +44,10 @@ constexpr int kDecMaxSr = 16;    // row-ring stages
 constexpr int kDecMaxUnits = 128;  // units per CTA
 constexpr int kDecRows = 4;      // kept rows per gather batch
 constexpr int kDecMaxGw = 16;    // gather warps
-constexpr int kUpThreads = (2 * kDecMaxSb + 2) * 32;  // up warps, strip producer, finalize warp
+constexpr int kUpThreads = (2 * kDecMaxSb + 3) * 32;  // up warps, strip producer, 2 finalize warps
+// register cap of the up kernel: 96 per thread, so that 5 warps fit one SM sub-partition
+constexpr int kUpRegThreads = 640;
+static_assert(kUpThreads <= kUpRegThreads, "up kernel block exceeds its register budget");
 constexpr int kGaThreads = (kDecMaxGw + 1) * 32;      // gather warps + the row producer warp
 constexpr int kDecMaxD = 4096;
 
@@ -55,31 +59,29 @@ struct UpMisc {
   int G;
   int pend[kDecMaxSu];         // strip in flight in the stage (issue index + 1) or 0
   int total;                   // kept columns of this CTA's units
-  float logits[2][kDecMaxE];
   int tidx[2][kMaxTok];
-  float tlog[2][kMaxTok];
   float tw[2][kMaxTok];
   float vbuf[kDecNV][16 * 2];
+  int ucnt[kDecMaxUnits];      // kept columns of each unit, then their list offsets
 };
 
 struct UpLayoutD {
   int nsb, nwarps, su;
-  size_t strip, wr_bytes, ring;
-  size_t off_bar, off_misc, off_ring, off_x, off_vpart, off_xg, off_grp, off_lred, total;
+  size_t strip, ring;
+  size_t off_bar, off_misc, off_ring, off_x, off_vpart, off_xg, off_grp, off_lred, off_ent, total;
 };
 
-__host__ __device__ inline UpLayoutD up_layout_d(int d, int B, int E, int su) {
+// umax: units per CTA, at most
+__host__ __device__ inline UpLayoutD up_layout_d(int d, int B, int E, int su, int umax) {
   UpLayoutD L;
   L.nsb = n_superblocks(d);
-  L.nwarps = 2 * L.nsb + 2;
+  L.nwarps = 2 * L.nsb + 3;
   L.su = su;
   L.strip = (size_t)L.nsb * kBlkBytes;
-  L.wr_bytes = (size_t)d * E * 2;
   L.ring = L.strip * su;
-  if (L.ring < L.wr_bytes) L.ring = L.wr_bytes;
   size_t o = 0;
   L.off_bar = o;
-  o += 8 * (size_t)(2 * kDecMaxSu + 2 * kDecNV + 1);
+  o += 8 * (size_t)(2 * kDecMaxSu + 2 * kDecNV);
   o = al16(o);
   L.off_misc = o;
   o += al16(sizeof(UpMisc));
@@ -96,6 +98,8 @@ __host__ __device__ inline UpLayoutD up_layout_d(int d, int B, int E, int su) {
   o += al16(sizeof(GroupDesc) * kDecMaxG);
   L.off_lred = o;
   o += (size_t)L.nwarps * 2 * kDecMaxE * 4;
+  L.off_ent = o;
+  o += (size_t)umax * 16 * 16;
   L.total = o;
   return L;
 }
@@ -111,7 +115,6 @@ struct GaMisc {
   int abort;
   int last;                    // this CTA finished last
   int G;
-  int c0;                      // up CTA whose list holds this CTA's first row
   int issued;                  // rows issued (0 .. issued-1)
   int consumed;                // rows whose stages are free again
   int tmap[kDecMaxG][2];       // group token of batch token b, -1 if none
@@ -181,42 +184,91 @@ __device__ __forceinline__ long long muldiv(long long a, long long b, long long 
 // ---------------------------------------------------------------------------
 // Routing (all threads of the CTA): logits, softmax top-k, groups.  Ties between
 // equal logits go to the lower expert index; groups are the chosen experts in
-// ascending order, each with its tokens in ascending order, then the shared experts.
-// wr: the router weight [d][E], in shared memory.
+// ascending index order, then the shared experts.
+//
+// Thread t owns the router rows rs + u * nrs (u < kRouteRows per pass) of expert chunk
+// ec (8 experts, 16 bytes per row); the first pass's rows are loaded before the
+// dependency wait (the router weight is not written by the previous kernel).  The
+// products x * W_r are formed by fma.rn.f32.f16 on the fp16 values as stored: the
+// exact product rounded once into the fp32 sum, without conversions.
 // ---------------------------------------------------------------------------
+constexpr int kRouteRows = 8;
+
+template <int HA, int HB>
+__device__ __forceinline__ float fma_f16(uint32_t a, uint32_t b, float c) {
+  float r;
+  if constexpr (HA == 0 && HB == 0)
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %3;\n\t}" : "=f"(r) : "r"(a), "r"(b), "f"(c));
+  else if constexpr (HA == 0 && HB == 1)
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b1, %3;\n\t}" : "=f"(r) : "r"(a), "r"(b), "f"(c));
+  else if constexpr (HA == 1 && HB == 0)
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a1, b0, %3;\n\t}" : "=f"(r) : "r"(a), "r"(b), "f"(c));
+  else
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a1, b1, %3;\n\t}" : "=f"(r) : "r"(a), "r"(b), "f"(c));
+  return r;
+}
+
+struct RouteSplit {
+  int nchunk, ec, rs, nrs;
+};
+
+__device__ __forceinline__ RouteSplit route_split(int E, int nthreads) {
+  RouteSplit r;
+  r.nchunk = E / 8;
+  r.ec = (int)threadIdx.x % r.nchunk;
+  r.rs = (int)threadIdx.x / r.nchunk;
+  r.nrs = nthreads / r.nchunk;
+  return r;
+}
+
+// the first pass's router rows of this thread (zero past d)
+__device__ __forceinline__ void route_prefetch(const DecodeParams& p, const RouteSplit& rt, uint4 (&wv)[kRouteRows]) {
+  const int E = p.routed.E, d = p.d;
+#pragma unroll
+  for (int u = 0; u < kRouteRows; ++u) {
+    const int r = rt.rs + u * rt.nrs;
+    wv[u] = r < d ? __ldg(reinterpret_cast<const uint4*>(p.w_router + (size_t)r * E + rt.ec * 8))
+                  : make_uint4(0, 0, 0, 0);
+  }
+}
+
 template <int B>
-__device__ __forceinline__ void dec_route(const DecodeParams& p, int nthreads, const __half* wr, const __half* xs,
-                          float* lred, UpMisc* m, GroupDesc* grp) {
+__device__ __forceinline__ void dec_route(const DecodeParams& p, int nthreads, const RouteSplit& rt,
+                                          const uint4 (&wv0)[kRouteRows], const __half* xs, float* lred,
+                                          UpMisc* m, GroupDesc* grp) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = nthreads / 32;
   const int E = p.routed.E, d = p.d, k = p.k;
-  const int nchunk = E / 8;
-  const int ec = tid % nchunk, rs = tid / nchunk, nrs = nthreads / nchunk;
+  const int nchunk = rt.nchunk;
   float acc[B][8];
 #pragma unroll
   for (int b = 0; b < B; ++b)
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[b][i] = 0.f;
-  constexpr int RU = 8;
-  for (int r0 = rs; r0 < d; r0 += RU * nrs) {
-    uint4 wv[RU];
+  for (int r0 = rt.rs, pass = 0; r0 < d; r0 += kRouteRows * rt.nrs, ++pass) {
+    uint4 wv[kRouteRows];
 #pragma unroll
-    for (int u = 0; u < RU; ++u) {
-      const int r = r0 + u * nrs;
-      wv[u] = r < d ? *reinterpret_cast<const uint4*>(wr + (size_t)r * E + ec * 8) : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < kRouteRows; ++u) {
+      const int r = r0 + u * rt.nrs;
+      wv[u] = pass == 0 ? wv0[u]
+                        : (r < d ? __ldg(reinterpret_cast<const uint4*>(p.w_router + (size_t)r * E + rt.ec * 8))
+                                 : make_uint4(0, 0, 0, 0));
     }
 #pragma unroll
-    for (int u = 0; u < RU; ++u) {
-      const int r = r0 + u * nrs;
+    for (int u = 0; u < kRouteRows; ++u) {
+      const int r = r0 + u * rt.nrs;
       if (r < d) {
-        const __half2* h2 = reinterpret_cast<const __half2*>(&wv[u]);
+        const uint32_t w4[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
 #pragma unroll
         for (int b = 0; b < B; ++b) {
-          const float xv = __half2float(xs[(size_t)b * d + r]);
+          const uint32_t xh = *reinterpret_cast<const unsigned short*>(xs + (size_t)b * d + r);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float2 wf = __half22float2(h2[i]);
-            acc[b][2 * i] = fmaf(xv, wf.x, acc[b][2 * i]);
-            acc[b][2 * i + 1] = fmaf(xv, wf.y, acc[b][2 * i + 1]);
+            acc[b][2 * i] = fma_f16<0, 0>(xh, w4[i], acc[b][2 * i]);
+            acc[b][2 * i + 1] = fma_f16<0, 1>(xh, w4[i], acc[b][2 * i + 1]);
           }
         }
       }
@@ -242,46 +294,41 @@ __device__ __forceinline__ void dec_route(const DecodeParams& p, int nthreads, c
     if ((lane & 3) < nchunk) lred[(warp * B + b) * kDecMaxE + (lane % nchunk) * 8 + e_in] = v;
   }
   __syncthreads();
-  for (int t = tid; t < B * E; t += nthreads) {
-    const int b = t / E, e = t % E;
-    float s = 0.f;
-#pragma unroll 6
-    for (int w = 0; w < nw; ++w) s += lred[(w * B + b) * kDecMaxE + e];
-    m->logits[b][e] = s;
-  }
-  __syncthreads();
   if (warp == 0) {
   for (int b = 0; b < B; ++b) {
+    // lane e: the logit of expert e, the warps' partial sums added in a fixed order
+    float l = -INFINITY;
+    if (lane < E) {
+      float s = 0.f;
+#pragma unroll 6
+      for (int w = 0; w < nw; ++w) s += lred[(w * B + b) * kDecMaxE + lane];
+      l = s;
+    }
     // top-k by rank: an expert's rank counts the experts with a larger logit, or an
     // equal one and a lower index; ranks 0..k-1 are chosen, listed by rank
-    const float l = lane < E ? m->logits[b][lane] : -INFINITY;
     int rank = 0;
     for (int e = 0; e < E; ++e) {
-      const float le = m->logits[b][e];
+      const float le = __shfl_sync(0xffffffffu, l, e);
       rank += (le > l || (le == l && e < lane)) ? 1 : 0;
     }
-    if (lane < E && rank < k) {
+    const bool chosen = lane < E && rank < k;
+    const int top = __ffs(__ballot_sync(0xffffffffu, lane < E && rank == 0)) - 1;
+    const float lmax = __shfl_sync(0xffffffffu, l, top);
+    // softmax over the chosen experts (renormalised top-k) or over all E; the
+    // denominator is a fixed-order butterfly sum
+    const float ex = (lane < E && (chosen || !p.renorm)) ? expf(l - lmax) : 0.f;
+    float denom = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, off);
+    if (chosen) {
+      const float w = ex / denom;
       m->tidx[b][rank] = lane;
-      m->tlog[b][rank] = l;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      // softmax weights, the denominator summed in a fixed order
-      const float lmax = m->tlog[b][0];
-      float denom = 0.f;
-      if (p.renorm)
-        for (int j = 0; j < k; ++j) denom += expf(m->tlog[b][j] - lmax);
-      else
-        for (int e = 0; e < E; ++e) denom += expf(m->logits[b][e] - lmax);
-      for (int j = 0; j < k; ++j) {
-        const float w = expf(m->tlog[b][j] - lmax) / denom;
-        m->tw[b][j] = w;
-        if (blockIdx.x == 0) {
-          p.topk_idx[b * k + j] = m->tidx[b][j];
-          p.topk_w[b * k + j] = w;
-          if (p.user_idx) p.user_idx[b * k + j] = m->tidx[b][j];
-          if (p.user_w) p.user_w[b * k + j] = w;
-        }
+      m->tw[b][rank] = w;
+      if (blockIdx.x == 0) {
+        p.topk_idx[b * k + rank] = lane;
+        p.topk_w[b * k + rank] = w;
+        if (p.user_idx) p.user_idx[b * k + rank] = lane;
+        if (p.user_w) p.user_w[b * k + rank] = w;
       }
     }
     __syncwarp();
@@ -548,15 +595,14 @@ __device__ __forceinline__ int dec_finalize(const DecodeParams& p, const float4*
 // Up kernel.  B = tokens (1 or 2), also the group width of the tensor-core mapping.
 // ---------------------------------------------------------------------------
 template <int B>
-__global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kUpRegThreads, 1) decode_up_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t usm[];
   const int d = p.d, SU = p.su;
-  const UpLayoutD L = up_layout_d(d, B, p.routed.E, SU);
+  const UpLayoutD L = up_layout_d(d, B, p.routed.E, SU, p.umax);
   uint64_t* full = reinterpret_cast<uint64_t*>(usm + L.off_bar);
   uint64_t* empty = full + kDecMaxSu;
   uint64_t* vfull = empty + kDecMaxSu;
   uint64_t* vfree = vfull + kDecNV;
-  uint64_t* wbar = vfree + kDecNV;
   UpMisc* m = reinterpret_cast<UpMisc*>(usm + L.off_misc);
   uint8_t* ring = usm + L.off_ring;
   __half* xs = reinterpret_cast<__half*>(usm + L.off_x);
@@ -575,19 +621,17 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
       mbar_init(&vfull[v], nsb);
       mbar_init(&vfree[v], 1);
     }
-    mbar_init(wbar, 1);
     fence_barrier_init();
-    // the router weight is not written by the previous kernel: fetch it before waiting
-    mbar_arrive_expect_tx(wbar, (uint32_t)L.wr_bytes);
-    for (size_t o = 0; o < L.wr_bytes; o += 32768) {
-      const size_t n = L.wr_bytes - o < 32768 ? L.wr_bytes - o : 32768;
-      bulk_g2s(ring + o, reinterpret_cast<const uint8_t*>(p.w_router) + o, (uint32_t)n, wbar,
-               policy_evict_last());
-    }
     m->abort = 0;
     m->total = 0;
     for (int s = 0; s < kDecMaxSu; ++s) m->pend[s] = 0;
   }
+  for (int j = tid; j < kDecMaxUnits; j += nthreads) m->ucnt[j] = 0;
+  // the router weight is not written by the previous kernel: load this thread's rows
+  // of it before waiting
+  const RouteSplit rt = route_split(p.routed.E, nthreads);
+  uint4 wv[kRouteRows];
+  route_prefetch(p, rt, wv);
   __syncthreads();
   griddep_wait();
   griddep_launch_dependents();
@@ -598,35 +642,27 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
   if (blockIdx.x == 0 && tid == 0) p.ctrl->gdone = 0;
   for (int i = tid; i < B * d / 8; i += nthreads)
     reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
-  const bool wok = mbar_wait(wbar, 0);
-  if (__syncthreads_or(!wok)) {
-    if (tid == 0) {
-      set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
-      (void)mbar_wait(wbar, 0);
-    }
-    return;
-  }
-  dec_route<B>(p, nthreads, reinterpret_cast<const __half*>(ring), xs, lred, m, grp);
+  __syncthreads();
+  dec_route<B>(p, nthreads, rt, wv, xs, lred, m, grp);
   const int G = m->G;
   if (blockIdx.x == 0) {
     for (int i = tid; i < G * (int)(sizeof(GroupDesc) / 4); i += nthreads)
       reinterpret_cast<int*>(p.groups)[i] = reinterpret_cast<const int*>(grp)[i];
     if (tid == 0) p.ctrl->G = G;
   }
-  // the ring held the router weight (generic reads); the strips are written by TMA
-  fence_proxy_async_smem();
-  __syncthreads();
   const int MT = p.f / kMTile;
   const int U = G * MT;
   const int u0 = (int)muldiv(U, blockIdx.x, gridDim.x), u1 = (int)muldiv(U, blockIdx.x + 1, gridDim.x);
   const int n = u1 - u0;
 
-  if (warp == 2 * nsb + 1) {
-    // ---- finalize warp: every unit in order, once all its superblock partials are in
-    int g = u0 / MT, mt = u0 - g * MT, cur_g = -1, off = 0;
+  int4* ent = reinterpret_cast<int4*>(usm + L.off_ent);  // [unit][16] kept columns
+  if (warp > 2 * nsb) {
+    // ---- finalize warps, one per unit lane: each unit once all its superblock
+    // partials are in; its kept columns go to the unit's 16 entries
+    const int fl = warp - 2 * nsb - 1;
+    int g = (u0 + fl) / MT, mt = (u0 + fl) - g * MT, cur_g = -1;
     float thr = 0.f;
-    int4* out = p.klist + (size_t)blockIdx.x * p.kcap;
-    for (int j = 0; j < n; ++j) {
+    for (int j = fl; j < n; j += 2) {
       const int slot = j & (kDecNV - 1);
       if (!__all_sync(0xffffffffu, mbar_wait(&vfull[slot], (j >> 2) & 1))) {
         if (lane == 0) dec_fail(p, &m->abort);
@@ -638,16 +674,17 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
         thr = es.thr[el];
         cur_g = g;
       }
-      off += dec_finalize<B>(p, vpart + (size_t)slot * nsb * 32, nsb, grp[g], g, mt, thr,
-                             m->vbuf[slot], out + off);
+      const int cnt = dec_finalize<B>(p, vpart + (size_t)slot * nsb * 32, nsb, grp[g], g, mt, thr,
+                                      m->vbuf[slot], ent + (size_t)j * 16);
+      if (lane == 0) m->ucnt[j] = cnt;
       __syncwarp();
       if (lane == 0) mbar_arrive(&vfree[slot]);
-      if (++mt == MT) {
-        mt = 0;
+      mt += 2;
+      while (mt >= MT) {
+        mt -= MT;
         ++g;
       }
     }
-    if (lane == 0) m->total = off;
   } else if (warp == 2 * nsb) {
     // ---- producer warp: the strips of this CTA's units, in order
     if (lane == 0) {
@@ -730,6 +767,29 @@ __global__ void __launch_bounds__(kUpThreads, 1) decode_up_kernel(DecodeParams p
     }
   }
   __syncthreads();
+  // this CTA's list: the units' kept columns in unit order
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < n; base += 32) {
+      const int c = base + lane;
+      const int v = c < n ? m->ucnt[c] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (c < n) m->ucnt[c] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) m->total = carry;
+  }
+  __syncthreads();
+  int4* out = p.klist + (size_t)blockIdx.x * p.kcap;
+  for (int j = warp; j < n; j += L.nwarps) {
+    const int o = m->ucnt[j], c = (j + 1 < n ? m->ucnt[j + 1] : m->total) - o;
+    if (lane < c) out[o + lane] = ent[(size_t)j * 16 + lane];
+  }
   if (tid == 0) {
     if (m->abort) {
       // wait (bounded) for the strips still in flight before the CTA exits
@@ -774,29 +834,36 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
     m->consumed = 0;
   }
   for (int i = tid; i < 2 * kDecRows * 2 * kDecMaxGw; i += nthreads) red[i] = 0.f;
-  // this thread's 8 hidden elements of the tokens (x precedes the up kernel)
-  float xf[B][8];
+  // this thread's 8 hidden elements of the tokens, fp16 pairs (x precedes the up kernel)
+  uint32_t xh[B][4];
 #pragma unroll
   for (int b = 0; b < B; ++b) {
     const uint4 xv = tid < nct ? __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)b * d) + tid)
                                : make_uint4(0, 0, 0, 0);
-    const __half2* h2 = reinterpret_cast<const __half2*>(&xv);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f2 = __half22float2(h2[e]);
-      xf[b][2 * e] = f2.x;
-      xf[b][2 * e + 1] = f2.y;
-    }
+    xh[b][0] = xv.x;
+    xh[b][1] = xv.y;
+    xh[b][2] = xv.z;
+    xh[b][3] = xv.w;
   }
   griddep_wait();
   griddep_launch_dependents();
 
-  // ---- prologue: this CTA's rows [a, bnd) of the kept columns in unit order
+  // ---- prologue: this CTA's rows [a, bnd) of the kept columns in unit order.  The
+  // per-CTA kept counts, the group count and the group descriptors are loaded at once.
+  for (int c = tid; c < P; c += nthreads) pre[c] = __ldcg(p.cta_total + c);
+  {
+    const int nwords = min(p.gmax, kDecMaxG) * (int)(sizeof(GroupDesc) / 4);
+    for (int i = tid; i < nwords; i += nthreads)
+      reinterpret_cast<int*>(grp)[i] = __ldcg(reinterpret_cast<const int*>(p.groups) + i);
+    if (tid == 0) m->G = __ldcg(&p.ctrl->G);
+  }
+  __syncthreads();
   if (tid < 32) {
+    // exclusive prefix of the counts, in place; pre[P] = all kept columns
     int carry = 0;
     for (int base = 0; base < P; base += 32) {
       const int c = base + lane;
-      const int v = c < P ? __ldcg(p.cta_total + c) : 0;
+      const int v = c < P ? pre[c] : 0;
       int incl = v;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -806,21 +873,12 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
       if (c < P) pre[c] = carry + incl - v;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) {
-      pre[P] = carry;
-      m->G = __ldcg(&p.ctrl->G);
-    }
+    if (lane == 0) pre[P] = carry;
   }
   __syncthreads();
   const int N = pre[P], G = m->G;
-  for (int i = tid; i < G * (int)(sizeof(GroupDesc) / 4); i += nthreads)
-    reinterpret_cast<int*>(grp)[i] = __ldcg(reinterpret_cast<const int*>(p.groups) + i);
   const int a = (int)muldiv(N, blockIdx.x, P), bnd = (int)muldiv(N, blockIdx.x + 1, P);
   const int nrows = bnd - a;
-  // the up CTA whose list holds row a: the last c with pre[c] <= a
-  for (int c = tid; c < P; c += nthreads)
-    if (pre[c] <= a && (c + 1 == P || pre[c + 1] > a)) m->c0 = c;
-  __syncthreads();
   if (tid < G * 2) {
     const int g = tid >> 1, b = tid & 1;
     const GroupDesc& gd = grp[g];
@@ -834,20 +892,23 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
     m->tmap[g][b] = t_of_b;
     m->tw[g][b] = w;
   }
-  // rows [a, bnd): entries of up CTAs c0..c1, each list in unit order
-  {
-    const int c0 = m->c0;
-    for (int r = a + tid; r < bnd; r += nthreads) {
-      int cc = c0;
-      while (cc + 1 < P && pre[cc + 1] <= r) ++cc;
-      const int4 e = __ldcg(p.klist + (size_t)cc * p.kcap + (r - pre[cc]));
-      GaRow gr;
-      gr.col = e.x & 0xffff;
-      gr.g = e.x >> 16;
-      gr.v[0] = __int_as_float(e.y);
-      gr.v[1] = __int_as_float(e.z);
-      list[r - a] = gr;
+  // rows [a, bnd): row r is entry r - pre[c] of up CTA c, the last c with pre[c] <= r
+  for (int r = a + tid; r < bnd; r += nthreads) {
+    int lo = 0, hi = P - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= r)
+        lo = mid;
+      else
+        hi = mid - 1;
     }
+    const int4 e = __ldcg(p.klist + (size_t)lo * p.kcap + (r - pre[lo]));
+    GaRow gr;
+    gr.col = e.x & 0xffff;
+    gr.g = e.x >> 16;
+    gr.v[0] = __int_as_float(e.y);
+    gr.v[1] = __int_as_float(e.z);
+    list[r - a] = gr;
   }
   __syncthreads();
   if (warp == ngw) {
@@ -953,14 +1014,13 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
       for (int b = 0; b < B; ++b) dot[q][b] = 0.f;
       if (q < nb && ok) {
         const uint4 gr = reinterpret_cast<const uint4*>(ring + (size_t)st[q] * L.row)[tid];
-        const __half2* gh = reinterpret_cast<const __half2*>(&gr);
+        const uint32_t gw[4] = {gr.x, gr.y, gr.z, gr.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float2 gf = __half22float2(gh[e]);
 #pragma unroll
           for (int b = 0; b < B; ++b) {
-            dot[q][b] = fmaf(xf[b][2 * e], gf.x, dot[q][b]);
-            dot[q][b] = fmaf(xf[b][2 * e + 1], gf.y, dot[q][b]);
+            dot[q][b] = fma_f16<0, 0>(xh[b][e], gw[e], dot[q][b]);
+            dot[q][b] = fma_f16<1, 1>(xh[b][e], gw[e], dot[q][b]);
           }
         }
       }
@@ -1087,19 +1147,24 @@ bool decode_supported(int B, int d, int f, int E, int k, int n_shared, int P) {
   return (units + P - 1) / P <= kDecMaxUnits;
 }
 
+int decode_units_max(int B, int f, int k, int n_shared, int P) {
+  const long long units = (long long)(B * k + n_shared) * (f / kMTile);
+  return (int)((units + P - 1) / P);
+}
+
 int decode_list_cap(int B, int f, int k, int n_shared, int P) {
   const long long rows = (long long)(B * k + n_shared) * f;
   return (int)((rows + P - 1) / P) + 1;
 }
 
-int decode_plan(int B, int d, int E, int list_cap, int P, int smem_optin, int& su, int& sr) {
+int decode_plan(int B, int d, int E, int umax, int list_cap, int P, int smem_optin, int& su, int& sr) {
   su = sr = 0;
-  const UpLayoutD u0 = up_layout_d(d, B, E, 0);
+  const UpLayoutD u0 = up_layout_d(d, B, E, 0, umax);
   const size_t strip = u0.strip;
-  size_t fixed = up_layout_d(d, B, E, 0).total - al16(u0.ring);
+  size_t fixed = u0.total - al16(u0.ring);
   int s = (int)(((size_t)smem_optin - fixed - 256) / strip);
   if (s > kDecMaxSu) s = kDecMaxSu;
-  if (s < 2 || up_layout_d(d, B, E, s).total > (size_t)smem_optin) return 0;
+  if (s < 2 || up_layout_d(d, B, E, s, umax).total > (size_t)smem_optin) return 0;
   su = s;
   const GaLayoutD g0 = ga_layout_d(d, 0, list_cap, P);
   const size_t row = (size_t)4 * d;
@@ -1109,7 +1174,7 @@ int decode_plan(int B, int d, int E, int list_cap, int P, int smem_optin, int& s
   return 1;
 }
 
-size_t decode_up_smem(const DecodeParams& p) { return up_layout_d(p.d, p.B, p.routed.E, p.su).total; }
+size_t decode_up_smem(const DecodeParams& p) { return up_layout_d(p.d, p.B, p.routed.E, p.su, p.umax).total; }
 size_t decode_gather_smem(const DecodeParams& p) { return ga_layout_d(p.d, p.sr, p.list_cap, p.P).total; }
 
 static cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st,
@@ -1127,7 +1192,7 @@ static cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, size_t smem, cudaStream
 }
 
 cudaError_t launch_decode_up(const DecodeParams& p, cudaStream_t st, bool pdl) {
-  const UpLayoutD L = up_layout_d(p.d, p.B, p.routed.E, p.su);
+  const UpLayoutD L = up_layout_d(p.d, p.B, p.routed.E, p.su, p.umax);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_cfg(dim3(p.P), dim3(L.nwarps * 32), L.total, st, attr, pdl);
   const void* fn = p.B == 1 ? (const void*)decode_up_kernel<1> : (const void*)decode_up_kernel<2>;

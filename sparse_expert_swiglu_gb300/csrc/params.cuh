@@ -60,6 +60,8 @@ struct DecodeParams {
   int4* klist;              // [P][kcap] kept columns of every up CTA, in unit order:
                             // {column | group << 16, v of group token 0, 1 (float bits), 0}
   int kcap;                 // entries per up CTA
+  int gmax;                 // group descriptors the workspace holds
+  int umax;                 // units per up CTA, at most
   int* cta_total;           // [P] kept columns per up CTA
   float* yacc;              // [B][d] fp32 sum of the gather CTAs' shares (zero between calls)
   int P;                    // CTAs of the up and gather kernels (one per SM)
@@ -108,7 +110,8 @@ cudaError_t launch_combine(const ExpertParams& p, cudaStream_t st, bool pdl);
 // decode.cu
 bool decode_supported(int B, int d, int f, int E, int k, int n_shared, int P);
 int decode_list_cap(int B, int f, int k, int n_shared, int P);
-int decode_plan(int B, int d, int E, int list_cap, int P, int smem_optin, int& su, int& sr);
+int decode_units_max(int B, int f, int k, int n_shared, int P);
+int decode_plan(int B, int d, int E, int umax, int list_cap, int P, int smem_optin, int& su, int& sr);
 cudaError_t launch_decode_up(const DecodeParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_decode_gather(const DecodeParams& p, cudaStream_t st, bool pdl);
 
