@@ -71,7 +71,7 @@ WsLayout ws_layout(int B, int npairs, int G_max, int d, int f, int P3) {
   L.item_col = take(sizeof(int) * (size_t)G_max * MT * 16);
   L.item_v = take(sizeof(float) * (size_t)G_max * MT * 16 * 8);
   L.part = take(sizeof(float) * (size_t)(P3 + G_max) * kMaxTok * d);
-  L.yacc = take(sizeof(float) * (size_t)B * d);
+  L.yacc = take(sizeof(float) * (size_t)kDecYRep * B * d);
   L.cta_total = take(sizeof(int) * (size_t)P3);
   // decode path: per up CTA, 16 entries of 16 bytes for each of its units
   L.klist = take((size_t)P3 * (((size_t)G_max * MT + P3 - 1) / P3) * 16 * 16);

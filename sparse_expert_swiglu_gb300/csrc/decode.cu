@@ -18,8 +18,9 @@
 //                         (group, column) order: their gate and down rows stream
 //                         through a TMA ring; 16 warps form x . gate for a batch of
 //                         rows (one barrier per batch), h = SiLU(.) * v * router
-//                         weight, acc += h * down; each CTA adds its share of y to an
-//                         fp32 accumulator with vector atomics and the last CTA to
+//                         weight, acc += h * down; each CTA adds its share of y to
+//                         one of four fp32 accumulator copies with vector atomics
+//                         (fewer additions per address) and the last CTA to
 //                         finish rounds y to fp16 once, after the RMSNorm of stacked
 //                         layers.
 //
@@ -637,7 +638,7 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_up_kernel(DecodeParam
   griddep_launch_dependents();
   // the gather kernel's fp32 accumulator of y and its finish counter start at zero
   // (the previous kernel, which may be the last call's gather kernel, has finished)
-  for (int i = blockIdx.x * nthreads + tid; i < p.B * p.d / 4; i += gridDim.x * nthreads)
+  for (int i = blockIdx.x * nthreads + tid; i < kDecYRep * p.B * p.d / 4; i += gridDim.x * nthreads)
     reinterpret_cast<float4*>(p.yacc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (blockIdx.x == 0 && tid == 0) p.ctrl->gdone = 0;
   for (int i = tid; i < B * d / 8; i += nthreads)
@@ -1084,51 +1085,67 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
   }
   // the last batch: its h is written once warp 0 reaches the barrier
   if (!stop && bt > 0 && !bar_or(false)) apply((bt - 1) & 1, prev_nb, (bt & 1) ? dA : dB);
-  // this CTA's share of y, added in fp32 (the order of the CTAs' additions varies)
+  // this CTA's share of y, added in fp32 into copy blockIdx.x % kDecYRep of the
+  // accumulator (the order of the CTAs' additions varies)
 #pragma unroll
   for (int b = 0; b < B; ++b) {
-    float* dst = p.yacc + (size_t)b * d + tid * 8;
+    float* dst = p.yacc + ((size_t)(blockIdx.x % kDecYRep) * B + b) * d + tid * 8;
     red_add_v4(dst, acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
     red_add_v4(dst + 4, acc[b][4], acc[b][5], acc[b][6], acc[b][7]);
   }
-  __threadfence();
+  }
+  // the last CTA to finish: y = fp16(sum) or, for stacked layers, the RMSNorm
+  // y / sqrt(mean(y^2) + 1e-6) of it.  The barrier orders every thread's additions
+  // before thread 0's fence and count (release); the last count is followed by a fence
+  // before the barrier that precedes the reads (acquire).
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const bool last = atomicAdd(&p.ctrl->gdone, 1) == (int)gridDim.x - 1;
+    if (last) __threadfence();
+    m->last = last;
   }
   __syncthreads();
-  // the last CTA to finish: y = fp16(sum) or, for stacked layers, the RMSNorm
-  // y / sqrt(mean(y^2) + 1e-6) of it
-  if (tid == 0) m->last = atomicAdd(&p.ctrl->gdone, 1) == (int)gridDim.x - 1;
-  __syncthreads();
   if (m->last) {
-    __threadfence();
-    float* ss = red;  // [B][warps]
-    for (int b = 0; b < B; ++b) {
-      float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
-      float sq = 0.f;
-      if (tid < d / 8) {
-        const float4* src = reinterpret_cast<const float4*>(p.yacc + (size_t)b * d + tid * 8);
-        v0 = __ldcg(src);
-        v1 = __ldcg(src + 1);
-        sq = ((v0.x * v0.x + v0.y * v0.y) + (v0.z * v0.z + v0.w * v0.w)) +
-             ((v1.x * v1.x + v1.y * v1.y) + (v1.z * v1.z + v1.w * v1.w));
-      }
+    float* ss = red;  // [B][32]
+    float4 v[B][2];
+    float sq[B];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-      if (lane == 0) ss[warp] = sq;
-      __syncthreads();
+    for (int b = 0; b < B; ++b) {
+      v[b][0] = v[b][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (tid < d / 8) {
+#pragma unroll
+        for (int r = 0; r < kDecYRep; ++r) {
+          const float4* src = reinterpret_cast<const float4*>(p.yacc + ((size_t)r * B + b) * d + tid * 8);
+          const float4 a0 = __ldcg(src), a1 = __ldcg(src + 1);
+          v[b][0] = make_float4(v[b][0].x + a0.x, v[b][0].y + a0.y, v[b][0].z + a0.z, v[b][0].w + a0.w);
+          v[b][1] = make_float4(v[b][1].x + a1.x, v[b][1].y + a1.y, v[b][1].z + a1.z, v[b][1].w + a1.w);
+        }
+      }
+      const float4 v0 = v[b][0], v1 = v[b][1];
+      sq[b] = ((v0.x * v0.x + v0.y * v0.y) + (v0.z * v0.z + v0.w * v0.w)) +
+              ((v1.x * v1.x + v1.y * v1.y) + (v1.z * v1.z + v1.w * v1.w));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sq[b] += __shfl_xor_sync(0xffffffffu, sq[b], off);
+      if (lane == 0) ss[b * 32 + warp] = sq[b];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
       float rinv = 1.f;
       if (p.rmsnorm) {
         float t = 0.f;
-        for (int w = 0; w < L.nwarps; ++w) t += ss[w];
+        for (int w = 0; w < L.nwarps; ++w) t += ss[b * 32 + w];
         rinv = rsqrtf(t / (float)d + 1e-6f);
       }
       if (tid < d / 8) {
+        const float4 v0 = v[b][0], v1 = v[b][1];
         __half2* yo = reinterpret_cast<__half2*>(p.y + (size_t)b * d + tid * 8);
         yo[0] = __floats2half2_rn(v0.x * rinv, v0.y * rinv);
         yo[1] = __floats2half2_rn(v0.z * rinv, v0.w * rinv);
         yo[2] = __floats2half2_rn(v1.x * rinv, v1.y * rinv);
         yo[3] = __floats2half2_rn(v1.z * rinv, v1.w * rinv);
       }
-      __syncthreads();
     }
   }
   if (m->abort && tid == 0) {

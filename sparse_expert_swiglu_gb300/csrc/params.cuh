@@ -50,6 +50,9 @@ struct ExpertParams {
 
 // The decode path (one or two tokens): up kernel (routing, up projection, mask, kept
 // lists) and gather kernel (kept gate/down rows, the weighted sum and RMSNorm).
+// copies of the decode path's fp32 accumulator of y (fewer atomic additions per address)
+constexpr int kDecYRep = 4;
+
 struct DecodeParams {
   const __half* x;          // [B][d]
   const __half* w_router;   // [d][E]
@@ -63,7 +66,8 @@ struct DecodeParams {
   int gmax;                 // group descriptors the workspace holds
   int umax;                 // units per up CTA, at most
   int* cta_total;           // [P] kept columns per up CTA
-  float* yacc;              // [B][d] fp32 sum of the gather CTAs' shares (zero between calls)
+  float* yacc;              // [kDecYRep][B][d] fp32 sums of the gather CTAs' shares, CTA c
+                            // adding into copy c % kDecYRep (zeroed by the up kernel)
   int P;                    // CTAs of the up and gather kernels (one per SM)
   int list_cap;             // rows per gather CTA, at most
   int32_t* topk_idx;        // [B][k] workspace copies (written by CTA 0)
