@@ -36,6 +36,17 @@ import torch  # noqa: E402
 WORKLOAD = dict(name="mixtral-8x7b-moe-layer-decode", d=4096, f=14336, E=8, k=2, B=1,
                 calib_tokens=1024)
 SPARSITIES = (0, 50, 70, 90)
+
+# Further layer shapes, timed with --workload (one JSON line per point; the default run
+# above is the headline).  Shared experts have the routed experts' d and f.
+WORKLOADS = {
+    "mixtral-8x7b-batch": dict(d=4096, f=14336, E=8, k=2, shared=0, tokens=(1, 2, 4, 8, 16, 32),
+                               sparsities=(70,), calib_tokens=1024, copies=8, chained=False),
+    "deepseek-v2-lite": dict(d=2048, f=1408, E=64, k=6, shared=2, tokens=(1, 2, 4, 8, 16, 32, 64),
+                             sparsities=(0, 50, 90), calib_tokens=1024, copies=8, chained=False),
+    "mixtral-8x22b-stack": dict(d=6144, f=16384, E=8, k=2, shared=0, tokens=(1, 8), sparsities=(70,),
+                                calib_tokens=256, copies=56, chained=True),
+}
 HEADLINE_PCT = 70
 N_LAYER_COPIES = 8
 METRIC = "MoE decode layer expert-tokens/s (Mixtral-8x7B-shaped layer, 1 token, 70% sparsity)"
@@ -61,6 +72,9 @@ def parse_args():
                     help="rotating layer copies (fewer: a small case for profiling; below 8 the "
                          "weights no longer exceed L2 by a wide margin)")
     ap.add_argument("--no-sweep", action="store_true", help="time only the headline sparsity")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=None,
+                    help="time one of the further layer shapes instead of the headline")
+    ap.add_argument("--tokens", type=int, default=None, help="with --workload: only this batch size")
     return ap.parse_args()
 
 
@@ -574,12 +588,148 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_workload(args, world, rank, local):
+    """The further shapes: for every batch size and sparsity of the workload, the layer
+    copies back to back in one CUDA graph (a stack: each copy's input is the previous
+    copy's RMS-normalised output when `chained`, else its own tokens), timed on the
+    device; algorithmic bytes from the realised masks."""
+    import sparse_expert_swiglu_gb300 as ses
+    from sparse_expert_swiglu_gb300 import synth
+    ses.build_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    W = dict(WORKLOADS[args.workload])
+    d, f, E, k, ns = W["d"], W["f"], W["E"], W["k"], W["shared"]
+    R = W["copies"] if args.copies == N_LAYER_COPIES else max(1, args.copies)
+    peak, peak_kind = measured_peaks()
+    layers, tables = [], []
+    xcal = synth.calibration_tokens(W["calib_tokens"], d, 7, device=dev)
+    cws = ses.Workspace(ses.expert_workspace_bytes(W["calib_tokens"], d, f), dev)
+
+    def packed(de, nexp):
+        return ses.Experts.from_dense(de.w_up, de.gate_t, de.down,
+                                      torch.zeros(nexp, dtype=torch.float32, device=dev), interleave=True)
+
+    def thresholds(ex, nexp):
+        ex.thr.fill_(float("inf"))  # nothing kept: only v is computed
+        thr = {p: torch.zeros(nexp, dtype=torch.float32, device=dev) for p in W["sparsities"]}
+        for e in range(nexp):
+            _, dbg = ses.expert_sparse_swiglu(xcal, ex, e, ws=cws, debug=True)
+            a = torch.sort(dbg["v"].abs().flatten()).values
+            for p in W["sparsities"]:
+                if p > 0:
+                    thr[p][e] = a[(p * a.numel() + 99) // 100 - 1]
+        return thr
+
+    for r in range(R):
+        ex = packed(synth.experts(E, d, f, 200 + r, device=dev, layer=r), E)
+        sh = packed(synth.experts(ns, d, f, 200 + r, device=dev, layer=r, kind=1), ns) if ns else None
+        torch.cuda.empty_cache()
+        layers.append(ses.Layer(synth.router(d, E, 200 + r, device=dev, layer=r), ex, k, True, sh))
+        tables.append((thresholds(ex, E), thresholds(sh, ns) if ns else None))
+    up_bytes = ses.packed_bytes(d, f)
+    weights_gb = sum(l.routed.gate_t.numel() * 4 + l.routed.up_packed.numel() +
+                     (l.shared.gate_t.numel() * 4 + l.shared.up_packed.numel() if l.shared else 0)
+                     for l in layers) / 1e9
+    stream = torch.cuda.Stream()
+    for B in ([args.tokens] if args.tokens else W["tokens"]):
+        xs = [synth.tokens(B, d, 3000 + r + 100 * rank, device=dev) for r in range(R)]
+        ys = [torch.empty_like(x) for x in xs]
+        if W["chained"]:
+            xs = [xs[0]] + ys[:-1]
+        wss = [ses.Workspace(ses.layer_workspace_bytes(layers[r], B), dev) for r in range(R)]
+        path = ses.layer_path(layers[0], B)
+        with torch.cuda.stream(stream):
+            for r in range(R):
+                ses.layer_decode(xs[r], layers[r], rmsnorm=True, ws=wss[r], out=ys[r])
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        c_layers = [l.c_struct() for l in layers]
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for r in range(R):
+                ses.layer_decode(xs[r], layers[r], rmsnorm=True, ws=wss[r], out=ys[r], c_layer=c_layers[r])
+        torch.cuda.synchronize()
+        for pct in W["sparsities"]:
+            for r, layer in enumerate(layers):
+                layer.routed.thr.copy_(tables[r][0][pct])
+                if ns:
+                    layer.shared.thr.copy_(tables[r][1][pct])
+            # realised bytes, layer by layer along the same inputs
+            total, kept, cols = 0.0, 0, 0
+            for r, layer in enumerate(layers):
+                _, dbg = ses.layer_decode(xs[r], layer, rmsnorm=True, ws=wss[r], out=ys[r], debug=True)
+                idx = dbg["topk_idx"].cpu().numpy()
+                words = dbg["mask"].cpu().numpy().astype(np.uint32)
+                bits = ((words[..., None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(B, k + ns, -1)[..., :f]
+                bits = bits.astype(bool)
+                groups = [bits[np.nonzero(idx == e)[0], np.nonzero(idx == e)[1]] for e in sorted(set(idx.ravel().tolist()))]
+                groups += [bits[:, k + s_] for s_ in range(ns)]
+                for gb in groups:
+                    u = int(np.any(gb, axis=0).sum())
+                    kept += u
+                    cols += f
+                    total += up_bytes + 4 * d * u
+                total += 2 * d * E + 4 * B * d
+            torch.cuda.synchronize()
+            reps = max(2, 200 // R)
+            with torch.cuda.stream(stream):
+                for _ in range(2):
+                    g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            secs = max_over_ranks(world, e0.elapsed_time(e1) / 1e3, dev)
+            steps = reps * R
+            us = secs / steps * 1e6
+            mean_bytes = total / R
+            # per-kernel device times on copy 0, from events inside a graph (they
+            # serialise the kernels but leave no host gaps)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            for ev in evs:
+                ev.record()
+            torch.cuda.synchronize()
+            ge = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(ge, stream=stream, capture_error_mode="thread_local"):
+                ses.layer_decode(xs[0], layers[0], rmsnorm=True, ws=wss[0], out=ys[0], c_layer=c_layers[0],
+                                 events=evs)
+            kacc = np.zeros(4)
+            for it in range(12):
+                with torch.cuda.stream(stream):
+                    ge.replay()
+                torch.cuda.synchronize()
+                if it >= 2:
+                    kacc += [evs[j].elapsed_time(evs[j + 1]) * 1e3 for j in range(4)]
+            del ge
+            names = (["event_pair_us", "decode_up_kernel", "decode_gather_kernel", "event_pair_us_2"]
+                     if path == "decode" else ["route_kernel", "up_kernel", "gather_kernel", "combine_kernel"])
+            kt = {nm: float(v) / 10 for nm, v in zip(names, kacc)}
+            if rank == 0:
+                print(json.dumps({
+                    "workload": args.workload, "tokens": B, "sparsity_pct": pct, "path": path,
+                    "layer_us": us, "expert_tokens_per_s": world * B * k * steps / secs,
+                    "bytes_per_step": mean_bytes, "hbm_gbs": mean_bytes / (us * 1e-6) / 1e9,
+                    "frac_of_measured_hbm": mean_bytes / (us * 1e-6) / 1e9 / peak, "peak_kind": peak_kind,
+                    "kept_fraction": kept / max(cols, 1), "layers_per_graph": R, "chained": W["chained"],
+                    "steps": steps, "weights_gb": weights_gb, "kernel_us": kt,
+                    "config": {"d": d, "f": f, "experts": E, "top_k": k, "shared": ns,
+                               "calib_tokens": W["calib_tokens"]}}), flush=True)
+        del g, wss
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":
             run_reference(args, world, rank, local)
+        elif args.workload:
+            run_workload(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

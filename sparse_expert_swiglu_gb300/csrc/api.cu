@@ -33,7 +33,9 @@ cudaError_t device_info(DeviceInfo& di) {
 
 // Tokens of one expert handled together: their fp32 accumulators must fit in the
 // gather kernel's registers (8 x 8 floats per thread up to d = 4096, 4 x 8 up to 6144).
-int group_cap(int d) { return d <= 4096 ? 8 : d <= 6144 ? 4 : 2; }
+// tokens per expert group: the gather kernel keeps x and the output of every token of a
+// group in registers
+int group_cap(int d) { return d <= 4096 ? 4 : 2; }
 
 int groups_max_routed(int B, int E, int k, int gcap) {
   const long long pairs = (long long)B * k;
@@ -129,7 +131,7 @@ moe_status_t plan(const DeviceInfo& di, const WsLayout& L, int d, int f, int max
   const int occ = up_blocks_per_sm(d, max_tok);
   if (occ < 1) return MOE_ERR_UNSUPPORTED_SHAPE;
   pl.up_grid = di.sms * occ;
-  pl.nt = max_tok <= 1 ? 1 : max_tok <= 2 ? 2 : max_tok <= 4 ? 4 : 8;
+  pl.nt = max_tok <= 1 ? 1 : max_tok <= 2 ? 2 : 4;
   const size_t fixed = gather_smem_bytes(d, 0, pl.nt, L.list_cap, L.G_max) + 2048;
   const size_t stage = (size_t)4 * d + 32 + 16;
   if (fixed + 2 * stage > (size_t)di.smem_optin) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -147,8 +149,14 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 // Optional per-kernel timing events of moe_debug_t (index 0..4).
 cudaError_t record(const moe_debug_t* dbg, int i, cudaStream_t st) {
   if (!dbg || !dbg->events || !dbg->events[i]) return cudaSuccess;
-  // External: inside stream capture this becomes an event-record node of the graph.
-  return cudaEventRecordWithFlags((cudaEvent_t)dbg->events[i], st, cudaEventRecordExternal);
+  // Inside stream capture an external record becomes an event-record node of the
+  // graph; outside it the plain record is the one that applies.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t q = cudaStreamIsCapturing(st, &cs);
+  if (q != cudaSuccess) return q;
+  if (cs == cudaStreamCaptureStatusActive)
+    return cudaEventRecordWithFlags((cudaEvent_t)dbg->events[i], st, cudaEventRecordExternal);
+  return cudaEventRecord((cudaEvent_t)dbg->events[i], st);
 }
 
 }  // namespace

@@ -8,13 +8,14 @@
 // Each CTA takes an equal share of the kept items of the whole call (in the fixed
 // order group, M-tile, column).  One producer thread brings the gate row, the down
 // row and the v values of every item into a shared-memory ring with 1-D bulk copies
-// (TMA).  The consumer warps form NGRP independent groups; group q handles items
-// q, q + NGRP, ...: its threads own interleaved 16-byte chunks of the hidden
-// dimension, form the partial dot products x . gate, sum them across the group
-// (double-buffered, one named barrier per item), apply SiLU * v * (router weight)
-// and accumulate h * down in fp32 registers.  At the end of every expert group the
-// NGRP accumulators are added in a fixed order and written as this CTA's partial
-// output; the combine kernel adds the partials.
+// (TMA).  The consumer warps own interleaved 16-byte chunks of the hidden dimension;
+// per group segment they hold the group's x (fp32) and its output accumulators in
+// registers.  Items go in batches (one barrier per batch): every warp forms the
+// partial dot products x . gate of a batch (packed fp32 FMAs, one recursive-halving
+// warp reduction for all items and tokens), warp 0 turns the per-warp sums into
+// h = SiLU(.) * v * (router weight) while the others apply the previous batch,
+// acc += h * down.  At the end of a segment the accumulators are this CTA's partial
+// output of the group; the combine kernel adds the partials.
 #include "params.cuh"
 
 namespace sesg {
@@ -22,22 +23,42 @@ namespace sesg {
 constexpr int kChunk = 8;  // fp16 elements per 16-byte chunk
 
 struct GatherLayout {
-  size_t off_full, off_empty, off_stage, off_lslot, off_lcol, off_lgrp, off_red, off_accred, off_tmp,
+  size_t off_full, off_empty, off_stage, off_lslot, off_lcol, off_lgrp, off_red, off_hbuf, off_tmp,
       off_goff, total, stage_bytes;
 };
 
-__host__ __device__ inline int gather_ngrp(int d, int nt) {
-  const int ncw = d / 256;
-  const int maxg = nt == 1 ? 4 : nt == 2 ? 2 : 1;
-  for (int g = maxg; g > 1; g >>= 1)
-    if (ncw % g == 0) return g;
-  return 1;
+constexpr int kGaBatchTok = 16;  // items per batch x tokens per group, at most
+
+// Warp sums of V values (V a power of two <= 32) by recursive halving: at each of the
+// first log2(V) levels every lane keeps half of its values and adds its partner's copy
+// of them; the last levels add the one remaining value.  Returns the sum of value
+// `idx` over the 32 lanes, where idx is set from the lane's bits 4, 3, ... .
+template <int V>
+__device__ __forceinline__ float warp_sum_halving(float (&a)[V], int lane, int& idx) {
+  idx = 0;
+  int cnt = V;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    if (cnt > 1) {
+      const int h = cnt / 2;
+      const bool up = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < h && i < V / 2; ++i)
+        a[i] = (up ? a[i + h] : a[i]) + __shfl_xor_sync(0xffffffffu, up ? a[i] : a[i + h], off);
+      if (up) idx += h;
+      cnt = h;
+    } else {
+      a[0] += __shfl_xor_sync(0xffffffffu, a[0], off);
+    }
+  }
+  return a[0];
 }
 
 __host__ __device__ inline GatherLayout gather_layout(int d, int stages, int nt, int list_cap,
                                                       int g_max) {
   GatherLayout L;
-  const int ncw = d / 256, ngrp = gather_ngrp(d, nt);
+  const int ncw = d / 256;
+  (void)nt;
   size_t o = 0;
   L.off_full = o;
   o += 8 * (size_t)stages;
@@ -53,11 +74,12 @@ __host__ __device__ inline GatherLayout gather_layout(int d, int stages, int nt,
   o += (size_t)list_cap * 4;
   L.off_lgrp = o;
   o += (size_t)list_cap * 4;
-  L.off_red = o;  // [ngrp][2][warps per group][kMaxTok]
-  o += (size_t)2 * ncw * kMaxTok * 4;
   o = (o + 15) & ~(size_t)15;
-  L.off_accred = o;  // cross-group reduction buffer [nt][d]
-  o += ngrp > 1 ? (size_t)nt * d * 4 : 0;
+  L.off_red = o;  // [2][items][tokens][consumer warps] partial dot products
+  o += (size_t)2 * kGaBatchTok * ncw * 4;
+  o = (o + 15) & ~(size_t)15;
+  L.off_hbuf = o;  // [2][items][tokens] h of a batch
+  o += (size_t)2 * kGaBatchTok * 4;
   L.off_tmp = o;  // block-scan scratch
   o += (size_t)1040 * 4;
   L.off_goff = o;  // kept-item offsets of the groups [G_max + 1]
@@ -103,15 +125,15 @@ __device__ void block_exclusive_scan(int* data, int n, int* tmp) {
   __syncthreads();
 }
 
-template <int NT, int NGRP, int MAXT>
+template <int NT, int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
   extern __shared__ __align__(128) uint8_t gsm[];
+  // items per batch (one barrier per batch), within the register budget
+  constexpr int kR = NT == 4 ? 2 : (MAXT > 640 && NT == 2) ? 2 : 4;
+  static_assert(kR * NT <= kGaBatchTok, "batch buffers");
   const int d = p.d;
-  const int ncw = d / 256;          // consumer warps
-  const int nct = ncw * 32;         // consumer threads
-  constexpr int ngrp = NGRP;
-  const int wg = ncw / ngrp;        // warps per consumer group
-  const int tpg = wg * 32;          // threads per consumer group
+  const int ncw = d / 256;   // consumer warps
+  const int nct = ncw * 32;  // consumer threads
   const int S = p.stages;
   const GatherLayout L = gather_layout(d, S, NT, p.list_cap, p.G_max);
   uint64_t* full = reinterpret_cast<uint64_t*>(gsm + L.off_full);
@@ -120,8 +142,8 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
   int* lslot = reinterpret_cast<int*>(gsm + L.off_lslot);
   int* lcol = reinterpret_cast<int*>(gsm + L.off_lcol);
   int* lgrp = reinterpret_cast<int*>(gsm + L.off_lgrp);
-  float* red = reinterpret_cast<float*>(gsm + L.off_red);
-  float* accred = reinterpret_cast<float*>(gsm + L.off_accred);
+  float* red = reinterpret_cast<float*>(gsm + L.off_red);    // [2][kR][NT][ncw] partial dots
+  float* hbuf = reinterpret_cast<float*>(gsm + L.off_hbuf);  // [2][kR][NT]
   int* tmp = reinterpret_cast<int*>(gsm + L.off_tmp);
   __shared__ int s_abort, s_issued, s_consumed;
   __shared__ GroupDesc s_gd;
@@ -131,7 +153,7 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], wg);
+      mbar_init(&empty[s], ncw);
     }
     fence_barrier_init();
     s_abort = 0;
@@ -153,12 +175,11 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
   if (blockIdx.x == 0 && tid == 0) p.ctrl->N = (int)N;
   const int a = (int)(N * blockIdx.x / p.P3), b = (int)(N * (blockIdx.x + 1) / p.P3);
 
-  // consumer-group geometry
-  const int q = producer ? 0 : warp / wg;        // consumer group
-  const int tg = producer ? 0 : tid - q * tpg;   // thread within the group
-  const int wig = tg >> 5;                       // warp within the group
-  float acc[NT][kChunk * NGRP];
-  uint4 xr[NT][NGRP];
+  // ring positions: the producer's next stage and the consumers' next stage, each with
+  // its barrier parity, advanced one item at a time (no divisions in the loops)
+  int ps = 0, pph = 0, cs = 0, cph = 0;
+  float2 acc[NT][kChunk / 2];
+  float2 xf[NT][kChunk / 2];
   float wt[NT];
 
   for (int wa = a; wa < b; wa += p.list_cap) {
@@ -196,17 +217,14 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
     __syncthreads();
 
     if (producer) {
-      // two producer lanes (even / odd items): two bulk-copy transactions in flight per SM
-      if (lane < 2) {
+      if (lane == 0) {
         const uint64_t pol = policy_evict_first();
         int last_g = -1;
         const __half* gbase_ptr = nullptr;
         const __half* dbase_ptr = nullptr;
         int row_stride = d;
-        for (int i = lane; i < n; i += 2) {
-          const int gidx = base + i;
-          const int s = gidx % S;
-          if (gidx >= S && !mbar_wait(&empty[s], ((gidx / S) - 1) & 1)) {
+        for (int i = 0; i < n; ++i) {
+          if (base + i >= S && !mbar_wait(&empty[ps], pph ^ 1)) {
             set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
             atomicExch(&s_abort, 1);
             break;
@@ -222,23 +240,73 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
             row_stride = es.rs;
           }
           const size_t roff = (size_t)lcol[i] * row_stride;
-          uint8_t* st = stage + (size_t)s * L.stage_bytes;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(4 * d + 32));
-          bulk_g2s(st, gbase_ptr + roff, (uint32_t)(2 * d), &full[s], pol);
-          bulk_g2s(st + 2 * d, dbase_ptr + roff, (uint32_t)(2 * d), &full[s], pol);
-          bulk_g2s(st + 4 * d, p.item_v + (size_t)lslot[i] * 8, 32u, &full[s], pol);
-          atomicMax(&s_issued, gidx + 1);
+          uint8_t* st = stage + (size_t)ps * L.stage_bytes;
+          mbar_arrive_expect_tx(&full[ps], (uint32_t)(4 * d + 32));
+          if (row_stride == 2 * d) {
+            bulk_g2s(st, gbase_ptr + roff, (uint32_t)(4 * d), &full[ps], pol);
+          } else {
+            bulk_g2s(st, gbase_ptr + roff, (uint32_t)(2 * d), &full[ps], pol);
+            bulk_g2s(st + 2 * d, dbase_ptr + roff, (uint32_t)(2 * d), &full[ps], pol);
+          }
+          bulk_g2s(st + 4 * d, p.item_v + (size_t)lslot[i] * 8, 32u, &full[ps], pol);
+          s_issued = base + i + 1;
+          if (++ps == S) {
+            ps = 0;
+            pph ^= 1;
+          }
         }
       }
     } else {
-      // ---- consumers: segments of equal group, items of a segment dealt round-robin
+      // ---- consumers: segments of equal group; in a segment, batches of up to kR
+      // items with one barrier each, software-pipelined: every warp forms the dot
+      // products of batch k, then (after the barrier) applies batch k-1 while warp 0
+      // turns batch k's sums into h = SiLU(.) * v * w.
+      auto bar_or = [&](bool bad) -> bool {
+        int fail;
+        asm volatile(
+            "{\n\t.reg .pred pin, pout;\n\t"
+            "setp.ne.u32 pin, %1, 0;\n\t"
+            "barrier.red.or.pred pout, 1, %2, pin;\n\t"
+            "selp.u32 %0, 1, 0, pout;\n\t}"
+            : "=r"(fail)
+            : "r"((unsigned)bad), "r"(nct)
+            : "memory");
+        return fail != 0;
+      };
+      // acc += h (batch parity par) * this thread's down slices of the batch's stages
+      auto apply = [&](int par, int nbq, const int (&sq)[kR]) {
+        const float* hb = hbuf + par * kR * NT;
+#pragma unroll
+        for (int q = 0; q < kR; ++q) {
+          if (q < nbq) {
+            const uint8_t* st = stage + (size_t)sq[q] * L.stage_bytes;
+            const uint4 dr = reinterpret_cast<const uint4*>(st + 2 * d)[tid];
+            const __half2* dh = reinterpret_cast<const __half2*>(&dr);
+            float2 hv[NT];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) hv[t] = make_float2(hb[q * NT + t], hb[q * NT + t]);
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const float2 df = __half22float2(dh[e2]);
+#pragma unroll
+              for (int t = 0; t < NT; ++t) acc[t][e2] = __ffma2_rn(hv[t], df, acc[t][e2]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int q = 0; q < kR; ++q)
+            if (q < nbq) mbar_arrive(&empty[sq[q]]);
+        }
+      };
+      bool stop = false;
       int i = 0;
-      int local = 0;  // items this consumer group has processed (red buffer parity)
-      while (i < n) {
+      while (i < n && !stop) {
         const int g = lgrp[i];
         int e = i;
         while (e < n && lgrp[e] == g) ++e;
-        // segment start: the group's tokens, weights, x chunks
+        // segment start: the group's tokens, weights, x
         named_barrier(1, nct);
         if (tid == 0) s_gd = p.groups[g];
         named_barrier(1, nct);
@@ -246,138 +314,121 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           wt[t] = t < ntok ? s_gd.w[t] : 0.f;
+          uint4 xv = make_uint4(0, 0, 0, 0);
+          if (t < ntok) xv = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)s_gd.tok[t] * d) + tid);
+          const __half2* xh = reinterpret_cast<const __half2*>(&xv);
 #pragma unroll
-          for (int k = 0; k < NGRP; ++k) {
-            xr[t][k] = make_uint4(0, 0, 0, 0);
-            if (t < ntok)
-              xr[t][k] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)s_gd.tok[t] * d) + tg + k * tpg);
+          for (int e2 = 0; e2 < 4; ++e2) {
+            xf[t][e2] = __half22float2(xh[e2]);
+            acc[t][e2] = make_float2(0.f, 0.f);
           }
-#pragma unroll
-          for (int e2 = 0; e2 < kChunk * NGRP; ++e2) acc[t][e2] = 0.f;
         }
-        for (int ii = i + q; ii < e; ii += ngrp) {
-          const int gidx = base + ii;
-          const int s = gidx % S;
-          const bool ok = mbar_wait(&full[s], (gidx / S) & 1);
-          const uint8_t* st = stage + (size_t)s * L.stage_bytes;
-          // x . gate over this thread's chunks, summed over the warp
-          float dot[NT];
+        int prev_s[kR];
+        int prev_nb = 0, bt = 0;
+        for (int i0 = i; i0 < e; i0 += kR) {
+          const int nb = min(kR, e - i0);
+          int sq[kR];
+          bool ok = !*reinterpret_cast<volatile int*>(&s_abort);
 #pragma unroll
-          for (int t = 0; t < NT; ++t) dot[t] = 0.f;
-#pragma unroll
-          for (int k = 0; k < NGRP; ++k) {
-            {
-              uint4 gr = make_uint4(0, 0, 0, 0);
-              if (ok) gr = reinterpret_cast<const uint4*>(st)[tg + k * tpg];
-              const __half2* gh = reinterpret_cast<const __half2*>(&gr);
-#pragma unroll
-              for (int t = 0; t < NT; ++t) {
-                if (t < ntok) {
-                  const __half2* xh = reinterpret_cast<const __half2*>(&xr[t][k]);
-#pragma unroll
-                  for (int e2 = 0; e2 < 4; ++e2) {
-                    const float2 gf = __half22float2(gh[e2]);
-                    const float2 xf = __half22float2(xh[e2]);
-                    dot[t] = fmaf(xf.x, gf.x, dot[t]);
-                    dot[t] = fmaf(xf.y, gf.y, dot[t]);
-                  }
-                }
+          for (int q = 0; q < kR; ++q) {
+            sq[q] = cs;
+            if (q < nb) {
+              ok = ok && mbar_wait(&full[cs], cph);
+              if (++cs == S) {
+                cs = 0;
+                cph ^= 1;
               }
             }
           }
-          float* rb = red + ((size_t)(q * 2 + (local & 1)) * wg) * kMaxTok;
+          float dot[kR * NT];
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            if (t < ntok) {
+          for (int q = 0; q < kR; ++q) {
+            float2 d2[NT];
 #pragma unroll
-              for (int off = 16; off > 0; off >>= 1) dot[t] += __shfl_xor_sync(0xffffffffu, dot[t], off);
-              if (lane == 0) rb[wig * kMaxTok + t] = dot[t];
+            for (int t = 0; t < NT; ++t) d2[t] = make_float2(0.f, 0.f);
+            if (q < nb && ok) {
+              const uint4 gr = reinterpret_cast<const uint4*>(stage + (size_t)sq[q] * L.stage_bytes)[tid];
+              const __half2* gh = reinterpret_cast<const __half2*>(&gr);
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const float2 gf = __half22float2(gh[e2]);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) d2[t] = __ffma2_rn(xf[t][e2], gf, d2[t]);
+              }
             }
+#pragma unroll
+            for (int t = 0; t < NT; ++t) dot[q * NT + t] = d2[t].x + d2[t].y;
           }
-          // one barrier per item within the group; any failed wait ends the group
-          int fail;
-          asm volatile(
-              "{\n\t.reg .pred pin, pout;\n\t"
-              "setp.ne.u32 pin, %1, 0;\n\t"
-              "barrier.red.or.pred pout, %2, %3, pin;\n\t"
-              "selp.u32 %0, 1, 0, pout;\n\t}"
-              : "=r"(fail)
-              : "r"((unsigned)(!ok)), "r"(2 + q), "r"(tpg)
-              : "memory");
-          if (fail) {
-            if (tg == 0) {
+          // warp sums of the kR x NT dot products; lanes 0, 4, ... hold one each
+          int vi;
+          const float vs = warp_sum_halving<kR * NT>(dot, lane, vi);
+          float* rb = red + (size_t)(bt & 1) * kR * NT * ncw;
+          if ((lane & (32 / (kR * NT) - 1)) == 0) rb[vi * ncw + warp] = vs;
+          if (bar_or(!ok)) {
+            if (tid == 0) {
               set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
               atomicExch(&s_abort, 1);
             }
+            stop = true;
             break;
           }
-          const float* hv = reinterpret_cast<const float*>(st + 4 * d);
-          float h[NT];
+          // the previous batch, with the h warp 0 wrote before this barrier
+          if (bt > 0) apply((bt - 1) & 1, prev_nb, prev_s);
+          if (tid == 0) s_consumed = base + i0;  // the stages before this batch are free
+          if (warp == 0 && lane < kR * NT) {
+            const int q = lane / NT, t = lane - (lane / NT) * NT;
+            float hq = 0.f;
+            int sl = sq[0];
+#pragma unroll
+            for (int qq = 1; qq < kR; ++qq)
+              if (q == qq) sl = sq[qq];
+            float wtt = wt[0];
+#pragma unroll
+            for (int tt = 1; tt < NT; ++tt)
+              if (t == tt) wtt = wt[tt];
+            if (q < nb && t < ntok) {
+              // the consumer warps' partial sums, four at a time (independent loads)
+              const float* pr = rb + lane * ncw;
+              float gs = 0.f;
+              int w = 0;
+              if ((ncw & 3) == 0) {
+                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (; w < ncw; w += 4) {
+                  const float4 v4 = *reinterpret_cast<const float4*>(pr + w);
+                  s4 = make_float4(s4.x + v4.x, s4.y + v4.y, s4.z + v4.z, s4.w + v4.w);
+                }
+                gs = (s4.x + s4.y) + (s4.z + s4.w);
+              }
+              for (; w < ncw; ++w) gs += pr[w];
+              const float* hv = reinterpret_cast<const float*>(stage + (size_t)sl * L.stage_bytes + 4 * d);
+              hq = silu_f(gs) * hv[t] * wtt;
+            }
+            hbuf[(bt & 1) * kR * NT + lane] = hq;
+          }
+#pragma unroll
+          for (int q = 0; q < kR; ++q) prev_s[q] = sq[q];
+          prev_nb = nb;
+          ++bt;
+        }
+        // the segment's last batch
+        if (!stop && bt > 0) {
+          if (bar_or(false)) {
+            stop = true;
+          } else {
+            apply((bt - 1) & 1, prev_nb, prev_s);
+          }
+        }
+        // segment end: this CTA's partial output of the group
+        if (!stop) {
+          float* dst = p.part + ((size_t)(blockIdx.x + g) * kMaxTok) * d;
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            h[t] = 0.f;
             if (t < ntok) {
-              float gsum = 0.f;
-              for (int w = 0; w < wg; ++w) gsum += rb[w * kMaxTok + t];
-              h[t] = silu_f(gsum) * hv[t] * wt[t];
+              float4* o = reinterpret_cast<float4*>(dst + (size_t)t * d + tid * kChunk);
+              o[0] = make_float4(acc[t][0].x, acc[t][0].y, acc[t][1].x, acc[t][1].y);
+              o[1] = make_float4(acc[t][2].x, acc[t][2].y, acc[t][3].x, acc[t][3].y);
             }
           }
-          // down rows: acc += h * down[kept row]
-#pragma unroll
-          for (int k = 0; k < NGRP; ++k) {
-            {
-              const uint4 dr = reinterpret_cast<const uint4*>(st + 2 * d)[tg + k * tpg];
-              const __half2* dh = reinterpret_cast<const __half2*>(&dr);
-#pragma unroll
-              for (int e2 = 0; e2 < 4; ++e2) {
-                const float2 df = __half22float2(dh[e2]);
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                  acc[t][k * kChunk + 2 * e2] = fmaf(h[t], df.x, acc[t][k * kChunk + 2 * e2]);
-                  acc[t][k * kChunk + 2 * e2 + 1] = fmaf(h[t], df.y, acc[t][k * kChunk + 2 * e2 + 1]);
-                }
-              }
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[s]);
-          ++local;
-        }
-        // segment end: add the groups' accumulators in a fixed order, write the partial
-        named_barrier(1, nct);
-        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
-        float* dst = p.part + ((size_t)(blockIdx.x + g) * kMaxTok) * d;
-        for (int r = 0; r < ngrp; ++r) {
-          if (q == r) {
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-              if (t < ntok) {
-#pragma unroll
-                for (int k = 0; k < NGRP; ++k) {
-                  {
-                    const int c = tg + k * tpg;
-                    float4* ar = reinterpret_cast<float4*>(accred + (size_t)t * d + c * kChunk);
-                    float4 v0 = make_float4(acc[t][k * 8 + 0], acc[t][k * 8 + 1], acc[t][k * 8 + 2], acc[t][k * 8 + 3]);
-                    float4 v1 = make_float4(acc[t][k * 8 + 4], acc[t][k * 8 + 5], acc[t][k * 8 + 6], acc[t][k * 8 + 7]);
-                    if (r > 0) {
-                      const float4 p0 = ar[0], p1 = ar[1];
-                      v0 = make_float4(p0.x + v0.x, p0.y + v0.y, p0.z + v0.z, p0.w + v0.w);
-                      v1 = make_float4(p1.x + v1.x, p1.y + v1.y, p1.z + v1.z, p1.w + v1.w);
-                    }
-                    if (r + 1 < ngrp) {
-                      ar[0] = v0;
-                      ar[1] = v1;
-                    } else {
-                      float4* o = reinterpret_cast<float4*>(dst + (size_t)t * d + c * kChunk);
-                      o[0] = v0;
-                      o[1] = v1;
-                    }
-                  }
-                }
-              }
-            }
-          }
-          if (ngrp > 1) named_barrier(1, nct);
         }
         if (tid == 0) s_consumed = base + e;
         i = e;
@@ -399,7 +450,6 @@ size_t gather_smem_bytes(int d, int stages, int nt, int list_cap, int g_max) {
 cudaError_t launch_gather(const ExpertParams& p, int nt, cudaStream_t st, bool pdl) {
   const int ncw = p.d / 256;
   const size_t smem = gather_smem_bytes(p.d, p.stages, nt, p.list_cap, p.G_max);
-  const int ngrp = gather_ngrp(p.d, nt);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.P3);
   cfg.blockDim = dim3((ncw + 1) * 32);
@@ -411,20 +461,18 @@ cudaError_t launch_gather(const ExpertParams& p, int nt, cudaStream_t st, bool p
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
-#define SESG_G(NTV, NG, MT)                                                                        \
+#define SESG_G(NTV, MT)                                                                            \
   if ((ncw + 1) * 32 > MT) return cudaErrorInvalidConfiguration;                                  \
-  e = cudaFuncSetAttribute(gather_kernel<NTV, NG, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+  e = cudaFuncSetAttribute(gather_kernel<NTV, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
                            (int)smem);                                                             \
   if (e != cudaSuccess) return e;                                                                  \
-  return cudaLaunchKernelEx(&cfg, gather_kernel<NTV, NG, MT>, p);
-  const bool small = (ncw + 1) * 32 <= 544;  // d <= 4096: more registers per thread
-  if (nt == 1 && ngrp == 4) { if (small) { SESG_G(1, 4, 544) } SESG_G(1, 4, 1024) }
-  if (nt == 1 && ngrp == 2) { if (small) { SESG_G(1, 2, 544) } SESG_G(1, 2, 1024) }
-  if (nt == 1) { if (small) { SESG_G(1, 1, 544) } SESG_G(1, 1, 1024) }
-  if (nt == 2 && ngrp == 2) { if (small) { SESG_G(2, 2, 544) } SESG_G(2, 2, 1024) }
-  if (nt == 2) { if (small) { SESG_G(2, 1, 544) } SESG_G(2, 1, 1024) }
-  if (nt == 4) { if (small) { SESG_G(4, 1, 544) } SESG_G(4, 1, 800) }
-  SESG_G(8, 1, 544)
+  return cudaLaunchKernelEx(&cfg, gather_kernel<NTV, MT>, p);
+  // register caps: 96 per thread up to 640 threads (d <= 4096), 64 above
+  const bool small = (ncw + 1) * 32 <= 640;
+  if (nt == 1) { if (small) { SESG_G(1, 640) } SESG_G(1, 1024) }
+  if (nt == 2) { if (small) { SESG_G(2, 640) } SESG_G(2, 1024) }
+  if (nt == 4 && small) { SESG_G(4, 640) }
+  return cudaErrorInvalidConfiguration;
 #undef SESG_G
 }
 

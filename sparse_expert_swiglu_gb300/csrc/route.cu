@@ -12,7 +12,7 @@
 namespace sesg {
 
 
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 512;
 
 // Logits of one token: each thread owns EV consecutive experts and a strided set of
 // rows; the rows are fetched RU at a time so that their loads are in flight together.
@@ -28,6 +28,8 @@ __device__ void router_logits(const RouteParams& p, int b, float* logits, float*
   for (int i = 0; i < EV; ++i) acc[i] = 0.f;
   if (rs < nrs) {
     const __half* xb = p.x + (size_t)b * p.d;
+    // (a CTA of kRouteThreads covers nrs * RU rows per pass: every load of a pass is
+    // in flight at once)
     for (int r0 = rs; r0 < p.d; r0 += nrs * RU) {
       float xv[RU];
       uint4 wv[RU];
@@ -296,7 +298,7 @@ size_t route_group_smem(int B, int k) { return (size_t)3 * B * k * sizeof(int); 
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.B <= 4 ? 1 : p.B);  // few tokens: one CTA, no cross-CTA hand-off
+  cfg.gridDim = dim3(p.B);  // one CTA per token; the last one groups the pairs
   cfg.blockDim = dim3(kRouteThreads);
   cfg.dynamicSmemBytes = route_group_smem(p.B, p.k);
   cfg.stream = st;
