@@ -37,7 +37,7 @@ namespace sesg {
 namespace {
 
 constexpr int kDecMaxG = 24;     // groups: 2 tokens x 8 experts + 8 shared experts
-constexpr int kDecMaxE = 32;     // routed experts of the in-kernel router
+constexpr int kDecMaxE = 64;     // routed experts of the in-kernel router
 constexpr int kDecMaxSb = 8;     // superblocks of 512 inputs (d <= 4096)
 constexpr int kDecNV = 4;        // unit slots of superblock partials (a power of two)
 constexpr int kDecMaxSu = 12;    // up-ring stages
@@ -98,7 +98,7 @@ __host__ __device__ inline UpLayoutD up_layout_d(int d, int B, int E, int su, in
   L.off_grp = o;
   o += al16(sizeof(GroupDesc) * kDecMaxG);
   L.off_lred = o;
-  o += (size_t)L.nwarps * 2 * kDecMaxE * 4;
+  o += (size_t)L.nwarps * 2 * E * 4;
   L.off_ent = o;
   o += (size_t)umax * 16 * 16;
   L.total = o;
@@ -289,47 +289,71 @@ __device__ __forceinline__ void dec_route(const DecodeParams& p, int nthreads, c
 #pragma unroll
     for (int i = 0; i < 2; ++i)
       w2[i] = (u8 ? w4[i + 2] : w4[i]) + __shfl_xor_sync(0xffffffffu, u8 ? w4[i] : w4[i + 2], 8);
+    if (nchunk == 8) {
+      // lane bits 0-2 name the chunk: every lane keeps two experts of its chunk
+      const int e2 = (u16 ? 4 : 0) + (u8 ? 2 : 0);
+      lred[(warp * B + b) * E + (lane & 7) * 8 + e2] = w2[0];
+      lred[(warp * B + b) * E + (lane & 7) * 8 + e2 + 1] = w2[1];
+      continue;
+    }
     float v = (u4 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, u4 ? w2[0] : w2[1], 4);
     if (nchunk <= 2) v += __shfl_xor_sync(0xffffffffu, v, 2);
     if (nchunk == 1) v += __shfl_xor_sync(0xffffffffu, v, 1);
-    if ((lane & 3) < nchunk) lred[(warp * B + b) * kDecMaxE + (lane % nchunk) * 8 + e_in] = v;
+    if ((lane & 3) < nchunk) lred[(warp * B + b) * E + (lane % nchunk) * 8 + e_in] = v;
   }
   __syncthreads();
   if (warp == 0) {
   for (int b = 0; b < B; ++b) {
-    // lane e: the logit of expert e, the warps' partial sums added in a fixed order
-    float l = -INFINITY;
-    if (lane < E) {
-      float s = 0.f;
+    // lane j: the logits of experts j and j + 32 (E <= 64), the warps' partial sums
+    // added in a fixed order
+    float l[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = lane + 32 * h;
+      if (e < E) {
+        float s = 0.f;
 #pragma unroll 6
-      for (int w = 0; w < nw; ++w) s += lred[(w * B + b) * kDecMaxE + lane];
-      l = s;
+        for (int w = 0; w < nw; ++w) s += lred[(w * B + b) * E + e];
+        l[h] = s;
+      }
     }
     // top-k by rank: an expert's rank counts the experts with a larger logit, or an
     // equal one and a lower index; ranks 0..k-1 are chosen, listed by rank
-    int rank = 0;
+    int rank[2] = {0, 0};
     for (int e = 0; e < E; ++e) {
-      const float le = __shfl_sync(0xffffffffu, l, e);
-      rank += (le > l || (le == l && e < lane)) ? 1 : 0;
+      const float le = __shfl_sync(0xffffffffu, e < 32 ? l[0] : l[1], e & 31);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) rank[h] += (le > l[h] || (le == l[h] && e < lane + 32 * h)) ? 1 : 0;
     }
-    const bool chosen = lane < E && rank < k;
-    const int top = __ffs(__ballot_sync(0xffffffffu, lane < E && rank == 0)) - 1;
-    const float lmax = __shfl_sync(0xffffffffu, l, top);
+    bool chosen[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) chosen[h] = lane + 32 * h < E && rank[h] < k;
+    // the largest logit (that of the rank-0 expert)
+    float lmax = fmaxf(l[0], l[1]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
     // softmax over the chosen experts (renormalised top-k) or over all E; the
     // denominator is a fixed-order butterfly sum
-    const float ex = (lane < E && (chosen || !p.renorm)) ? expf(l - lmax) : 0.f;
-    float denom = ex;
+    float ex[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      ex[h] = (lane + 32 * h < E && (chosen[h] || !p.renorm)) ? expf(l[h] - lmax) : 0.f;
+    float denom = ex[0] + ex[1];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, off);
-    if (chosen) {
-      const float w = ex / denom;
-      m->tidx[b][rank] = lane;
-      m->tw[b][rank] = w;
-      if (blockIdx.x == 0) {
-        p.topk_idx[b * k + rank] = lane;
-        p.topk_w[b * k + rank] = w;
-        if (p.user_idx) p.user_idx[b * k + rank] = lane;
-        if (p.user_w) p.user_w[b * k + rank] = w;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (chosen[h]) {
+        const int e = lane + 32 * h, r = rank[h];
+        const float w = ex[h] / denom;
+        m->tidx[b][r] = e;
+        m->tw[b][r] = w;
+        if (blockIdx.x == 0) {
+          p.topk_idx[b * k + r] = e;
+          p.topk_w[b * k + r] = w;
+          if (p.user_idx) p.user_idx[b * k + r] = e;
+          if (p.user_w) p.user_w[b * k + r] = w;
+        }
       }
     }
     __syncwarp();
@@ -1156,8 +1180,8 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
 }
 
 bool decode_supported(int B, int d, int f, int E, int k, int n_shared, int P) {
-  // the in-kernel router splits the experts into 1, 2 or 4 chunks of 8
-  if (!(B >= 1 && B <= 2 && d <= kDecMaxD && d % 256 == 0 && (E == 8 || E == 16 || E == 32) &&
+  // the in-kernel router splits the experts into 1, 2, 4 or 8 chunks of 8
+  if (!(B >= 1 && B <= 2 && d <= kDecMaxD && d % 256 == 0 && (E == 8 || E == 16 || E == 32 || E == 64) &&
         k <= kMaxTok && B * k + n_shared <= kDecMaxG && n_shared <= 8 && P >= 1))
     return false;
   const long long units = (long long)(B * k + n_shared) * (f / kMTile);

@@ -345,6 +345,14 @@ def test_decode_wider_routing(E, k, shared, d, f):
     run_layer_case(d, f, E, k, 2, shared, [0, 70], seed=25 + k, gen_device="cuda")
 
 
+@pytest.mark.parametrize("B", [1, 2])
+def test_decode_deepseek_v2_lite(B):
+    """DeepSeek-V2-Lite shape (64 routed experts, top-6, 2 shared experts, d = 2048,
+    f = 1408) on the decode path: the router's 8-chunk reduction and two experts per
+    lane in its top-k."""
+    run_layer_case(2048, 1408, 64, 6, B, 2, [0, 50, 90], seed=60 + B, gen_device="cuda")
+
+
 def test_decode_mixtral_8x7b_b2():
     run_layer_case(4096, 14336, 8, 2, 2, 0, [50, 90], seed=30, gen_device="cuda", rmsnorm=True)
 
@@ -360,7 +368,7 @@ def test_layer_interleaved_gate_down(B):
 
 
 def test_layer_path_selection():
-    """One or two tokens with 8/16/32 routed experts and d <= 4096 take the decode
+    """One or two tokens with 8/16/32/64 routed experts and d <= 4096 take the decode
     kernels; other shapes take the general path."""
     def layer(d, f, E):
         de = synth.experts(E, d, f, 50)
@@ -371,7 +379,8 @@ def test_layer_path_selection():
     assert ses.layer_path(small, 1) == "decode"
     assert ses.layer_path(small, 2) == "decode"
     assert ses.layer_path(small, 3) == "general"
-    assert ses.layer_path(layer(1024, 256, 64), 1) == "general"
+    assert ses.layer_path(layer(1024, 256, 64), 1) == "decode"
+    assert ses.layer_path(layer(1024, 256, 128), 1) == "general"
     assert ses.layer_path(layer(6144, 256, 8), 1) == "general"
 
 
