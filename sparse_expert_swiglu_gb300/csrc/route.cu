@@ -61,24 +61,26 @@ __device__ void router_logits(const RouteParams& p, int b, float* logits, float*
       }
     }
   }
-  // red[rs][e], then a two-level fixed-order sum over the row slots
+  // red[rs][e], then a fixed-order sum over the row slots: warp w adds the slots of
+  // experts w, w + 16, ... with its lanes taking every 32nd slot, then a butterfly
   if (rs < nrs) {
 #pragma unroll
     for (int i = 0; i < EV; ++i) red[rs * p.E + ec * EV + i] = acc[i];
   }
   __syncthreads();
-  const int Q = kRouteThreads / p.E;  // >= 1
-  float part = 0.f;
-  const int e0 = tid % p.E, q0 = tid / p.E;
-  if (q0 < Q)
-    for (int r = q0; r < nrs; r += Q) part += red[r * p.E + e0];
-  __syncthreads();
-  if (q0 < Q) red[q0 * p.E + e0] = part;
-  __syncthreads();
-  for (int e = tid; e < p.E; e += kRouteThreads) {
-    float s = 0.f;
-    for (int q = 0; q < Q; ++q) s += red[q * p.E + e];
-    logits[e] = s;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = kRouteThreads / 32;
+  for (int e = warp; e < p.E; e += nwarps) {
+    float s0 = 0.f, s1 = 0.f;
+    int r = lane;
+    for (; r + 32 < nrs; r += 64) {
+      s0 += red[r * p.E + e];
+      s1 += red[(r + 32) * p.E + e];
+    }
+    if (r < nrs) s0 += red[r * p.E + e];
+    float s = s0 + s1;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) logits[e] = s;
   }
   __syncthreads();
 }
@@ -176,16 +178,32 @@ __device__ void router_group(const RouteParams& p, bool local) {
     if (p.expert_count) p.expert_count[e] = c;
   }
   __syncthreads();
-  if (tid == 0) {
+  if (tid < 32) {
+    // exclusive prefixes of the pair counts and of the group counts (warp scans)
     int o = 0, go = 0;
-    for (int e = 0; e < p.E; ++e) {
-      s_off[e] = o;
-      s_goff[e] = go;
-      o += s_cnt[e];
-      go += (s_cnt[e] + p.gcap - 1) / p.gcap;
+    for (int base = 0; base < p.E; base += 32) {
+      const int e = base + tid;
+      const int c = e < p.E ? s_cnt[e] : 0, gc = (c + p.gcap - 1) / p.gcap;
+      int ic = c, ig = gc;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int oc = __shfl_up_sync(0xffffffffu, ic, off), og = __shfl_up_sync(0xffffffffu, ig, off);
+        if (tid >= off) {
+          ic += oc;
+          ig += og;
+        }
+      }
+      if (e < p.E) {
+        s_off[e] = o + ic - c;
+        s_goff[e] = go + ig - gc;
+      }
+      o += __shfl_sync(0xffffffffu, ic, 31);
+      go += __shfl_sync(0xffffffffu, ig, 31);
     }
-    s_off[p.E] = o;
-    s_goff[p.E] = go;
+    if (tid == 0) {
+      s_off[p.E] = o;
+      s_goff[p.E] = go;
+    }
   }
   __syncthreads();
   if (!p.group) return;
