@@ -33,9 +33,9 @@ cudaError_t device_info(DeviceInfo& di) {
 
 // Tokens of one expert handled together: their fp32 accumulators must fit in the
 // gather kernel's registers (8 x 8 floats per thread up to d = 4096, 4 x 8 up to 6144).
-// tokens per expert group: the gather kernel keeps x and the output of every token of a
-// group in registers
-int group_cap(int d) { return d <= 4096 ? 4 : 2; }
+// tokens per expert group: up to 8 where the gather kernel runs on the tensor cores
+// (d <= 4096), 2 where it keeps x and the outputs of a group in registers
+int group_cap(int d) { return d <= 4096 ? 8 : 2; }
 
 int groups_max_routed(int B, int E, int k, int gcap) {
   const long long pairs = (long long)B * k;
@@ -131,7 +131,7 @@ moe_status_t plan(const DeviceInfo& di, const WsLayout& L, int d, int f, int max
   const int occ = up_blocks_per_sm(d, max_tok);
   if (occ < 1) return MOE_ERR_UNSUPPORTED_SHAPE;
   pl.up_grid = di.sms * occ;
-  pl.nt = max_tok <= 1 ? 1 : max_tok <= 2 ? 2 : 4;
+  pl.nt = max_tok <= 1 ? 1 : max_tok <= 2 ? 2 : max_tok <= 4 ? 4 : 8;
   const size_t fixed = gather_smem_bytes(d, 0, pl.nt, L.list_cap, L.G_max) + 2048;
   const size_t stage = (size_t)4 * d + 32 + 16;
   if (fixed + 2 * stage > (size_t)di.smem_optin) return MOE_ERR_UNSUPPORTED_SHAPE;

@@ -24,10 +24,29 @@ constexpr int kChunk = 8;  // fp16 elements per 16-byte chunk
 
 struct GatherLayout {
   size_t off_full, off_empty, off_stage, off_lslot, off_lcol, off_lgrp, off_red, off_hbuf, off_tmp,
-      off_goff, total, stage_bytes;
+      off_goff, off_x, off_h16, total, stage_bytes;
 };
 
+// Tensor-core consumers (groups of up to 8 tokens, d <= 4096): the group's x in shared
+// memory, 8 rows of d + 8 halves (the padding spreads the rows over the banks).
+constexpr int kMmaTok = 8;
+constexpr int kMmaBatch = 4;  // kept rows per batch
+__host__ __device__ inline bool gather_mma(int d, int nt) { return d <= 4096 && nt >= 2; }
+
 constexpr int kGaBatchTok = 16;  // items per batch x tokens per group, at most
+
+// Two 8x8 fp16 matrices from shared memory (rows given by lanes 0-7 and 8-15), as
+// mma operand fragments; .trans delivers them transposed.
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
 
 // Warp sums of V values (V a power of two <= 32) by recursive halving: at each of the
 // first log2(V) levels every lane keeps half of its values and adds its partner's copy
@@ -58,7 +77,6 @@ __host__ __device__ inline GatherLayout gather_layout(int d, int stages, int nt,
                                                       int g_max) {
   GatherLayout L;
   const int ncw = d / 256;
-  (void)nt;
   size_t o = 0;
   L.off_full = o;
   o += 8 * (size_t)stages;
@@ -84,6 +102,15 @@ __host__ __device__ inline GatherLayout gather_layout(int d, int stages, int nt,
   o += (size_t)1040 * 4;
   L.off_goff = o;  // kept-item offsets of the groups [G_max + 1]
   o += ((size_t)g_max + 1) * 4;
+  o = (o + 127) & ~(size_t)127;
+  L.off_x = L.off_h16 = o;
+  if (gather_mma(d, nt)) {
+    L.off_x = o;  // [8][d + 8] fp16
+    o += (size_t)kMmaTok * (d + 8) * 2;
+    o = (o + 127) & ~(size_t)127;
+    L.off_h16 = o;  // [hi, lo][8 tokens][16 items] fp16
+    o += (size_t)2 * kMmaTok * 16 * 2;
+  }
   L.total = o;
   return L;
 }
@@ -125,12 +152,12 @@ __device__ void block_exclusive_scan(int* data, int n, int* tmp) {
   __syncthreads();
 }
 
-template <int NT, int MAXT>
+template <int NT, int MAXT, bool MMA>
 __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
   extern __shared__ __align__(128) uint8_t gsm[];
   // items per batch (one barrier per batch), within the register budget
-  constexpr int kR = NT == 4 ? 2 : (MAXT > 640 && NT == 2) ? 2 : 4;
-  static_assert(kR * NT <= kGaBatchTok, "batch buffers");
+  constexpr int kR = NT >= 4 ? 2 : (MAXT > 640 && NT == 2) ? 2 : 4;
+  static_assert(MMA || kR * NT <= kGaBatchTok, "batch buffers");
   const int d = p.d;
   const int ncw = d / 256;   // consumer warps
   const int nct = ncw * 32;  // consumer threads
@@ -178,9 +205,15 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
   // ring positions: the producer's next stage and the consumers' next stage, each with
   // its barrier parity, advanced one item at a time (no divisions in the loops)
   int ps = 0, pph = 0, cs = 0, cph = 0;
-  float2 acc[NT][kChunk / 2];
-  float2 xf[NT][kChunk / 2];
-  float wt[NT];
+  float2 acc[MMA ? 1 : NT][kChunk / 2];
+  float2 xf[MMA ? 1 : NT][kChunk / 2];
+  float wt[MMA ? 1 : NT];
+  if constexpr (MMA) {
+    // the h buffer's items 4..15 stay zero (a batch holds at most kMmaBatch items)
+    __half* h16 = reinterpret_cast<__half*>(gsm + L.off_h16);
+    for (int i = tid; i < 2 * kMmaTok * 16; i += blockDim.x) h16[i] = __float2half(0.f);
+    __syncthreads();
+  }
 
   for (int wa = a; wa < b; wa += p.list_cap) {
     const int wb = min(b, wa + p.list_cap);
@@ -255,6 +288,177 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
             pph ^= 1;
           }
         }
+      }
+    } else if constexpr (MMA) {
+      // ---- consumers on the tensor cores, for groups of up to 8 tokens.  Warp w owns
+      // the hidden slice [256 w, 256 w + 256).  Per batch of up to 4 kept rows:
+      //   dots   D[row][token] += G[row][k] . X[k][token]: mma.m16n8k16 with the gate
+      //          rows as A (ldmatrix from the stages; rows 4..15 absent) and the group's x
+      //          as B (shared memory), 16 k-steps over the warp's slice;
+      //   h      warp 0 adds the 16 warps' partial dots, h = SiLU(.) * v * w, split into
+      //          fp16 hi + lo (hi + lo carries h to about 22 bits);
+      //   down   acc[col][token] += Down^T[col][row] . H[row][token]: ldmatrix.trans of
+      //          the down rows as A, hi and lo as B (two mma per 16 columns).
+      __half* xs = reinterpret_cast<__half*>(gsm + L.off_x);
+      __half* h16 = reinterpret_cast<__half*>(gsm + L.off_h16);
+      float* redm = red;  // [ncw][4 rows][8 tokens]
+      const int xstride = d + 8;
+      const int gid = lane >> 2, c = lane & 3;
+      const int kw = warp * 256;
+      const int lit = lane & 7, lhalf = (lane >> 3) & 1;  // ldmatrix: row, 8-column half
+      auto bar_or = [&](bool bad) -> bool {
+        int fail;
+        asm volatile(
+            "{\n\t.reg .pred pin, pout;\n\t"
+            "setp.ne.u32 pin, %1, 0;\n\t"
+            "barrier.red.or.pred pout, 1, %2, pin;\n\t"
+            "selp.u32 %0, 1, 0, pout;\n\t}"
+            : "=r"(fail)
+            : "r"((unsigned)bad), "r"(nct)
+            : "memory");
+        return fail != 0;
+      };
+      bool stop = false;
+      int i = 0;
+      while (i < n && !stop) {
+        const int g = lgrp[i];
+        int e = i;
+        while (e < n && lgrp[e] == g) ++e;
+        // segment start: the group, and its tokens' x in shared memory (zero rows after
+        // the last token)
+        named_barrier(1, nct);
+        if (tid == 0) s_gd = p.groups[g];
+        named_barrier(1, nct);
+        const int ntok = s_gd.n_tok;
+#pragma unroll
+        for (int t = 0; t < kMmaTok; ++t) {
+          uint4 xv = make_uint4(0, 0, 0, 0);
+          if (t < ntok) xv = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)s_gd.tok[t] * d) + tid);
+          reinterpret_cast<uint4*>(xs + (size_t)t * xstride)[tid] = xv;
+        }
+        const float wtl = (lane & 7) < ntok ? s_gd.w[lane & 7] : 0.f;  // warp 0: token lane % 8
+        float accm[16][4];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) accm[j][0] = accm[j][1] = accm[j][2] = accm[j][3] = 0.f;
+        named_barrier(1, nct);
+        for (int i0 = i; i0 < e; i0 += kMmaBatch) {
+          const int nb = min(kMmaBatch, e - i0);
+          int sq0 = cs, sq1 = cs, sq2 = cs, sq3 = cs;
+          bool ok = !*reinterpret_cast<volatile int*>(&s_abort);
+#pragma unroll
+          for (int q = 0; q < kMmaBatch; ++q) {
+            if (q < nb) {
+              if (q == 0) sq0 = cs;
+              if (q == 1) sq1 = cs;
+              if (q == 2) sq2 = cs;
+              if (q == 3) sq3 = cs;
+              ok = ok && mbar_wait(&full[cs], cph);
+              if (++cs == S) {
+                cs = 0;
+                cph ^= 1;
+              }
+            }
+          }
+          // this lane's ldmatrix row: kept row lit of the batch.  Absent rows repeat row
+          // 0 (same address: no bank conflict; finite weights whose dot products are not
+          // used and whose down contributions are multiplied by h = 0)
+          const int sl = (lit < nb) ? (lit == 1 ? sq1 : lit == 2 ? sq2 : lit == 3 ? sq3 : sq0) : sq0;
+          const uint32_t sbase = smem_addr(stage + (size_t)sl * L.stage_bytes);
+          const uint32_t garow = sbase + (uint32_t)(kw + lhalf * 8) * 2u;
+          const uint32_t darow = sbase + (uint32_t)(2 * d) + (uint32_t)(kw + lhalf * 8) * 2u;
+          // two accumulator chains (even and odd k-steps) halve the dependent mma latency
+          float dd[4] = {0.f, 0.f, 0.f, 0.f}, de[4] = {0.f, 0.f, 0.f, 0.f};
+          if (ok) {
+            const __half* xg = xs + (size_t)gid * xstride + kw + 2 * c;
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              uint32_t a[4], a2[4];
+              ldsm_x2(garow + j * 32u, a[0], a[2]);
+              ldsm_x2(garow + (j + 1) * 32u, a2[0], a2[2]);
+              a[1] = a[3] = a2[1] = a2[3] = 0u;
+              mma_16816(dd, a, *reinterpret_cast<const uint32_t*>(xg + j * 16),
+                        *reinterpret_cast<const uint32_t*>(xg + j * 16 + 8));
+              mma_16816(de, a2, *reinterpret_cast<const uint32_t*>(xg + (j + 1) * 16),
+                        *reinterpret_cast<const uint32_t*>(xg + (j + 1) * 16 + 8));
+            }
+            dd[0] += de[0];
+            dd[1] += de[1];
+          }
+          if (gid < kMmaBatch) {
+            redm[(warp * kMmaBatch + gid) * kMmaTok + 2 * c] = dd[0];
+            redm[(warp * kMmaBatch + gid) * kMmaTok + 2 * c + 1] = dd[1];
+          }
+          if (bar_or(!ok)) {
+            if (tid == 0) {
+              set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
+              atomicExch(&s_abort, 1);
+            }
+            stop = true;
+            break;
+          }
+          if (warp == 0) {
+            // lane = row * 8 + token
+            const int it = lane >> 3, t = lane & 7;
+            float hq = 0.f;
+            if (it < nb && t < ntok) {
+              float s0 = 0.f, s1 = 0.f;
+              int w = 0;
+              for (; w + 1 < ncw; w += 2) {
+                s0 += redm[(w * kMmaBatch + it) * kMmaTok + t];
+                s1 += redm[((w + 1) * kMmaBatch + it) * kMmaTok + t];
+              }
+              if (w < ncw) s0 += redm[(w * kMmaBatch + it) * kMmaTok + t];
+              const int si = it == 0 ? sq0 : it == 1 ? sq1 : it == 2 ? sq2 : sq3;
+              const float* hv = reinterpret_cast<const float*>(stage + (size_t)si * L.stage_bytes + 4 * d);
+              hq = silu_f(s0 + s1) * hv[t] * wtl;
+            }
+            const __half hi = __float2half_rn(hq);
+            const __half lo = __float2half_rn(hq - __half2float(hi));
+            h16[(0 * kMmaTok + t) * 16 + it] = hi;
+            h16[(1 * kMmaTok + t) * 16 + it] = lo;
+          }
+          named_barrier(1, nct);
+          {
+            const uint32_t bhi = *reinterpret_cast<const uint32_t*>(h16 + (0 * kMmaTok + gid) * 16 + 2 * c);
+            const uint32_t blo = *reinterpret_cast<const uint32_t*>(h16 + (1 * kMmaTok + gid) * 16 + 2 * c);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              uint32_t a[4];
+              ldsm_x2_trans(darow + j * 32u, a[0], a[1]);
+              a[2] = a[3] = 0u;
+              mma_16816(accm[j], a, bhi, 0u);
+              mma_16816(accm[j], a, blo, 0u);
+            }
+          }
+          // the batch's stages are free once every warp has read them
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&empty[sq0]);
+            if (nb > 1) mbar_arrive(&empty[sq1]);
+            if (nb > 2) mbar_arrive(&empty[sq2]);
+            if (nb > 3) mbar_arrive(&empty[sq3]);
+          }
+          if (tid == 0) s_consumed = base + i0 + nb;
+        }
+        // segment end: this CTA's partial output of the group; accm[j] holds columns
+        // kw + 16 j + gid (+ 8) of tokens 2c and 2c + 1
+        if (!stop) {
+          float* dst = p.part + ((size_t)(blockIdx.x + g) * kMaxTok) * d;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = kw + 16 * j + gid;
+            if (2 * c < ntok) {
+              dst[(size_t)(2 * c) * d + col] = accm[j][0];
+              dst[(size_t)(2 * c) * d + col + 8] = accm[j][2];
+            }
+            if (2 * c + 1 < ntok) {
+              dst[(size_t)(2 * c + 1) * d + col] = accm[j][1];
+              dst[(size_t)(2 * c + 1) * d + col + 8] = accm[j][3];
+            }
+          }
+        }
+        if (tid == 0) s_consumed = base + e;
+        i = e;
       }
     } else {
       // ---- consumers: segments of equal group; in a segment, batches of up to kR
@@ -461,17 +665,18 @@ cudaError_t launch_gather(const ExpertParams& p, int nt, cudaStream_t st, bool p
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
-#define SESG_G(NTV, MT)                                                                            \
-  if ((ncw + 1) * 32 > MT) return cudaErrorInvalidConfiguration;                                  \
-  e = cudaFuncSetAttribute(gather_kernel<NTV, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
-                           (int)smem);                                                             \
-  if (e != cudaSuccess) return e;                                                                  \
-  return cudaLaunchKernelEx(&cfg, gather_kernel<NTV, MT>, p);
+#define SESG_G(NTV, MT, MM)                                                                        \
+  if ((ncw + 1) * 32 > MT) return cudaErrorInvalidConfiguration;                                     \
+  e = cudaFuncSetAttribute(gather_kernel<NTV, MT, MM>, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
+                           (int)smem);                                                                \
+  if (e != cudaSuccess) return e;                                                                     \
+  return cudaLaunchKernelEx(&cfg, gather_kernel<NTV, MT, MM>, p);
   // register caps: 96 per thread up to 640 threads (d <= 4096), 64 above
   const bool small = (ncw + 1) * 32 <= 640;
-  if (nt == 1) { if (small) { SESG_G(1, 640) } SESG_G(1, 1024) }
-  if (nt == 2) { if (small) { SESG_G(2, 640) } SESG_G(2, 1024) }
-  if (nt == 4 && small) { SESG_G(4, 640) }
+  if (gather_mma(p.d, nt)) { SESG_G(8, 640, true) }
+  if (nt == 1) { if (small) { SESG_G(1, 640, false) } SESG_G(1, 1024, false) }
+  if (nt == 2) { if (small) { SESG_G(2, 640, false) } SESG_G(2, 1024, false) }
+  if (nt == 4 && small) { SESG_G(4, 640, false) }
   return cudaErrorInvalidConfiguration;
 #undef SESG_G
 }
