@@ -56,7 +56,7 @@ METRIC = "MoE decode layer expert-tokens/s (Mixtral-8x7B-shaped layer, 1 token, 
 NCU_TRAFFIC = {
     # decode_gather_kernel: 147.68 MB (read + write) captured on layer copy 0 at 70% (the
     # 1-copy small case, 143.97 MB algorithmic), scaled to the 8-copy mean of 139.12 MB
-    ("decode_gather_kernel", "232dd32c4b2ac70d"): 147.68e6 * 139.12 / 143.97,
+    ("decode_gather_kernel", "5e9db423f1b1cd24"): 147.68e6 * 139.12 / 143.97,
 }
 
 
@@ -342,10 +342,13 @@ def per_kernel_times(prof_graphs, events_list, stream, steps, path):
     return {"route_kernel": t[0], "up_kernel": t[1], "gather_kernel": t[2], "combine_kernel": t[3]}
 
 
-def source_hash():
+def source_hash(kernel="decode_gather_kernel"):
+    """Hash of the sources a kernel is built from (the traffic table is keyed by it)."""
     import hashlib
     h = hashlib.sha256()
-    for fn in ["up.cu", "gather.cu", "combine.cu", "decode.cu", "common.cuh", "params.cuh"]:
+    files = (["decode.cu", "common.cuh", "params.cuh"] if kernel.startswith("decode_")
+             else ["up.cu", "gather.cu", "combine.cu", "route.cu", "common.cuh", "params.cuh"])
+    for fn in files:
         with open(os.path.join(ROOT, "sparse_expert_swiglu_gb300", "csrc", fn), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -518,7 +521,7 @@ def run_ours(args, world, rank, local):
         kernel_bytes = {"up_kernel": up_b, "gather_kernel": ga_b, "route_kernel": rt_b}
     dominant = max((k for k in kernel_bytes if k in kt and k != "route_kernel"), key=lambda kname: kt[kname])
     achieved = kernel_bytes[dominant] / (kt[dominant] * 1e-6) / 1e9
-    traffic = NCU_TRAFFIC.get((dominant, source_hash()))
+    traffic = NCU_TRAFFIC.get((dominant, source_hash(dominant)))
 
     # end to end through the public API: pinned host token in, host result out
     x_host = torch.stack([synth.tokens(B, d, 5000 + i, device="cpu") for i in range(64)]).pin_memory()
