@@ -213,7 +213,7 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
 /*
  * moe_layer_path -- which kernels moe_layer_decode runs for this layer and B tokens on
  * the current device: 1 = the decode path (one or two tokens, 8/16/32/64 routed experts,
- * d <= 4096: an up-projection kernel that also routes and a gather kernel that also
+ * d <= 6144: an up-projection kernel that also routes and a gather kernel that also
  * combines), 0 = the general path (router, up-projection, gather and combine kernels),
  * or a negative moe_status_t for an invalid layer.  Both paths compute the same layer.
  * The general path is bitwise reproducible; on the decode path the experts' shares

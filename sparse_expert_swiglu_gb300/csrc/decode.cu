@@ -38,19 +38,24 @@ namespace {
 
 constexpr int kDecMaxG = 24;     // groups: 2 tokens x 8 experts + 8 shared experts
 constexpr int kDecMaxE = 64;     // routed experts of the in-kernel router
-constexpr int kDecMaxSb = 8;     // superblocks of 512 inputs (d <= 4096)
+constexpr int kDecMaxSb = 12;    // superblocks of 512 inputs (d <= 6144)
 constexpr int kDecNV = 4;        // unit slots of superblock partials (a power of two)
 constexpr int kDecMaxSu = 12;    // up-ring stages
 constexpr int kDecMaxSr = 16;    // row-ring stages
 constexpr int kDecMaxUnits = 128;  // units per CTA
 constexpr int kDecRows = 4;      // kept rows per gather batch
-constexpr int kDecMaxGw = 16;    // gather warps
-constexpr int kUpThreads = (2 * kDecMaxSb + 3) * 32;  // up warps, strip producer, 2 finalize warps
+constexpr int kDecMaxGw = 24;    // gather warps
+// up kernel: two unit lanes of up to 8 superblock warps (d <= 4096) or one lane of up to 12,
+// plus the strip producer and one finalize warp per lane
+__host__ __device__ constexpr int dec_lanes(int nsb) { return nsb <= 8 ? 2 : 1; }
+constexpr int kUpThreads = (2 * 8 + 3) * 32;
+static_assert((kDecMaxSb + 2) * 32 <= kUpThreads, "one-lane up kernel block");
 // register cap of the up kernel: 96 per thread, so that 5 warps fit one SM sub-partition
 constexpr int kUpRegThreads = 640;
 static_assert(kUpThreads <= kUpRegThreads, "up kernel block exceeds its register budget");
 constexpr int kGaThreads = (kDecMaxGw + 1) * 32;      // gather warps + the row producer warp
-constexpr int kDecMaxD = 4096;
+constexpr int kGaSmallThreads = (16 + 1) * 32;       // d <= 4096: 96 registers per thread
+constexpr int kDecMaxD = 6144;
 
 __host__ __device__ inline size_t al16(size_t o) { return (o + 15) & ~(size_t)15; }
 
@@ -76,7 +81,7 @@ struct UpLayoutD {
 __host__ __device__ inline UpLayoutD up_layout_d(int d, int B, int E, int su, int umax) {
   UpLayoutD L;
   L.nsb = n_superblocks(d);
-  L.nwarps = 2 * L.nsb + 3;
+  L.nwarps = dec_lanes(L.nsb) * (L.nsb + 1) + 1;
   L.su = su;
   L.strip = (size_t)L.nsb * kBlkBytes;
   L.ring = L.strip * su;
@@ -681,13 +686,14 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_up_kernel(DecodeParam
   const int n = u1 - u0;
 
   int4* ent = reinterpret_cast<int4*>(usm + L.off_ent);  // [unit][16] kept columns
-  if (warp > 2 * nsb) {
+  const int NL = dec_lanes(nsb);
+  if (warp > NL * nsb) {
     // ---- finalize warps, one per unit lane: each unit once all its superblock
     // partials are in; its kept columns go to the unit's 16 entries
-    const int fl = warp - 2 * nsb - 1;
+    const int fl = warp - NL * nsb - 1;
     int g = (u0 + fl) / MT, mt = (u0 + fl) - g * MT, cur_g = -1;
     float thr = 0.f;
-    for (int j = fl; j < n; j += 2) {
+    for (int j = fl; j < n; j += NL) {
       const int slot = j & (kDecNV - 1);
       if (!__all_sync(0xffffffffu, mbar_wait(&vfull[slot], (j >> 2) & 1))) {
         if (lane == 0) dec_fail(p, &m->abort);
@@ -704,13 +710,13 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_up_kernel(DecodeParam
       if (lane == 0) m->ucnt[j] = cnt;
       __syncwarp();
       if (lane == 0) mbar_arrive(&vfree[slot]);
-      mt += 2;
+      mt += NL;
       while (mt >= MT) {
         mt -= MT;
         ++g;
       }
     }
-  } else if (warp == 2 * nsb) {
+  } else if (warp == NL * nsb) {
     // ---- producer warp: the strips of this CTA's units, in order
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
@@ -748,7 +754,7 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_up_kernel(DecodeParam
     // (group g, M-tile mt), all advanced by 2 units per iteration without divisions
     int s = ug % SU, ph = (ug / SU) & 1;
     int g = (u0 + ug) / MT, mt = (u0 + ug) - g * MT;
-    for (int j = ug; j < n; j += 2) {
+    for (int j = ug; j < n; j += NL) {
       const int slot = j & (kDecNV - 1);
       const bool ab = vload(&m->abort) != 0;
       bool ok = __all_sync(0xffffffffu, !ab && mbar_wait(&full[s], ph));
@@ -779,12 +785,12 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_up_kernel(DecodeParam
       vpart[((size_t)slot * nsb + sb) * 32 + lane] = make_float4(vacc[0][0], vacc[0][1], vacc[1][0], vacc[1][1]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&vfull[slot]);
-      s += 2;
+      s += NL;
       if (s >= SU) {
         s -= SU;
         ph ^= 1;
       }
-      mt += 2;
+      mt += NL;
       while (mt >= MT) {
         mt -= MT;
         ++g;
@@ -833,8 +839,8 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_up_kernel(DecodeParam
 // gate and down rows are interleaved in one buffer costs one 4d-byte copy, else two
 // 2d-byte copies.
 // ---------------------------------------------------------------------------
-template <int B>
-__global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodeParams p) {
+template <int B, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1) decode_gather_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t gsm[];
   const int d = p.d, SR = p.sr, P = gridDim.x;
   const GaLayoutD L = ga_layout_d(d, SR, p.list_cap, P);
@@ -1090,8 +1096,12 @@ __global__ void __launch_bounds__(kGaThreads, 1) decode_gather_kernel(DecodePara
           if (t >= 0) {
             const float4* pr = reinterpret_cast<const float4*>(rb + (q * 2 + b) * kDecMaxGw);
             const float4 p0 = pr[0], p1 = pr[1], p2 = pr[2], p3 = pr[3];  // unused slots hold 0
-            const float gs = (((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w))) +
-                             (((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w)));
+            float gs = (((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w))) +
+                       (((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w)));
+            if (ngw > 16) {
+              const float4 p4 = pr[4], p5 = pr[5];
+              gs += ((p4.x + p4.y) + (p4.z + p4.w)) + ((p5.x + p5.y) + (p5.z + p5.w));
+            }
             hq = silu_fast(gs) * (t == 0 ? gr.v[0] : gr.v[1]) * m->tw[gr.g][b];
           }
         }
@@ -1247,11 +1257,19 @@ cudaError_t launch_decode_gather(const DecodeParams& p, cudaStream_t st, bool pd
   const GaLayoutD L = ga_layout_d(p.d, p.sr, p.list_cap, p.P);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_cfg(dim3(p.P), dim3(L.nwarps * 32), L.total, st, attr, pdl);
-  const void* fn = p.B == 1 ? (const void*)decode_gather_kernel<1> : (const void*)decode_gather_kernel<2>;
+  // d <= 4096: at most 17 warps (96 registers per thread); above, up to 25 warps
+  const bool small = L.nwarps * 32 <= kGaSmallThreads;
+  const void* fn = small ? (p.B == 1 ? (const void*)decode_gather_kernel<1, kGaSmallThreads>
+                                     : (const void*)decode_gather_kernel<2, kGaSmallThreads>)
+                         : (p.B == 1 ? (const void*)decode_gather_kernel<1, kGaThreads>
+                                     : (const void*)decode_gather_kernel<2, kGaThreads>);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
   if (e != cudaSuccess) return e;
-  if (p.B == 1) return cudaLaunchKernelEx(&cfg, decode_gather_kernel<1>, p);
-  return cudaLaunchKernelEx(&cfg, decode_gather_kernel<2>, p);
+  if (small)
+    return p.B == 1 ? cudaLaunchKernelEx(&cfg, decode_gather_kernel<1, kGaSmallThreads>, p)
+                    : cudaLaunchKernelEx(&cfg, decode_gather_kernel<2, kGaSmallThreads>, p);
+  return p.B == 1 ? cudaLaunchKernelEx(&cfg, decode_gather_kernel<1, kGaThreads>, p)
+                  : cudaLaunchKernelEx(&cfg, decode_gather_kernel<2, kGaThreads>, p);
 }
 
 }  // namespace sesg

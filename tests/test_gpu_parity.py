@@ -346,6 +346,13 @@ def test_decode_wider_routing(E, k, shared, d, f):
 
 
 @pytest.mark.parametrize("B", [1, 2])
+def test_decode_wide_hidden(B):
+    """d = 6144 (Mixtral-8x22B width) on the decode path: one unit lane of 12 superblock
+    warps in the up kernel, 24 gather warps."""
+    run_layer_case(6144, 1024, 8, 2, B, 0, [0, 70], seed=70 + B, gen_device="cuda", rmsnorm=(B == 2))
+
+
+@pytest.mark.parametrize("B", [1, 2])
 def test_decode_deepseek_v2_lite(B):
     """DeepSeek-V2-Lite shape (64 routed experts, top-6, 2 shared experts, d = 2048,
     f = 1408) on the decode path: the router's 8-chunk reduction and two experts per
@@ -368,7 +375,7 @@ def test_layer_interleaved_gate_down(B):
 
 
 def test_layer_path_selection():
-    """One or two tokens with 8/16/32/64 routed experts and d <= 4096 take the decode
+    """One or two tokens with 8/16/32/64 routed experts and d <= 6144 take the decode
     kernels; other shapes take the general path."""
     def layer(d, f, E):
         de = synth.experts(E, d, f, 50)
@@ -381,7 +388,8 @@ def test_layer_path_selection():
     assert ses.layer_path(small, 3) == "general"
     assert ses.layer_path(layer(1024, 256, 64), 1) == "decode"
     assert ses.layer_path(layer(1024, 256, 128), 1) == "general"
-    assert ses.layer_path(layer(6144, 256, 8), 1) == "general"
+    assert ses.layer_path(layer(6144, 256, 8), 1) == "decode"
+    assert ses.layer_path(layer(6400, 256, 8), 1) == "general"
 
 
 def _same_up_to_sum_order(a, b):
