@@ -163,8 +163,8 @@ __device__ __forceinline__ void up_superblock(const uint8_t* __restrict__ blk,
 // 16 columns, step 2 (mask = |v| > t, union over the group's tokens), compaction of
 // the kept columns by ballot, and the optional debug outputs.
 template <int T>
-__device__ __forceinline__ void up_finalize(const ExpertParams& p, const GroupDesc& gd, long long u,
-                                            int mt, float thr, const float (&vacc)[2][2],
+__device__ __forceinline__ void up_finalize(const ExpertParams& p, const GroupDesc& gd, int g,
+                                            long long u, int mt, float thr, const float (&vacc)[2][2],
                                             float* __restrict__ vbuf) {
   constexpr int G = 8 / T;
   const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
@@ -218,7 +218,6 @@ __device__ __forceinline__ void up_finalize(const ExpertParams& p, const GroupDe
   }
   if (lane == 0) {
     p.unit_cnt[u] = (uint8_t)__popc(bal);
-    const int g = (int)(u / (p.f / kMTile));
     if (bal) atomicAdd(&p.group_total[g], __popc(bal));
   }
   if (p.dbg_v || p.dbg_mask) {
@@ -306,17 +305,17 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
   const long long U = (long long)G * MT;
   const long long u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
   const int ngrp = d / kGroup;
-  // steps: up to mpar consecutive units of one group; stage = spp consecutive steps
-  auto step_end = [&](long long us) { return min(min(us + L.mpar, u1), (us / MT + 1) * MT); };
+  // steps: up to mpar consecutive units of one group; stage = up to spp consecutive steps
 
   if (warp == prod_warp) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int j = 0;
+      // stage st (ring slot s, parity ph) and the group g of unit us, advanced without
+      // divisions
+      int st = 0, s = 0, ph = 0;
+      long long g_lo = u0 >= 0 ? (u0 / MT) * MT : 0;  // first unit of us's group
       for (long long us = u0; us < u1;) {
-        const int st = j / spp;
-        const int s = st % S;
-        if (st >= S && !mbar_wait(&empty[s], ((st / S) - 1) & 1)) {
+        if (st >= S && !mbar_wait(&empty[s], ph ^ 1)) {
           set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
           atomicExch(&s_abort, 1);
           break;
@@ -326,24 +325,33 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
         long long ends[4];
         uint32_t bytes = 0;
         int nst = 0;
-        for (long long v = us; v < u1 && nst < spp; ++nst) {
-          ends[nst] = step_end(v);
-          bytes += (uint32_t)((ends[nst] - v) * L.strip);
-          v = ends[nst];
+        {
+          long long glo = g_lo;
+          for (long long v = us; v < u1 && nst < spp; ++nst) {
+            if (v >= glo + MT) glo += MT;
+            ends[nst] = min(min(v + L.mpar, u1), glo + MT);
+            bytes += (uint32_t)((ends[nst] - v) * L.strip);
+            v = ends[nst];
+          }
         }
         mbar_arrive_expect_tx(&full[s], bytes);
         for (int q = 0; q < nst; ++q) {
           const long long ue = ends[q];
-          const int g = (int)(us / MT);
+          if (us >= g_lo + MT) g_lo += MT;
+          const int g = (int)(g_lo / MT);
           int el;
           const ExpertSet& es = expert_set(p, p.groups[g].expert, el);
-          const uint8_t* src = es.up + (size_t)el * es.up_stride + (size_t)(us - (long long)g * MT) * L.strip;
+          const uint8_t* src = es.up + (size_t)el * es.up_stride + (size_t)(us - g_lo) * L.strip;
           bulk_g2s(stage + (size_t)s * L.stage_bytes + (size_t)q * L.mpar * L.strip, src,
                    (uint32_t)((ue - us) * L.strip), &full[s], pol);
           us = ue;
-          ++j;
         }
         s_issued = st + 1;
+        ++st;
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
       }
     }
   } else {
@@ -354,10 +362,17 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
     int cur_g = -1, T = 1;
     float thr = 0.f;
     uint32_t bf[64];
-    int j = 0;
-    for (long long us = u0; us < u1; ++j) {
-      const long long ue = step_end(us);
-      const int g = (int)(us / MT);
+    // step position: jj within the stage, stage st (ring slot s, parity ph); the group g
+    // of unit us and its first unit g_lo; all advanced without divisions
+    int jj = 0, st = 0, s = 0, ph = 0, jpar = 0;
+    int g = (int)(u0 / MT);
+    long long g_lo = (long long)g * MT;
+    for (long long us = u0; us < u1;) {
+      if (us >= g_lo + MT) {
+        g_lo += MT;
+        ++g;
+      }
+      const long long ue = min(min(us + L.mpar, u1), g_lo + MT);
       if (g != cur_g) {
         named_barrier(1, nbar);
         if (threadIdx.x == 0) s_gd = p.groups[g];
@@ -396,17 +411,16 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
         named_barrier(1, nbar);
         cur_g = g;
       }
-      const int st = j / spp, s = st % S;
-      const bool first = (j % spp) == 0;
-      const bool last = ((j % spp) == spp - 1) || ue >= u1;
+      const bool first = jj == 0;
+      const bool last = jj == spp - 1 || ue >= u1;
       bool ok = true;
       if (!fin) {
-        if (first) ok = mbar_wait(&full[s], (st / S) & 1);
+        if (first) ok = mbar_wait(&full[s], ph);
         const bool active = us + m_slot < ue;
         float vacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
         if (active && ok) {
           const uint8_t* blk = stage + (size_t)s * L.stage_bytes +
-                               ((size_t)(j % spp) * L.mpar + m_slot) * L.strip + (size_t)sb * kBlkBytes;
+                               ((size_t)jj * L.mpar + m_slot) * L.strip + (size_t)sb * kBlkBytes;
           switch (T) {
             case 1: up_superblock<1>(blk, bf, xg, sb, ng, ngrp, vacc); break;
             case 2: up_superblock<2>(blk, bf, xg, sb, ng, ngrp, vacc); break;
@@ -414,7 +428,7 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
             default: up_superblock<8>(blk, bf, xg, sb, ng, ngrp, vacc); break;
           }
         }
-        vpart[((j & 1) * nwc + warp) * 32 + lane] =
+        vpart[((jpar & 1) * nwc + warp) * 32 + lane] =
             make_float4(vacc[0][0], vacc[0][1], vacc[1][0], vacc[1][1]);
         __syncwarp();
         if (last && lane == 0) mbar_arrive(&empty[s]);
@@ -426,31 +440,40 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
         }
         break;
       }
-      if (threadIdx.x == 0 && last) s_consumed = st + 1;
+      if (threadIdx.x == 0 && last) s_consumed = st + 1;  // stages 0..st are free
       if (fin) {
         // sum the superblock partials of every M-tile of step j; threshold and compaction
         for (int m = 0; m < L.mpar; ++m) {
           if (us + m >= ue) break;
           float v[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
           for (int q = 0; q < nsb; ++q) {
-            const float4 pv = vpart[((j & 1) * nwc + m * nsb + q) * 32 + lane];
+            const float4 pv = vpart[((jpar & 1) * nwc + m * nsb + q) * 32 + lane];
             v[0][0] += pv.x;
             v[0][1] += pv.y;
             v[1][0] += pv.z;
             v[1][1] += pv.w;
           }
           const long long u = us + m;
-          const int mt = (int)(u - (long long)g * MT);
+          const int mt = (int)(u - g_lo);
           float* vb = vbuf + m * 16 * kMaxTok;
           switch (T) {
-            case 1: up_finalize<1>(p, s_gd, u, mt, thr, v, vb); break;
-            case 2: up_finalize<2>(p, s_gd, u, mt, thr, v, vb); break;
-            case 4: up_finalize<4>(p, s_gd, u, mt, thr, v, vb); break;
-            default: up_finalize<8>(p, s_gd, u, mt, thr, v, vb); break;
+            case 1: up_finalize<1>(p, s_gd, g, u, mt, thr, v, vb); break;
+            case 2: up_finalize<2>(p, s_gd, g, u, mt, thr, v, vb); break;
+            case 4: up_finalize<4>(p, s_gd, g, u, mt, thr, v, vb); break;
+            default: up_finalize<8>(p, s_gd, g, u, mt, thr, v, vb); break;
           }
         }
       }
       us = ue;
+      ++jpar;
+      if (++jj == spp || ue >= u1) {
+        jj = 0;
+        ++st;
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
     }
   }
   __syncthreads();
@@ -462,9 +485,10 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
 size_t up_smem_bytes(int d, int max_tok) { return up_layout(d, max_tok).total; }
 int up_threads(int d) { return (up_layout(d, 1).nwc + 2) * 32; }
 
-// Register budget: 10 warps (d <= 4096) or up to 18 warps per CTA.
+// Register budget: 10 warps (d <= 4096), 14 warps (d <= 6144) or up to 18 warps per CTA.
 static const void* up_kernel_for(int d) {
-  return up_threads(d) <= 320 ? (const void*)up_kernel<320> : (const void*)up_kernel<576>;
+  const int t = up_threads(d);
+  return t <= 320 ? (const void*)up_kernel<320> : t <= 448 ? (const void*)up_kernel<448> : (const void*)up_kernel<576>;
 }
 
 int up_blocks_per_sm(int d, int max_tok) {
@@ -493,7 +517,9 @@ cudaError_t launch_up(const ExpertParams& p, int grid, cudaStream_t st, bool pdl
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (up_threads(p.d) <= 320) return cudaLaunchKernelEx(&cfg, up_kernel<320>, p);
+  const int t = up_threads(p.d);
+  if (t <= 320) return cudaLaunchKernelEx(&cfg, up_kernel<320>, p);
+  if (t <= 448) return cudaLaunchKernelEx(&cfg, up_kernel<448>, p);
   return cudaLaunchKernelEx(&cfg, up_kernel<576>, p);
 }
 
