@@ -5,6 +5,11 @@
 
 using namespace sesg;
 
+namespace sesg {
+size_t gather_ring_scratch_bytes(int d, int f);  // gather.cu
+int gather_round_stages(int d, int nt, int stages);  // gather.cu
+}
+
 namespace {
 
 constexpr size_t kWsAlign = 256;
@@ -136,10 +141,9 @@ moe_status_t plan(const DeviceInfo& di, const WsLayout& L, int d, int f, int max
   const size_t stage = (size_t)4 * d + 32 + 16;
   if (fixed + 2 * stage > (size_t)di.smem_optin) return MOE_ERR_UNSUPPORTED_SHAPE;
   int S = (int)((di.smem_optin - fixed) / stage);
-  S = S > 16 ? 16 : S;
+  S = gather_round_stages(d, pl.nt, S > 16 ? 16 : S);
   // the gather prologue borrows the stage buffers for the scan of one group's tile counts
-  const size_t scratch = sizeof(int) * ((size_t)f / kMTile + 2);
-  if ((size_t)S * (4 * d + 32) < scratch) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((size_t)S * (4 * d + 32) < gather_ring_scratch_bytes(d, f)) return MOE_ERR_UNSUPPORTED_SHAPE;
   pl.stages = S;
   return MOE_OK;
 }

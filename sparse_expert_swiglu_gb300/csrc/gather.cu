@@ -23,15 +23,25 @@ namespace sesg {
 constexpr int kChunk = 8;  // fp16 elements per 16-byte chunk
 
 struct GatherLayout {
-  size_t off_full, off_empty, off_stage, off_lslot, off_lcol, off_lgrp, off_red, off_hbuf, off_tmp,
-      off_goff, off_x, off_h16, total, stage_bytes;
+  size_t off_full, off_empty, off_stage, off_lslot, off_lcol, off_lgrp, off_red, off_hbuf, off_goff,
+      off_x, off_h16, total, stage_bytes;
 };
 
 // Tensor-core consumers (groups of up to 8 tokens, d <= 4096): the group's x in shared
-// memory, 8 rows of d + 8 halves (the padding spreads the rows over the banks).
+// memory, 4 or 8 rows (the group size bound) of d + 8 halves (the padding spreads the
+// rows over the banks).
 constexpr int kMmaTok = 8;
 constexpr int kMmaBatch = 4;  // kept rows per batch
 __host__ __device__ inline bool gather_mma(int d, int nt) { return d <= 4096 && nt >= 2; }
+__host__ __device__ inline int gather_mma_xrows(int nt) { return nt <= 4 ? 4 : 8; }
+
+// Scratch of the prologue inside the (then idle) stage ring: the tile counts of one
+// group [MT + 1] and the block scan's [threads + 1].
+__host__ __device__ inline size_t gather_scan_tmp_off(int MT) { return ((size_t)(MT + 1) * 4 + 15) & ~(size_t)15; }
+__host__ __device__ inline size_t gather_scan_bytes(int MT, int threads) {
+  return gather_scan_tmp_off(MT) + (size_t)(threads + 1) * 4;
+}
+
 
 constexpr int kGaBatchTok = 16;  // items per batch x tokens per group, at most
 
@@ -98,18 +108,16 @@ __host__ __device__ inline GatherLayout gather_layout(int d, int stages, int nt,
   o = (o + 15) & ~(size_t)15;
   L.off_hbuf = o;  // [2][items][tokens] h of a batch
   o += (size_t)2 * kGaBatchTok * 4;
-  L.off_tmp = o;  // block-scan scratch
-  o += (size_t)1040 * 4;
   L.off_goff = o;  // kept-item offsets of the groups [G_max + 1]
   o += ((size_t)g_max + 1) * 4;
   o = (o + 127) & ~(size_t)127;
   L.off_x = L.off_h16 = o;
   if (gather_mma(d, nt)) {
-    L.off_x = o;  // [8][d + 8] fp16
-    o += (size_t)kMmaTok * (d + 8) * 2;
+    L.off_x = o;  // [4 or 8][d + 8] fp16
+    o += (size_t)gather_mma_xrows(nt) * (d + 8) * 2;
     o = (o + 127) & ~(size_t)127;
-    L.off_h16 = o;  // [hi, lo][8 tokens][16 items] fp16
-    o += (size_t)2 * kMmaTok * 16 * 2;
+    L.off_h16 = o;  // [8 tokens][16 k] fp16: k = row (hi), 4 + row (lo), 8..15 zero
+    o += (size_t)kMmaTok * 16 * 2;
   }
   L.total = o;
   return L;
@@ -171,7 +179,6 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
   int* lgrp = reinterpret_cast<int*>(gsm + L.off_lgrp);
   float* red = reinterpret_cast<float*>(gsm + L.off_red);    // [2][kR][NT][ncw] partial dots
   float* hbuf = reinterpret_cast<float*>(gsm + L.off_hbuf);  // [2][kR][NT]
-  int* tmp = reinterpret_cast<int*>(gsm + L.off_tmp);
   __shared__ int s_abort, s_issued, s_consumed;
   __shared__ GroupDesc s_gd;
 
@@ -195,6 +202,7 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
   const int MT = p.f / kMTile;
   int* goff = reinterpret_cast<int*>(gsm + L.off_goff);  // [G+1]
   int* uoff = reinterpret_cast<int*>(stage);  // scratch in the idle stage ring: [MT+1]
+  int* tmp = reinterpret_cast<int*>(stage + gather_scan_tmp_off(MT));  // [threads + 1]
   for (int g = tid; g < G; g += blockDim.x) goff[g] = __ldcg(p.group_total + g);
   __syncthreads();
   block_exclusive_scan(goff, G, tmp);
@@ -209,9 +217,9 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
   float2 xf[MMA ? 1 : NT][kChunk / 2];
   float wt[MMA ? 1 : NT];
   if constexpr (MMA) {
-    // the h buffer's items 4..15 stay zero (a batch holds at most kMmaBatch items)
+    // the h buffer's k = 8..15 stay zero
     __half* h16 = reinterpret_cast<__half*>(gsm + L.off_h16);
-    for (int i = tid; i < 2 * kMmaTok * 16; i += blockDim.x) h16[i] = __float2half(0.f);
+    for (int i = tid; i < kMmaTok * 16; i += blockDim.x) h16[i] = __float2half(0.f);
     __syncthreads();
   }
 
@@ -297,10 +305,12 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
       //          as B (shared memory), 16 k-steps over the warp's slice;
       //   h      warp 0 adds the 16 warps' partial dots, h = SiLU(.) * v * w, split into
       //          fp16 hi + lo (hi + lo carries h to about 22 bits);
-      //   down   acc[col][token] += Down^T[col][row] . H[row][token]: ldmatrix.trans of
-      //          the down rows as A, hi and lo as B (two mma per 16 columns).
+      //   down   acc[col][token] += Down^T[col][k] . H[k][token] with k = 0..3 the batch's
+      //          rows times hi and k = 4..7 the same rows times lo: ldmatrix.trans of the
+      //          down rows as A (lanes 4..7 address rows 0..3 again), one mma per 16
+      //          columns.
       __half* xs = reinterpret_cast<__half*>(gsm + L.off_x);
-      __half* h16 = reinterpret_cast<__half*>(gsm + L.off_h16);
+      __half* h16 = reinterpret_cast<__half*>(gsm + L.off_h16);  // [8 tokens][16 k]
       float* redm = red;  // [ncw][4 rows][8 tokens]
       const int xstride = d + 8;
       const int gid = lane >> 2, c = lane & 3;
@@ -330,13 +340,15 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
         if (tid == 0) s_gd = p.groups[g];
         named_barrier(1, nct);
         const int ntok = s_gd.n_tok;
+        constexpr int XR = NT <= 4 ? 4 : 8;  // x rows held (the group size bound)
 #pragma unroll
-        for (int t = 0; t < kMmaTok; ++t) {
+        for (int t = 0; t < XR; ++t) {
           uint4 xv = make_uint4(0, 0, 0, 0);
           if (t < ntok) xv = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)s_gd.tok[t] * d) + tid);
           reinterpret_cast<uint4*>(xs + (size_t)t * xstride)[tid] = xv;
         }
         const float wtl = (lane & 7) < ntok ? s_gd.w[lane & 7] : 0.f;  // warp 0: token lane % 8
+
         float accm[16][4];
 #pragma unroll
         for (int j = 0; j < 16; ++j) accm[j][0] = accm[j][1] = accm[j][2] = accm[j][3] = 0.f;
@@ -363,23 +375,29 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
           // 0 (same address: no bank conflict; finite weights whose dot products are not
           // used and whose down contributions are multiplied by h = 0)
           const int sl = (lit < nb) ? (lit == 1 ? sq1 : lit == 2 ? sq2 : lit == 3 ? sq3 : sq0) : sq0;
-          const uint32_t sbase = smem_addr(stage + (size_t)sl * L.stage_bytes);
-          const uint32_t garow = sbase + (uint32_t)(kw + lhalf * 8) * 2u;
-          const uint32_t darow = sbase + (uint32_t)(2 * d) + (uint32_t)(kw + lhalf * 8) * 2u;
+          const int ld = lit & 3;  // down operand: k = lit holds row lit % 4
+          const int sld = (ld < nb) ? (ld == 1 ? sq1 : ld == 2 ? sq2 : ld == 3 ? sq3 : sq0) : sq0;
+          const uint32_t garow = smem_addr(stage + (size_t)sl * L.stage_bytes) + (uint32_t)(kw + lhalf * 8) * 2u;
+          const uint32_t darow = smem_addr(stage + (size_t)sld * L.stage_bytes) + (uint32_t)(2 * d) +
+                                 (uint32_t)(kw + lhalf * 8) * 2u;
           // two accumulator chains (even and odd k-steps) halve the dependent mma latency
           float dd[4] = {0.f, 0.f, 0.f, 0.f}, de[4] = {0.f, 0.f, 0.f, 0.f};
           if (ok) {
-            const __half* xg = xs + (size_t)gid * xstride + kw + 2 * c;
+            // B column gid = token gid (zero beyond the x rows held)
+            const bool xon = gid < XR;
+            const __half* xg = xs + (size_t)(xon ? gid : 0) * xstride + kw + 2 * c;
+            auto xb = [&](int off) -> uint32_t {
+              if constexpr (XR == kMmaTok) return *reinterpret_cast<const uint32_t*>(xg + off);
+              return xon ? *reinterpret_cast<const uint32_t*>(xg + off) : 0u;
+            };
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
               uint32_t a[4], a2[4];
               ldsm_x2(garow + j * 32u, a[0], a[2]);
               ldsm_x2(garow + (j + 1) * 32u, a2[0], a2[2]);
               a[1] = a[3] = a2[1] = a2[3] = 0u;
-              mma_16816(dd, a, *reinterpret_cast<const uint32_t*>(xg + j * 16),
-                        *reinterpret_cast<const uint32_t*>(xg + j * 16 + 8));
-              mma_16816(de, a2, *reinterpret_cast<const uint32_t*>(xg + (j + 1) * 16),
-                        *reinterpret_cast<const uint32_t*>(xg + (j + 1) * 16 + 8));
+              mma_16816(dd, a, xb(j * 16), xb(j * 16 + 8));
+              mma_16816(de, a2, xb((j + 1) * 16), xb((j + 1) * 16 + 8));
             }
             dd[0] += de[0];
             dd[1] += de[1];
@@ -414,20 +432,18 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
             }
             const __half hi = __float2half_rn(hq);
             const __half lo = __float2half_rn(hq - __half2float(hi));
-            h16[(0 * kMmaTok + t) * 16 + it] = hi;
-            h16[(1 * kMmaTok + t) * 16 + it] = lo;
+            h16[t * 16 + it] = hi;
+            h16[t * 16 + kMmaBatch + it] = lo;
           }
           named_barrier(1, nct);
           {
-            const uint32_t bhi = *reinterpret_cast<const uint32_t*>(h16 + (0 * kMmaTok + gid) * 16 + 2 * c);
-            const uint32_t blo = *reinterpret_cast<const uint32_t*>(h16 + (1 * kMmaTok + gid) * 16 + 2 * c);
+            const uint32_t bh = *reinterpret_cast<const uint32_t*>(h16 + gid * 16 + 2 * c);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               uint32_t a[4];
               ldsm_x2_trans(darow + j * 32u, a[0], a[1]);
               a[2] = a[3] = 0u;
-              mma_16816(accm[j], a, bhi, 0u);
-              mma_16816(accm[j], a, blo, 0u);
+              mma_16816(accm[j], a, bh, 0u);
             }
           }
           // the batch's stages are free once every warp has read them
@@ -651,6 +667,16 @@ size_t gather_smem_bytes(int d, int stages, int nt, int list_cap, int g_max) {
   return gather_layout(d, stages, nt, list_cap, g_max).total;
 }
 
+// Ring depth for the tensor-core consumers: a multiple of 4 stages.  Stage k starts at
+// 32 k bytes modulo 128, so the 4 rows of any batch then sit in distinct bank quarters
+// for ldmatrix, also across the ring's wrap.
+int gather_round_stages(int d, int nt, int stages) {
+  return gather_mma(d, nt) && stages >= 8 ? stages & ~3 : stages;
+}
+
+// Bytes of the stage ring that the prologue borrows (checked against the ring size).
+size_t gather_ring_scratch_bytes(int d, int f) { return gather_scan_bytes(f / kMTile, (d / 256 + 1) * 32); }
+
 cudaError_t launch_gather(const ExpertParams& p, int nt, cudaStream_t st, bool pdl) {
   const int ncw = p.d / 256;
   const size_t smem = gather_smem_bytes(p.d, p.stages, nt, p.list_cap, p.G_max);
@@ -673,7 +699,10 @@ cudaError_t launch_gather(const ExpertParams& p, int nt, cudaStream_t st, bool p
   return cudaLaunchKernelEx(&cfg, gather_kernel<NTV, MT, MM>, p);
   // register caps: 96 per thread up to 640 threads (d <= 4096), 64 above
   const bool small = (ncw + 1) * 32 <= 640;
-  if (gather_mma(p.d, nt)) { SESG_G(8, 640, true) }
+  if (gather_mma(p.d, nt)) {
+    if (nt <= 4) { SESG_G(4, 640, true) }
+    SESG_G(8, 640, true)
+  }
   if (nt == 1) { if (small) { SESG_G(1, 640, false) } SESG_G(1, 1024, false) }
   if (nt == 2) { if (small) { SESG_G(2, 640, false) } SESG_G(2, 1024, false) }
   if (nt == 4 && small) { SESG_G(4, 640, false) }

@@ -317,8 +317,14 @@ def test_layer_mixtral_8x7b_batch8():
     run_layer_case(4096, 14336, 8, 2, 8, 0, [70], seed=5, gen_device="cuda")
 
 
+def test_layer_mixtral_8x7b_batch3():
+    """Three tokens: groups of at most 3 tokens on the tensor-core gather with the
+    4-row x buffer, 16 consumer warps."""
+    run_layer_case(4096, 14336, 8, 2, 3, 0, [70], seed=7, gen_device="cuda")
+
+
 def test_layer_mixtral_8x22b_shape_b2():
-    """d=6144, f=16384 (groups capped at 4 tokens for this d), RMSNorm output."""
+    """d=6144, f=16384, two tokens (the decode path), RMSNorm output."""
     run_layer_case(6144, 16384, 8, 2, 2, 0, [70], seed=6, gen_device="cuda", rmsnorm=True)
 
 
