@@ -46,6 +46,11 @@ WORKLOADS = {
                              sparsities=(0, 50, 90), calib_tokens=1024, copies=8, chained=False),
     "mixtral-8x22b-stack": dict(d=6144, f=16384, E=8, k=2, shared=0, tokens=(1, 8), sparsities=(70,),
                                 calib_tokens=256, copies=56, chained=True),
+    # FloE's on-the-fly setting: gate/down rows in page-locked host memory, only the kept
+    # rows fetched over the host link
+    "mixtral-8x7b-host-rows": dict(d=4096, f=14336, E=8, k=2, shared=0, tokens=(1, 2),
+                                   sparsities=(0, 50, 70, 90), calib_tokens=1024, copies=2, chained=False,
+                                   host_rows=True),
 }
 HEADLINE_PCT = 70
 N_LAYER_COPIES = 8
@@ -335,6 +340,22 @@ def time_steps(graphs, stream, steps, warmup, world, dev, stack=None):
     return start.elapsed_time(end) / 1e3  # seconds
 
 
+def step_distribution(stack, stream, R, replays):
+    """Spread of the step time: an event after every replay of the stacked graph (R layer
+    steps each), each replay's time / R, as p10 / median / p90 in microseconds."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(replays):
+            stack.replay()
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per_step = np.array([evs[i].elapsed_time(evs[i + 1]) * 1e3 / R for i in range(replays)])
+    return {"p10": float(np.percentile(per_step, 10)), "p50": float(np.median(per_step)),
+            "p90": float(np.percentile(per_step, 90)), "replays": replays, "steps_per_replay": R,
+            "how": "event after every replay of the stacked graph; replay time / steps per replay"}
+
+
 def per_kernel_times(prof_graphs, events_list, stream, steps, path):
     """Average device time of each kernel, from events recorded around it inside the
     graphs (replayed R at a time, read back before the events are re-recorded).  On the
@@ -521,6 +542,7 @@ def run_ours(args, world, rank, local):
     value = pairs / secs
     ms_per_step = secs / args.steps * 1e3
     mean_bytes = float(np.mean([b["total"] for b in byts]))
+    dist = step_distribution(stack, stream, R, max(20, args.steps // R))
 
     # per-kernel device times (events around each kernel inside graphs)
     events_list = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(R)]
@@ -616,6 +638,7 @@ def run_ours(args, world, rank, local):
                              "layers runs (PDL between all kernels); each copy keeps its own token"},
         "layer_us": ms_per_step * 1e3,
         "layer_us_one_graph_per_layer": secs_single / args.steps * 1e6,
+        "layer_us_distribution": dist,
         "layer_roofline": {"bytes_per_step": mean_bytes, "hbm_gbs": mean_bytes / (ms_per_step * 1e-3) / 1e9,
                            "peak": peak, "frac": mean_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
                            "peak_kind": peak_kind},
@@ -678,6 +701,28 @@ def run_workload(args, world, rank, local):
         torch.cuda.empty_cache()
         layers.append(ses.Layer(synth.router(d, E, 200 + r, device=dev, layer=r), ex, k, True, sh))
         tables.append((thresholds(ex, E), thresholds(sh, ns) if ns else None))
+    host_rows = bool(W.get("host_rows"))
+    h2d_gbs = None
+    if host_rows:
+        layers = [ses.Layer(l.w_router, l.routed.to_host_rows(), k, True,
+                            l.shared.to_host_rows() if l.shared else None) for l in layers]
+        torch.cuda.empty_cache()
+        # the host link's copy-engine rate: 1 GiB from page-locked host memory, best of 3
+        src = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+        dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+        best = math.inf
+        for _ in range(3):
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record()
+            dst.copy_(src, non_blocking=True)
+            a1.record()
+            torch.cuda.synchronize()
+            best = min(best, a0.elapsed_time(a1) / 1e3)
+        h2d_gbs = (1 << 30) / best / 1e9
+        del src, dst
+        torch.cuda.empty_cache()
+    decode = ses.layer_decode_host_rows if host_rows else ses.layer_decode
+    ws_bytes = ses.layer_host_rows_workspace_bytes if host_rows else ses.layer_workspace_bytes
     up_bytes = ses.packed_bytes(d, f)
     weights_gb = sum(l.routed.gate_t.numel() * 4 + l.routed.up_packed.numel() +
                      (l.shared.gate_t.numel() * 4 + l.shared.up_packed.numel() if l.shared else 0)
@@ -688,17 +733,17 @@ def run_workload(args, world, rank, local):
         ys = [torch.empty_like(x) for x in xs]
         if W["chained"]:
             xs = [xs[0]] + ys[:-1]
-        wss = [ses.Workspace(ses.layer_workspace_bytes(layers[r], B), dev) for r in range(R)]
-        path = ses.layer_path(layers[0], B)
+        wss = [ses.Workspace(ws_bytes(layers[r], B), dev) for r in range(R)]
+        path = "decode (host rows)" if host_rows else ses.layer_path(layers[0], B)
         with torch.cuda.stream(stream):
             for r in range(R):
-                ses.layer_decode(xs[r], layers[r], rmsnorm=True, ws=wss[r], out=ys[r])
+                decode(xs[r], layers[r], rmsnorm=True, ws=wss[r], out=ys[r])
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
-        c_layers = [l.c_struct() for l in layers]
+        c_layers = [l.c_struct(host_rows=host_rows) for l in layers]
         with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
             for r in range(R):
-                ses.layer_decode(xs[r], layers[r], rmsnorm=True, ws=wss[r], out=ys[r], c_layer=c_layers[r])
+                decode(xs[r], layers[r], rmsnorm=True, ws=wss[r], out=ys[r], c_layer=c_layers[r])
         torch.cuda.synchronize()
         for pct in W["sparsities"]:
             for r, layer in enumerate(layers):
@@ -708,7 +753,7 @@ def run_workload(args, world, rank, local):
             # realised bytes, layer by layer along the same inputs
             total, kept, cols = 0.0, 0, 0
             for r, layer in enumerate(layers):
-                _, dbg = ses.layer_decode(xs[r], layer, rmsnorm=True, ws=wss[r], out=ys[r], debug=True)
+                _, dbg = decode(xs[r], layer, rmsnorm=True, ws=wss[r], out=ys[r], debug=True)
                 idx = dbg["topk_idx"].cpu().numpy()
                 words = dbg["mask"].cpu().numpy().astype(np.uint32)
                 bits = ((words[..., None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(B, k + ns, -1)[..., :f]
@@ -746,8 +791,8 @@ def run_workload(args, world, rank, local):
             torch.cuda.synchronize()
             ge = torch.cuda.CUDAGraph()
             with torch.cuda.graph(ge, stream=stream, capture_error_mode="thread_local"):
-                ses.layer_decode(xs[0], layers[0], rmsnorm=True, ws=wss[0], out=ys[0], c_layer=c_layers[0],
-                                 events=evs)
+                decode(xs[0], layers[0], rmsnorm=True, ws=wss[0], out=ys[0], c_layer=c_layers[0],
+                       events=evs)
             kacc = np.zeros(4)
             for it in range(12):
                 with torch.cuda.stream(stream):
@@ -756,12 +801,20 @@ def run_workload(args, world, rank, local):
                 if it >= 2:
                     kacc += [evs[j].elapsed_time(evs[j + 1]) * 1e3 for j in range(4)]
             del ge
-            names = (["event_pair_us", "decode_up_kernel", "decode_gather_kernel", "event_pair_us_2"]
+            names = (["event_pair_us", "decode_up_kernel", "decode_fetch_and_gather_kernels", "event_pair_us_2"]
+                     if host_rows else
+                     ["event_pair_us", "decode_up_kernel", "decode_gather_kernel", "event_pair_us_2"]
                      if path == "decode" else ["route_kernel", "up_kernel", "gather_kernel", "combine_kernel"])
             kt = {nm: float(v) / 10 for nm, v in zip(names, kacc)}
+            extra = {}
+            if host_rows:
+                link = 4 * d * kept / R  # kept rows over the host link per step
+                extra = {"link_bytes_per_step": link, "link_gbs": link / (us * 1e-6) / 1e9,
+                         "h2d_copy_gbs": h2d_gbs, "frac_of_h2d_copy": link / (us * 1e-6) / 1e9 / h2d_gbs,
+                         "h2d_copy_how": "1 GiB page-locked host -> device copy in this run, best of 3"}
             if rank == 0:
                 print(json.dumps({
-                    "workload": args.workload, "tokens": B, "sparsity_pct": pct, "path": path,
+                    "workload": args.workload, "tokens": B, "sparsity_pct": pct, "path": path, **extra,
                     "layer_us": us, "expert_tokens_per_s": world * B * k * steps / secs,
                     "bytes_per_step": mean_bytes, "hbm_gbs": mean_bytes / (us * 1e-6) / 1e9,
                     "frac_of_measured_hbm": mean_bytes / (us * 1e-6) / 1e9 / peak, "peak_kind": peak_kind,

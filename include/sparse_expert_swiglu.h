@@ -222,6 +222,30 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
  */
 int32_t moe_layer_path(const moe_layer_t* layer, int32_t B);
 
+/*
+ * moe_layer_decode_host_rows -- moe_layer_decode with the experts' gate and down rows
+ * in page-locked host memory: FloE's on-the-fly setting ("FloE: On-the-Fly MoE
+ * Inference on Memory-constrained GPU", sec. 三 "系统协同优化"), where only the compressed
+ * up projection stays in GPU memory and only the rows that the masks keep are brought
+ * over.  Same arguments and result as moe_layer_decode, except:
+ *   layer: the router weight, up_packed and thr of both expert sets are device
+ *     pointers; gate_t and down (routed and shared) are host pointers to memory from
+ *     cudaHostAlloc / cudaMallocHost or registered with cudaHostRegister (device
+ *     pointers are accepted too); any other memory returns MOE_ERR_INVALID_ARG.
+ *   ws / ws_bytes: at least moe_layer_host_rows_workspace_bytes(layer, B) bytes: the
+ *     workspace of moe_layer_decode followed by a staging area for the kept rows (4d
+ *     bytes per row, room for at least (B k + shared E) f rows: the dense worst case).
+ * Only the decode path is supported (moe_layer_path(layer, B) == 1); other shapes
+ * return MOE_ERR_UNSUPPORTED_SHAPE.  Three kernels run: the up-projection kernel, a
+ * fetch kernel that copies each kept row (4d bytes) from host memory into the staging
+ * area, and the gather kernel, which streams the staging area.  dbg->events[2] marks
+ * the start of the fetch kernel.  The host rows must not change while the call runs.
+ */
+size_t moe_layer_host_rows_workspace_bytes(const moe_layer_t* layer, int32_t B);
+moe_status_t moe_layer_decode_host_rows(const uint16_t* x, int32_t B, const moe_layer_t* layer,
+                                        uint16_t* y, int32_t rmsnorm_out, const moe_debug_t* dbg,
+                                        void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------- workspace and status ---------------- */
 
 /* Zero-fills `ws` on `stream` (required once after allocating a workspace). */

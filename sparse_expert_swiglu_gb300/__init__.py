@@ -14,6 +14,8 @@ from ._lib import (  # noqa: F401
     expert_sparse_swiglu,
     expert_workspace_bytes,
     layer_decode,
+    layer_decode_host_rows,
+    layer_host_rows_workspace_bytes,
     layer_path,
     layer_workspace_bytes,
     lib,

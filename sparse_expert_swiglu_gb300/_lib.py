@@ -76,6 +76,10 @@ _SIGS = {
                                         ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(_Debug),
                                         ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_layer_path": (ctypes.c_int32, [ctypes.POINTER(_Layer), ctypes.c_int32]),
+    "moe_layer_host_rows_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(_Layer), ctypes.c_int32]),
+    "moe_layer_decode_host_rows": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(_Layer),
+                                                  ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(_Debug),
+                                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_workspace_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_get_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -116,9 +120,11 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _need(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor")
+def _need(t: torch.Tensor, dtype, name: str, host_ok: bool = False) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise TypeError(f"{name} must be a CUDA tensor" + (" or page-locked host tensor" if host_ok else ""))
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -209,18 +215,35 @@ class Experts:
                 and self.gate_t.stride(1) == 2 * self.d
                 and self.down.data_ptr() == self.gate_t.data_ptr() + 2 * self.d)
 
-    def c_struct(self) -> _Experts:
+    @property
+    def rows_on_host(self) -> bool:
+        """gate_t and down live in page-locked host memory (see to_host_rows)."""
+        return not self.gate_t.is_cuda
+
+    def c_struct(self, host_rows: bool = False) -> _Experts:
+        """The C description; host_rows=True admits gate_t/down in page-locked host memory
+        (only moe_layer_decode_host_rows reads such rows)."""
         _need(self.up_packed, torch.uint8, "up_packed")
         _need(self.thr, torch.float32, "thr")
         if self.interleaved:
             both = self.gate_t.as_strided((self.E, self.f, 2, self.d),
                                           (self.f * 2 * self.d, 2 * self.d, self.d, 1))
-            _need(both, torch.float16, "gate_t/down (interleaved)")
+            _need(both, torch.float16, "gate_t/down (interleaved)", host_rows)
         else:
-            _need(self.gate_t, torch.float16, "gate_t")
-            _need(self.down, torch.float16, "down")
+            _need(self.gate_t, torch.float16, "gate_t", host_rows)
+            _need(self.down, torch.float16, "down", host_rows)
         return _Experts(self.E, self.d, self.f, self.up_packed.data_ptr(), self.gate_t.data_ptr(),
                         self.down.data_ptr(), self.thr.data_ptr())
+
+    def to_host_rows(self) -> "Experts":
+        """A copy whose gate and down rows live in page-locked host memory (interleaving
+        kept); the packed up projection and the thresholds stay where they are."""
+        if self.interleaved:
+            both = self.gate_t.as_strided((self.E, self.f, 2, self.d),
+                                          (self.f * 2 * self.d, 2 * self.d, self.d, 1))
+            h = both.cpu().pin_memory()
+            return Experts(self.up_packed, h[:, :, 0, :], h[:, :, 1, :], self.thr)
+        return Experts(self.up_packed, self.gate_t.cpu().pin_memory(), self.down.cpu().pin_memory(), self.thr)
 
     @staticmethod
     def from_dense(w_up: torch.Tensor, gate_t: torch.Tensor, down: torch.Tensor,
@@ -252,10 +275,10 @@ class Layer:
     renorm: bool = True
     shared: Optional[Experts] = None
 
-    def c_struct(self) -> _Layer:
+    def c_struct(self, host_rows: bool = False) -> _Layer:
         _need(self.w_router, torch.float16, "w_router")
-        r = self.routed.c_struct()
-        s = self.shared.c_struct() if self.shared is not None else _empty_experts(r.d, r.f)
+        r = self.routed.c_struct(host_rows)
+        s = self.shared.c_struct(host_rows) if self.shared is not None else _empty_experts(r.d, r.f)
         return _Layer(self.k, 1 if self.renorm else 0, self.w_router.data_ptr(), r, s)
 
     @property
@@ -377,6 +400,8 @@ def layer_decode(x: torch.Tensor, layer: Layer, rmsnorm: bool = False,
                  out: Optional[torch.Tensor] = None, c_layer: Optional[_Layer] = None,
                  events=None):
     """One MoE decode layer on x fp16 [B, d] -> y fp16 [B, d] (and the debug dict)."""
+    if layer.routed.rows_on_host or (layer.shared is not None and layer.shared.rows_on_host):
+        raise ValueError("gate/down rows in host memory: use layer_decode_host_rows")
     _need(x, torch.float16, "x")
     B, d = x.shape
     c = c_layer if c_layer is not None else layer.c_struct()
@@ -391,4 +416,32 @@ def layer_decode(x: torch.Tensor, layer: Layer, rmsnorm: bool = False,
            lib().moe_layer_decode(_ptr(x), B, ctypes.byref(c), _ptr(y), 1 if rmsnorm else 0,
                                   ctypes.byref(dbg) if dbg is not None else None,
                                   ws.ptr(), ws.nbytes, _stream()))
+    return (y, dt) if debug else y
+
+
+def layer_host_rows_workspace_bytes(layer: Layer, B: int) -> int:
+    c = layer.c_struct(host_rows=True)
+    return int(lib().moe_layer_host_rows_workspace_bytes(ctypes.byref(c), B))
+
+
+def layer_decode_host_rows(x: torch.Tensor, layer: Layer, rmsnorm: bool = False,
+                           ws: Optional[Workspace] = None, debug: bool = False,
+                           out: Optional[torch.Tensor] = None, c_layer: Optional[_Layer] = None,
+                           events=None):
+    """layer_decode with the experts' gate/down rows in page-locked host memory
+    (Experts.to_host_rows): only the kept rows cross to the GPU.  One or two tokens."""
+    _need(x, torch.float16, "x")
+    B, d = x.shape
+    c = c_layer if c_layer is not None else layer.c_struct(host_rows=True)
+    if ws is None:
+        ws = Workspace(int(lib().moe_layer_host_rows_workspace_bytes(ctypes.byref(c), B)), x.device)
+    y = out if out is not None else torch.empty_like(x)
+    dbg, dt = (None, None)
+    if debug:
+        dbg, dt = _debug(B, layer.n_slots, layer.routed.f, layer.k, x.device, True)
+    dbg = _with_events(dbg, events)
+    _check("moe_layer_decode_host_rows",
+           lib().moe_layer_decode_host_rows(_ptr(x), B, ctypes.byref(c), _ptr(y), 1 if rmsnorm else 0,
+                                            ctypes.byref(dbg) if dbg is not None else None,
+                                            ws.ptr(), ws.nbytes, _stream()))
     return (y, dt) if debug else y

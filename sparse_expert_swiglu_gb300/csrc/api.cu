@@ -357,6 +357,50 @@ int32_t moe_layer_path(const moe_layer_t* layer, int32_t B) {
   return B >= 1 && use_decode_path(layer, B, di, su, sr, cap, umax) ? 1 : 0;
 }
 
+// Kept-column entries each up CTA's list holds (16 per unit of its share).
+static int decode_kcap(const WsLayout& L, int f, int P) {
+  return (int)((((long long)L.G_max * (f / kMTile)) + P - 1) / P) * 16;
+}
+
+// Decode-path parameters of one layer call (workspace carving, plan, debug outputs).
+static void fill_decode_params(DecodeParams& dp, const uint16_t* x, int B, const moe_layer_t* layer,
+                               uint16_t* y, int rmsnorm_out, const moe_debug_t* dbg, void* ws,
+                               const WsLayout& L, int P, int su, int sr, int cap, int umax) {
+  const int k = layer->k;
+  dp = DecodeParams{};
+  dp.x = reinterpret_cast<const __half*>(x);
+  dp.w_router = reinterpret_cast<const __half*>(layer->w_router);
+  dp.B = B;
+  dp.d = layer->routed.d;
+  dp.f = layer->routed.f;
+  dp.k = k;
+  dp.renorm = layer->renorm ? 1 : 0;
+  dp.n_shared = layer->shared.E;
+  dp.routed = to_set(layer->routed);
+  if (layer->shared.E > 0) dp.shared = to_set(layer->shared);
+  dp.ctrl = at<Ctrl>(ws, L.ctrl);
+  dp.groups = at<GroupDesc>(ws, L.groups);
+  dp.gmax = L.G_max;
+  dp.umax = umax;
+  dp.klist = at<int4>(ws, L.klist);
+  dp.kcap = decode_kcap(L, layer->routed.f, P);
+  dp.cta_total = at<int>(ws, L.cta_total);
+  dp.yacc = at<float>(ws, L.yacc);
+  dp.P = P;
+  dp.list_cap = cap;
+  dp.topk_idx = at<int32_t>(ws, L.topk_idx);
+  dp.topk_w = at<float>(ws, L.topk_w);
+  dp.user_idx = dbg ? dbg->topk_idx : nullptr;
+  dp.user_w = dbg ? dbg->topk_w : nullptr;
+  dp.n_slots = k + layer->shared.E;
+  dp.dbg_v = dbg ? dbg->v : nullptr;
+  dp.dbg_mask = dbg ? dbg->mask : nullptr;
+  dp.su = su;
+  dp.sr = sr;
+  dp.y = reinterpret_cast<__half*>(y);
+  dp.rmsnorm = rmsnorm_out ? 1 : 0;
+}
+
 moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* layer, uint16_t* y,
                               int32_t rmsnorm_out, const moe_debug_t* dbg, void* ws,
                               size_t ws_bytes, void* stream) {
@@ -376,38 +420,8 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
   int su = 0, sr = 0, cap = 0, umax = 0;
   if (use_decode_path(layer, B, di, su, sr, cap, umax)) {
     // one or two tokens: up kernel, gather kernel
-    DecodeParams dp = {};
-    dp.x = reinterpret_cast<const __half*>(x);
-    dp.w_router = reinterpret_cast<const __half*>(layer->w_router);
-    dp.B = B;
-    dp.d = layer->routed.d;
-    dp.f = layer->routed.f;
-    dp.k = k;
-    dp.renorm = layer->renorm ? 1 : 0;
-    dp.n_shared = layer->shared.E;
-    dp.routed = to_set(layer->routed);
-    if (layer->shared.E > 0) dp.shared = to_set(layer->shared);
-    dp.ctrl = at<Ctrl>(ws, L.ctrl);
-    dp.groups = at<GroupDesc>(ws, L.groups);
-    dp.gmax = L.G_max;
-    dp.umax = umax;
-    dp.klist = at<int4>(ws, L.klist);
-    dp.kcap = (int)((((long long)L.G_max * (layer->routed.f / kMTile)) + P - 1) / P) * 16;
-    dp.cta_total = at<int>(ws, L.cta_total);
-    dp.yacc = at<float>(ws, L.yacc);
-    dp.P = P;
-    dp.list_cap = cap;
-    dp.topk_idx = at<int32_t>(ws, L.topk_idx);
-    dp.topk_w = at<float>(ws, L.topk_w);
-    dp.user_idx = dbg ? dbg->topk_idx : nullptr;
-    dp.user_w = dbg ? dbg->topk_w : nullptr;
-    dp.n_slots = k + layer->shared.E;
-    dp.dbg_v = dbg ? dbg->v : nullptr;
-    dp.dbg_mask = dbg ? dbg->mask : nullptr;
-    dp.su = su;
-    dp.sr = sr;
-    dp.y = reinterpret_cast<__half*>(y);
-    dp.rmsnorm = rmsnorm_out ? 1 : 0;
+    DecodeParams dp;
+    fill_decode_params(dp, x, B, layer, y, rmsnorm_out, dbg, ws, L, P, su, sr, cap, umax);
     // the router runs inside the up kernel and the combination inside the gather kernel:
     // events 0 and 1, and 3 and 4, mark the same points
     cudaError_t e = record(dbg, 0, st);
@@ -444,6 +458,74 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
   if (launch_route(rp, st, true) != cudaSuccess) return MOE_ERR_CUDA;
   return run_experts(x, B, &layer->routed, &layer->shared, k + layer->shared.E, y,
                      rmsnorm_out ? 1 : 0, dbg, ws, L, di, B < rp.gcap ? B : rp.gcap, st);
+}
+
+// Staging area of a host-rows call: one 4d-byte row for every entry the up CTAs' lists
+// can hold (at least every column of every (token, expert) pair: the dense worst case).
+static size_t host_rows_staging_bytes(const moe_layer_t* layer, const WsLayout& L, int P) {
+  return (size_t)P * decode_kcap(L, layer->routed.f, P) * 4 * layer->routed.d;
+}
+
+size_t moe_layer_host_rows_workspace_bytes(const moe_layer_t* layer, int32_t B) {
+  if (check_layer(layer, B) != MOE_OK) return 0;
+  DeviceInfo di;
+  if (device_info(di) != cudaSuccess) return 0;
+  const WsLayout L = layer_layout(layer, B, di.sms);
+  return align_up(L.total, kWsAlign) + host_rows_staging_bytes(layer, L, di.sms);
+}
+
+// The device's address of a buffer in page-locked host memory (or in device memory).
+static moe_status_t device_view(const __half* p, const __half*& out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (a.type == cudaMemoryTypeUnregistered || a.devicePointer == nullptr) return MOE_ERR_INVALID_ARG;
+  out = reinterpret_cast<const __half*>(a.devicePointer);
+  return MOE_OK;
+}
+
+static moe_status_t device_view_rows(ExpertSet& es) {
+  moe_status_t s = device_view(es.gate_t, es.gate_t);
+  if (s == MOE_OK) s = device_view(es.down, es.down);
+  return s;
+}
+
+moe_status_t moe_layer_decode_host_rows(const uint16_t* x, int32_t B, const moe_layer_t* layer,
+                                        uint16_t* y, int32_t rmsnorm_out, const moe_debug_t* dbg,
+                                        void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = check_layer(layer, B);
+  if (s != MOE_OK) return s;
+  if (B == 0) return MOE_OK;
+  if (!x || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_ALIGNMENT;
+  if (!aligned(ws, kWsAlign)) return MOE_ERR_ALIGNMENT;
+  DeviceInfo di;
+  if (device_info(di) != cudaSuccess) return MOE_ERR_CUDA;
+  const WsLayout L = layer_layout(layer, B, di.sms);
+  const size_t off_staging = align_up(L.total, kWsAlign);
+  if (ws_bytes < off_staging + host_rows_staging_bytes(layer, L, di.sms)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int P = di.sms;
+  int su = 0, sr = 0, cap = 0, umax = 0;
+  if (!use_decode_path(layer, B, di, su, sr, cap, umax)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  DecodeParams dp;
+  fill_decode_params(dp, x, B, layer, y, rmsnorm_out, dbg, ws, L, P, su, sr, cap, umax);
+  s = device_view_rows(dp.routed);
+  if (s == MOE_OK && layer->shared.E > 0) s = device_view_rows(dp.shared);
+  if (s != MOE_OK) return s;
+  dp.staging = at<uint8_t>(ws, off_staging);
+  cudaStream_t st = (cudaStream_t)stream;
+  // up kernel, fetch kernel, gather kernel; event 2 marks the start of the fetch
+  cudaError_t e = record(dbg, 0, st);
+  if (e == cudaSuccess) e = record(dbg, 1, st);
+  if (e == cudaSuccess) e = launch_decode_up(dp, st, true);
+  if (e == cudaSuccess) e = record(dbg, 2, st);
+  if (e == cudaSuccess) e = launch_decode_fetch(dp, st, true);
+  if (e == cudaSuccess) e = launch_decode_gather(dp, st, true);
+  if (e == cudaSuccess) e = record(dbg, 3, st);
+  if (e == cudaSuccess) e = record(dbg, 4, st);
+  return cuda_status(e);
 }
 
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {

@@ -953,17 +953,22 @@ __global__ void __launch_bounds__(MAXT, 1) decode_gather_kernel(DecodeParams p) 
           break;
         }
         if (vload(&m->abort)) break;
-        const GaRow gr = list[i];
-        int el;
-        const ExpertSet& es = dec_set(p, grp[gr.g].expert, el);
-        const size_t roff = ((size_t)el * es.f + gr.col) * es.rs;
         uint8_t* st = ring + (size_t)s * L.row;
         mbar_arrive_expect_tx(&full[s], (uint32_t)L.row);
-        if (es.rs == 2 * d) {
-          bulk_g2s(st, es.gate_t + roff, (uint32_t)(4 * d), &full[s], pol);
+        if (p.staging) {
+          // rows copied from host memory: row a + i of the staging area
+          bulk_g2s(st, p.staging + (size_t)(a + i) * (4 * d), (uint32_t)(4 * d), &full[s], pol);
         } else {
-          bulk_g2s(st, es.gate_t + roff, (uint32_t)(2 * d), &full[s], pol);
-          bulk_g2s(st + 2 * d, es.down + roff, (uint32_t)(2 * d), &full[s], pol);
+          const GaRow gr = list[i];
+          int el;
+          const ExpertSet& es = dec_set(p, grp[gr.g].expert, el);
+          const size_t roff = ((size_t)el * es.f + gr.col) * es.rs;
+          if (es.rs == 2 * d) {
+            bulk_g2s(st, es.gate_t + roff, (uint32_t)(4 * d), &full[s], pol);
+          } else {
+            bulk_g2s(st, es.gate_t + roff, (uint32_t)(2 * d), &full[s], pol);
+            bulk_g2s(st + 2 * d, es.down + roff, (uint32_t)(2 * d), &full[s], pol);
+          }
         }
         m->issued = i + 1;
         if (++s == SR) {

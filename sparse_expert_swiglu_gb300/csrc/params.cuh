@@ -80,6 +80,9 @@ struct DecodeParams {
   int su, sr;               // depths of the up-strip ring and of the row ring
   __half* y;                // [B][d]
   int rmsnorm;
+  uint8_t* staging;         // or NULL: the kept rows in global kept order, 4d bytes each (gate
+                            // row, down row), copied from host memory by the fetch kernel;
+                            // the gather kernel then streams these instead of the experts
 };
 
 __device__ __forceinline__ const ExpertSet& expert_set(const ExpertParams& p, int expert,
@@ -118,5 +121,7 @@ int decode_units_max(int B, int f, int k, int n_shared, int P);
 int decode_plan(int B, int d, int E, int umax, int list_cap, int P, int smem_optin, int& su, int& sr);
 cudaError_t launch_decode_up(const DecodeParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_decode_gather(const DecodeParams& p, cudaStream_t st, bool pdl);
+// fetch.cu
+cudaError_t launch_decode_fetch(const DecodeParams& p, cudaStream_t st, bool pdl);
 
 }  // namespace sesg

@@ -186,7 +186,7 @@ def test_expert_empty_batch():
 # ---------------------------------------------------------------------------
 
 def run_layer_case(d, f, E, k, B, shared, pcts, seed, ncal=64, renorm=True, rmsnorm=False,
-                   gen_device="cpu", interleave=False):
+                   gen_device="cpu", interleave=False, host_rows=False):
     dev = gen_device
     de = synth.experts(E, d, f, seed, device=dev)
     ds = synth.experts(shared, d, f, seed, device=dev, kind=1) if shared else None
@@ -214,8 +214,16 @@ def run_layer_case(d, f, E, k, B, shared, pcts, seed, ncal=64, renorm=True, rmsn
         sh_gpu = ses.Experts.from_dense(ds.w_up.to("cuda"), ds.gate_t.to("cuda"), ds.down.to("cuda"),
                                         torch.zeros(shared, dtype=torch.float32, device="cuda"),
                                         interleave=interleave)
-    layer = ses.Layer(wr.to("cuda"), ex_gpu, k, renorm, sh_gpu)
-    ws = ses.Workspace(ses.layer_workspace_bytes(layer, B))
+    if host_rows:
+        # gate/down rows in page-locked host memory; thresholds shared with ex_gpu/sh_gpu
+        layer = ses.Layer(wr.to("cuda"), ex_gpu.to_host_rows(), k, renorm,
+                          sh_gpu.to_host_rows() if shared else None)
+        ws = ses.Workspace(ses.layer_host_rows_workspace_bytes(layer, B))
+        decode = ses.layer_decode_host_rows
+    else:
+        layer = ses.Layer(wr.to("cuda"), ex_gpu, k, renorm, sh_gpu)
+        ws = ses.Workspace(ses.layer_workspace_bytes(layer, B))
+        decode = ses.layer_decode
     results = []
     for pct in pcts:
         thr_r = np.zeros(E, np.float32)
@@ -227,7 +235,7 @@ def run_layer_case(d, f, E, k, B, shared, pcts, seed, ncal=64, renorm=True, rmsn
         ex_gpu.thr.copy_(torch.from_numpy(thr_r))
         if shared:
             sh_gpu.thr.copy_(torch.from_numpy(thr_s))
-        y, dbg = ses.layer_decode(x.to("cuda"), layer, rmsnorm=rmsnorm, ws=ws, debug=True)
+        y, dbg = decode(x.to("cuda"), layer, rmsnorm=rmsnorm, ws=ws, debug=True)
         assert ws.status() == 0
         y = _np16(y)
         idx_gpu = _np16(dbg["topk_idx"])
@@ -412,6 +420,46 @@ def _same_up_to_sum_order(a, b):
         i = int(torch.argmax(diff - tol))
         print("worst", i, float(a32.view(-1)[i]), float(b32.view(-1)[i]), float(tol.view(-1)[i]))
     return ok
+
+
+@pytest.mark.parametrize("B", [1, 2])
+def test_decode_host_rows(B):
+    """FloE's on-the-fly setting: gate and down rows in page-locked host memory, only the
+    kept rows fetched (up kernel, fetch kernel, gather kernel); one shared expert,
+    interleaved rows for one token, separate buffers for two."""
+    run_layer_case(1024, 352, 8, 2, B, 1, [0, 70, 101], seed=80 + B, interleave=(B == 1), host_rows=True)
+
+
+def test_decode_host_rows_mixtral_8x7b():
+    """Host-resident rows at the Mixtral-8x7B layer size (d = 4096, f = 14336)."""
+    run_layer_case(4096, 14336, 8, 2, 1, 0, [70], seed=90, gen_device="cuda", interleave=True,
+                   host_rows=True)
+
+
+def test_decode_host_rows_match_device_rows():
+    """The host-rows call gives the device-rows result up to the order of the fp32
+    additions (DeepSeek-V2-Lite shape, two tokens, RMSNorm); layer_decode refuses host
+    rows, and shapes off the decode path are unsupported."""
+    d, f, E, k, ns = 2048, 1408, 64, 6, 2
+    de, ds = synth.experts(E, d, f, 95, device="cuda"), synth.experts(ns, d, f, 95, device="cuda", kind=1)
+    thr = lambda n: torch.full((n,), 0.02, dtype=torch.float32, device="cuda")  # noqa: E731
+    ex = ses.Experts.from_dense(de.w_up, de.gate_t, de.down, thr(E), interleave=True)
+    sh = ses.Experts.from_dense(ds.w_up, ds.gate_t, ds.down, thr(ns))
+    wr = synth.router(d, E, 95, device="cuda")
+    dev_layer = ses.Layer(wr, ex, k, True, sh)
+    host_layer = ses.Layer(wr, ex.to_host_rows(), k, True, sh.to_host_rows())
+    assert host_layer.routed.rows_on_host and host_layer.routed.interleaved
+    x = synth.tokens(2, d, 95, device="cuda")
+    y_dev = ses.layer_decode(x, dev_layer, rmsnorm=True)
+    ws = ses.Workspace(ses.layer_host_rows_workspace_bytes(host_layer, 2))
+    y_host = ses.layer_decode_host_rows(x, host_layer, rmsnorm=True, ws=ws)
+    assert ws.status() == 0
+    assert _same_up_to_sum_order(y_host, y_dev)
+    with pytest.raises(ValueError):
+        ses.layer_decode(x, host_layer)
+    x5 = synth.tokens(5, d, 96, device="cuda")
+    with pytest.raises(ses.MoeError):
+        ses.layer_decode_host_rows(x5, host_layer)
 
 
 def test_decode_repeated_calls_share_the_workspace():
