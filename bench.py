@@ -51,6 +51,9 @@ WORKLOADS = {
     "mixtral-8x7b-host-rows": dict(d=4096, f=14336, E=8, k=2, shared=0, tokens=(1, 2),
                                    sparsities=(0, 50, 70, 90), calib_tokens=1024, copies=2, chained=False,
                                    host_rows=True),
+    # MoE-Infinity's expert activation matrix collection and expert cache (host code):
+    # per-query time at 1K stored matrices of the Mixtral-8x7B shape (32 MoE layers x 8)
+    "eamc-lookup": dict(L=32, E=8, capacity=1000, host_only=True),
 }
 HEADLINE_PCT = 70
 N_LAYER_COPIES = 8
@@ -826,12 +829,71 @@ def run_workload(args, world, rank, local):
         torch.cuda.empty_cache()
 
 
+def run_eamc(args):
+    """Host timing of the EAM collection (match, PredictEAM, insert with replacement) and
+    of a full expert cache's miss (prediction + eviction) through the Python binding, on
+    seeded synthetic request matrices (each request skewed towards a few experts per
+    layer).  The binding's own cost per call is reported beside it."""
+    import sparse_expert_swiglu_gb300 as ses
+    W = WORKLOADS[args.workload]
+    L, E, cap = W["L"], W["E"], W["capacity"]
+    rng = np.random.default_rng(11)
+    groups = [rng.dirichlet(np.full(E, 0.3), size=L) for _ in range(16)]
+
+    def request(iters):
+        pref = groups[rng.integers(len(groups))]
+        m = np.zeros((L, E), np.int32)
+        for i in range(L):
+            m[i] += np.bincount(rng.choice(E, size=2 * iters, p=pref[i]), minlength=E).astype(np.int32)
+        return m
+
+    eamc = ses.EAMC(L, E, cap)
+    for _ in range(cap):
+        eamc.insert(request(64))
+    cur = request(16)
+    n = 2000
+
+    def per_call(fn):
+        fn()
+        t = time.perf_counter()
+        for _ in range(n):
+            fn()
+        return (time.perf_counter() - t) / n * 1e6
+
+    cache = ses.ExpertCache(L * 2, L, E)
+    for i in range(L):
+        for j in range(2):
+            cache.lookup(eamc, cur, i, j)
+    keys = [(i, j) for i in range(L) for j in range(2, E)]
+    it = iter(keys * (n // len(keys) + 2))
+    line = {
+        "workload": args.workload, "L": L, "E": E, "capacity": cap, "stored": len(eamc),
+        "match_us": per_call(lambda: eamc.match(cur, 1)),
+        "predict_us": per_call(lambda: eamc.predict(cur, L // 2, 1)),
+        "predict_4_matches_us": per_call(lambda: eamc.predict(cur, L // 2, 4)),
+        "insert_full_us": per_call(lambda: eamc.insert(cur)),
+        "cache_miss_evict_us": per_call(lambda: cache.lookup(eamc, cur, *next(it))),
+        "binding_call_floor_us": per_call(lambda: ses.lib().moe_eamc_size(eamc.ptr())),
+        "cores_used": 1, "cpu": platform_cpu(),
+        "context": "the pages quote 21 us per query at 1K matrices on their CPU (matrix size not given)",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def platform_cpu():
+    import platform
+    return f"{platform.machine()} x{os.cpu_count()}"
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":
             run_reference(args, world, rank, local)
+        elif args.workload and WORKLOADS[args.workload].get("host_only"):
+            if rank == 0:
+                run_eamc(args)
         elif args.workload:
             run_workload(args, world, rank, local)
         else:

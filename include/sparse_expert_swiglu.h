@@ -246,6 +246,73 @@ moe_status_t moe_layer_decode_host_rows(const uint16_t* x, int32_t B, const moe_
                                         uint16_t* y, int32_t rmsnorm_out, const moe_debug_t* dbg,
                                         void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------- expert activation tracking and expert cache (host) ----------------
+ *
+ * "MoE-Infinity" (sec. 4.3, 4.5, 4.7 Algorithm 1 "专家缓存检索", appendix B.1): request-level
+ * expert activation matrices, their collection, the activation prediction from it and
+ * the sparsity-aware expert cache.  Host functions on caller-owned host memory (no GPU,
+ * no allocation, no internal locking: one thread per structure at a time).
+ *
+ * An EAM is int32 [L][E], row-major: cell [i][j] = tokens routed to expert j of MoE layer
+ * i.  One iteration's row i is the expert_count that moe_route_topk returns for layer i;
+ * a request's EAM is the sum over its iterations (moe_eam_add_counts).
+ */
+
+/* eam[layer][j] += counts[j] for j < E. */
+moe_status_t moe_eam_add_counts(int32_t* eam, int32_t L, int32_t E, int32_t layer, const int32_t* counts);
+
+/*
+ * EAMC: at most `capacity` past request EAMs.  moe_eamc_bytes sizes the caller's buffer
+ * (0 for invalid sizes); moe_eamc_init formats it (empty).  moe_eamc_insert appends
+ * `ream` while there is room, else overwrites the stored entry nearest to it (smallest
+ * cosine distance of the flattened matrices; ties: the lowest index); *slot (optional)
+ * receives the index written.  moe_eamc_size returns the entry count (negative status
+ * for an invalid buffer); moe_eamc_entry copies entry i out.
+ */
+size_t moe_eamc_bytes(int32_t L, int32_t E, int32_t capacity);
+moe_status_t moe_eamc_init(void* eamc, size_t bytes, int32_t L, int32_t E, int32_t capacity);
+moe_status_t moe_eamc_insert(void* eamc, const int32_t* ream, int32_t* slot);
+int32_t moe_eamc_size(const void* eamc);
+moe_status_t moe_eamc_entry(const void* eamc, int32_t i, int32_t* eam);
+
+/*
+ * moe_eamc_match -- the n_match stored entries nearest to `cur` (cosine distance
+ * 1 - a.b / (|a| |b|) in double, 1 when either matrix is all zero), by (distance,
+ * index) ascending: idx[n_match] and dist[n_match]; slots past the entry count get -1
+ * and +inf; *n_found (optional) = entries returned.
+ *
+ * moe_eamc_predict -- PredictEAM for current layer `layer` (0 <= layer < L): the nearest
+ * n_match entries (1 <= n_match <= 1024) summed cell by cell, each row normalised to sum
+ * 1 (rows summing to 0 stay 0), row i multiplied by 1 - (i - layer) / L.
+ * p_eam: double [L][E] out.  An empty EAMC predicts all zeros.
+ */
+moe_status_t moe_eamc_match(const void* eamc, const int32_t* cur, int32_t n_match, int32_t* idx,
+                            double* dist, int32_t* n_found);
+moe_status_t moe_eamc_predict(const void* eamc, const int32_t* cur, int32_t layer, int32_t n_match,
+                              double* p_eam);
+
+/*
+ * Expert cache (Algorithm 1): at most `capacity` experts, identified by (layer, expert),
+ * kept in insertion order.  moe_expert_cache_lookup requests expert `expert` of layer
+ * `layer`, the layer now running, with `cur` the current EAM:
+ *   hit            -> *hit = 1, nothing changes;
+ *   miss, room     -> *hit = 0, the expert is appended (the caller fetches it);
+ *   miss, full     -> *hit = 0; p = moe_eamc_predict(eamc, cur, layer, n_match); the cached
+ *                     expert e with the smallest (p[e.layer][e.expert] + eps) / n_token *
+ *                     (1 - e.layer / L), n_token = sum of row e.layer of p (1 where that
+ *                     row sums to 0), is removed (ties: the earliest inserted) and the
+ *                     requested expert appended.
+ * evicted[2] receives the removed (layer, expert), or (-1, -1).  The EAMC must have the
+ * cache's L and E.  moe_expert_cache_contents copies the (layer, expert) pairs in
+ * insertion order to layer_expert[2 * n] (optional) and sets *n.
+ */
+size_t moe_expert_cache_bytes(int32_t capacity);
+moe_status_t moe_expert_cache_init(void* cache, size_t bytes, int32_t capacity, int32_t L, int32_t E);
+moe_status_t moe_expert_cache_lookup(void* cache, const void* eamc, const int32_t* cur, int32_t layer,
+                                     int32_t expert, int32_t n_match, double eps, int32_t* hit,
+                                     int32_t* evicted);
+moe_status_t moe_expert_cache_contents(const void* cache, int32_t* layer_expert, int32_t* n);
+
 /* ---------------- workspace and status ---------------- */
 
 /* Zero-fills `ws` on `stream` (required once after allocating a workspace). */

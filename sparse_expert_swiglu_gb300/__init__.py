@@ -6,11 +6,14 @@ the seeded synthetic-input generator.
 """
 
 from ._lib import (  # noqa: F401
+    EAMC,
     EXPORTED,
+    ExpertCache,
     Experts,
     Layer,
     MoeError,
     Workspace,
+    eam_add_counts,
     expert_sparse_swiglu,
     expert_workspace_bytes,
     layer_decode,

@@ -12,6 +12,7 @@ import os
 from dataclasses import dataclass
 from typing import Optional
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -80,6 +81,25 @@ _SIGS = {
     "moe_layer_decode_host_rows": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(_Layer),
                                                   ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(_Debug),
                                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_eam_add_counts": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_void_p]),
+    "moe_eamc_bytes": (ctypes.c_size_t, [ctypes.c_int32] * 3),
+    "moe_eamc_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int32,
+                                     ctypes.c_int32]),
+    "moe_eamc_insert": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_eamc_size": (ctypes.c_int32, [ctypes.c_void_p]),
+    "moe_eamc_entry": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
+    "moe_eamc_match": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_eamc_predict": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_void_p]),
+    "moe_expert_cache_bytes": (ctypes.c_size_t, [ctypes.c_int32]),
+    "moe_expert_cache_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32]),
+    "moe_expert_cache_lookup": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_double, ctypes.c_void_p,
+                                               ctypes.c_void_p]),
+    "moe_expert_cache_contents": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "moe_workspace_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_get_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -445,3 +465,103 @@ def layer_decode_host_rows(x: torch.Tensor, layer: Layer, rmsnorm: bool = False,
                                             ctypes.byref(dbg) if dbg is not None else None,
                                             ws.ptr(), ws.nbytes, _stream()))
     return (y, dt) if debug else y
+
+
+# ---------------------------------------------------------------------------
+# expert activation tracking and the expert cache (host; numpy-backed buffers)
+# ---------------------------------------------------------------------------
+
+def _np_ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _i32(a, shape, name: str) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    if a.shape != shape:
+        raise ValueError(f"{name} must have shape {shape}, got {a.shape}")
+    return a
+
+
+def eam_add_counts(eam: np.ndarray, layer: int, counts) -> None:
+    """eam[layer] += counts (in place; eam int32 [L, E], C-contiguous)."""
+    if eam.dtype != np.int32 or not eam.flags.c_contiguous or eam.ndim != 2:
+        raise TypeError("eam must be a C-contiguous int32 [L, E] array")
+    L, E = eam.shape
+    c = _i32(counts, (E,), "counts")
+    _check("moe_eam_add_counts", lib().moe_eam_add_counts(_np_ptr(eam), L, E, layer, _np_ptr(c)))
+
+
+class EAMC:
+    """A fixed-capacity collection of request-level expert activation matrices (L x E)."""
+
+    def __init__(self, L: int, E: int, capacity: int):
+        self.L, self.E, self.capacity = L, E, capacity
+        n = int(lib().moe_eamc_bytes(L, E, capacity))
+        if n == 0:
+            raise ValueError("invalid EAMC size")
+        self._buf = np.zeros(n, dtype=np.uint8)
+        _check("moe_eamc_init", lib().moe_eamc_init(_np_ptr(self._buf), n, L, E, capacity))
+
+    def ptr(self):
+        return _np_ptr(self._buf)
+
+    def __len__(self) -> int:
+        return int(lib().moe_eamc_size(self.ptr()))
+
+    def insert(self, ream) -> int:
+        """Append, or replace the nearest stored entry when full; returns the slot."""
+        r = _i32(ream, (self.L, self.E), "ream")
+        slot = ctypes.c_int32(-1)
+        _check("moe_eamc_insert", lib().moe_eamc_insert(self.ptr(), _np_ptr(r), ctypes.byref(slot)))
+        return slot.value
+
+    def entry(self, i: int) -> np.ndarray:
+        out = np.empty((self.L, self.E), dtype=np.int32)
+        _check("moe_eamc_entry", lib().moe_eamc_entry(self.ptr(), i, _np_ptr(out)))
+        return out
+
+    def match(self, cur, n_match: int = 1):
+        """(indices, cosine distances) of the n_match nearest entries."""
+        c = _i32(cur, (self.L, self.E), "cur")
+        idx = np.empty(n_match, dtype=np.int32)
+        dist = np.empty(n_match, dtype=np.float64)
+        nf = ctypes.c_int32(0)
+        _check("moe_eamc_match", lib().moe_eamc_match(self.ptr(), _np_ptr(c), n_match, _np_ptr(idx),
+                                                      _np_ptr(dist), ctypes.byref(nf)))
+        return idx[:nf.value], dist[:nf.value]
+
+    def predict(self, cur, layer: int, n_match: int = 1) -> np.ndarray:
+        """PredictEAM: float64 [L, E] activation likelihoods for the current layer."""
+        c = _i32(cur, (self.L, self.E), "cur")
+        out = np.empty((self.L, self.E), dtype=np.float64)
+        _check("moe_eamc_predict", lib().moe_eamc_predict(self.ptr(), _np_ptr(c), layer, n_match, _np_ptr(out)))
+        return out
+
+
+class ExpertCache:
+    """The sparsity-aware expert cache (MoE-Infinity's Algorithm 1) over (layer, expert) ids."""
+
+    def __init__(self, capacity: int, L: int, E: int):
+        self.capacity, self.L, self.E = capacity, L, E
+        n = int(lib().moe_expert_cache_bytes(capacity))
+        if n == 0:
+            raise ValueError("invalid cache capacity")
+        self._buf = np.zeros(n, dtype=np.uint8)
+        _check("moe_expert_cache_init", lib().moe_expert_cache_init(_np_ptr(self._buf), n, capacity, L, E))
+
+    def lookup(self, eamc: EAMC, cur, layer: int, expert: int, n_match: int = 1, eps: float = 1e-4):
+        """(hit, evicted (layer, expert) or None)."""
+        c = _i32(cur, (self.L, self.E), "cur")
+        hit = ctypes.c_int32(0)
+        ev = np.full(2, -1, dtype=np.int32)
+        _check("moe_expert_cache_lookup",
+               lib().moe_expert_cache_lookup(_np_ptr(self._buf), eamc.ptr(), _np_ptr(c), layer, expert, n_match,
+                                             float(eps), ctypes.byref(hit), _np_ptr(ev)))
+        return bool(hit.value), (None if ev[0] < 0 else (int(ev[0]), int(ev[1])))
+
+    def contents(self):
+        out = np.empty(2 * self.capacity, dtype=np.int32)
+        n = ctypes.c_int32(0)
+        _check("moe_expert_cache_contents", lib().moe_expert_cache_contents(_np_ptr(self._buf), _np_ptr(out),
+                                                                            ctypes.byref(n)))
+        return [(int(out[2 * i]), int(out[2 * i + 1])) for i in range(n.value)]

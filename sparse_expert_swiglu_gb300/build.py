@@ -1,6 +1,7 @@
 """Build the CUDA library (sm_103a) in-tree: sparse_expert_swiglu_gb300/_build/.
 
-Each translation unit is compiled by its own nvcc process (in parallel), then the
+Each translation unit (CUDA, plus the host-only eam.cpp) is compiled by its own nvcc
+process (in parallel), then the
 objects are linked into one shared library with a C ABI (include/sparse_expert_swiglu.h).
 No torch headers are involved; the CUDA runtime is linked statically.
 """
@@ -20,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libsparse_expert_swiglu.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 SOURCES = ["pack.cu", "route.cu", "up.cu", "gather.cu", "combine.cu", "decode.cu", "fetch.cu", "api.cu",
-           "noalloc.cu"]
+           "noalloc.cu", "eam.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]
@@ -52,7 +53,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
