@@ -839,7 +839,10 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_up_kernel(DecodeParam
 // gate and down rows are interleaved in one buffer costs one 4d-byte copy, else two
 // 2d-byte copies.
 // ---------------------------------------------------------------------------
-template <int B, int MAXT>
+// STAGED: the rows come from the staging area that the fetch kernel filled (host-resident
+// gate/down rows) instead of from the experts; a separate build, so that the usual one
+// carries no code for it.
+template <int B, int MAXT, bool STAGED>
 __global__ void __launch_bounds__(MAXT, 1) decode_gather_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t gsm[];
   const int d = p.d, SR = p.sr, P = gridDim.x;
@@ -953,16 +956,18 @@ __global__ void __launch_bounds__(MAXT, 1) decode_gather_kernel(DecodeParams p) 
           break;
         }
         if (vload(&m->abort)) break;
-        uint8_t* st = ring + (size_t)s * L.row;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)L.row);
-        if (p.staging) {
+        if constexpr (STAGED) {
           // rows copied from host memory: row a + i of the staging area
+          uint8_t* st = ring + (size_t)s * L.row;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)L.row);
           bulk_g2s(st, p.staging + (size_t)(a + i) * (4 * d), (uint32_t)(4 * d), &full[s], pol);
         } else {
           const GaRow gr = list[i];
           int el;
           const ExpertSet& es = dec_set(p, grp[gr.g].expert, el);
           const size_t roff = ((size_t)el * es.f + gr.col) * es.rs;
+          uint8_t* st = ring + (size_t)s * L.row;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)L.row);
           if (es.rs == 2 * d) {
             bulk_g2s(st, es.gate_t + roff, (uint32_t)(4 * d), &full[s], pol);
           } else {
@@ -1258,23 +1263,27 @@ cudaError_t launch_decode_up(const DecodeParams& p, cudaStream_t st, bool pdl) {
   return cudaLaunchKernelEx(&cfg, decode_up_kernel<2>, p);
 }
 
+template <int B, int MAXT, bool STAGED>
+static cudaError_t launch_ga(cudaLaunchConfig_t& cfg, const DecodeParams& p, size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(decode_gather_kernel<B, MAXT, STAGED>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, decode_gather_kernel<B, MAXT, STAGED>, p);
+}
+
+template <int B, int MAXT>
+static cudaError_t launch_ga(cudaLaunchConfig_t& cfg, const DecodeParams& p, size_t smem) {
+  return p.staging ? launch_ga<B, MAXT, true>(cfg, p, smem) : launch_ga<B, MAXT, false>(cfg, p, smem);
+}
+
 cudaError_t launch_decode_gather(const DecodeParams& p, cudaStream_t st, bool pdl) {
   const GaLayoutD L = ga_layout_d(p.d, p.sr, p.list_cap, p.P);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_cfg(dim3(p.P), dim3(L.nwarps * 32), L.total, st, attr, pdl);
   // d <= 4096: at most 17 warps (96 registers per thread); above, up to 25 warps
-  const bool small = L.nwarps * 32 <= kGaSmallThreads;
-  const void* fn = small ? (p.B == 1 ? (const void*)decode_gather_kernel<1, kGaSmallThreads>
-                                     : (const void*)decode_gather_kernel<2, kGaSmallThreads>)
-                         : (p.B == 1 ? (const void*)decode_gather_kernel<1, kGaThreads>
-                                     : (const void*)decode_gather_kernel<2, kGaThreads>);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
-  if (e != cudaSuccess) return e;
-  if (small)
-    return p.B == 1 ? cudaLaunchKernelEx(&cfg, decode_gather_kernel<1, kGaSmallThreads>, p)
-                    : cudaLaunchKernelEx(&cfg, decode_gather_kernel<2, kGaSmallThreads>, p);
-  return p.B == 1 ? cudaLaunchKernelEx(&cfg, decode_gather_kernel<1, kGaThreads>, p)
-                  : cudaLaunchKernelEx(&cfg, decode_gather_kernel<2, kGaThreads>, p);
+  if (L.nwarps * 32 <= kGaSmallThreads)
+    return p.B == 1 ? launch_ga<1, kGaSmallThreads>(cfg, p, L.total) : launch_ga<2, kGaSmallThreads>(cfg, p, L.total);
+  return p.B == 1 ? launch_ga<1, kGaThreads>(cfg, p, L.total) : launch_ga<2, kGaThreads>(cfg, p, L.total);
 }
 
 }  // namespace sesg
