@@ -697,14 +697,16 @@ cudaError_t launch_gather(const ExpertParams& p, int nt, cudaStream_t st, bool p
                            (int)smem);                                                                \
   if (e != cudaSuccess) return e;                                                                     \
   return cudaLaunchKernelEx(&cfg, gather_kernel<NTV, MT, MM>, p);
-  // register caps: 96 per thread up to 640 threads (d <= 4096), 64 above
+  // register caps: 96 per thread up to 640 threads (d <= 4096), 72 up to 800 (d <= 6144),
+  // 64 above
   const bool small = (ncw + 1) * 32 <= 640;
+  const bool mid = (ncw + 1) * 32 <= 800;
   if (gather_mma(p.d, nt)) {
     if (nt <= 4) { SESG_G(4, 640, true) }
     SESG_G(8, 640, true)
   }
-  if (nt == 1) { if (small) { SESG_G(1, 640, false) } SESG_G(1, 1024, false) }
-  if (nt == 2) { if (small) { SESG_G(2, 640, false) } SESG_G(2, 1024, false) }
+  if (nt == 1) { if (small) { SESG_G(1, 640, false) } if (mid) { SESG_G(1, 800, false) } SESG_G(1, 1024, false) }
+  if (nt == 2) { if (small) { SESG_G(2, 640, false) } if (mid) { SESG_G(2, 800, false) } SESG_G(2, 1024, false) }
   if (nt == 4 && small) { SESG_G(4, 640, false) }
   return cudaErrorInvalidConfiguration;
 #undef SESG_G

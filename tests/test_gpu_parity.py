@@ -331,6 +331,12 @@ def test_layer_mixtral_8x7b_batch3():
     run_layer_case(4096, 14336, 8, 2, 3, 0, [70], seed=7, gen_device="cuda")
 
 
+def test_layer_wide_hidden_general_path():
+    """d = 6144 with five tokens: the general path's gather with 24 consumer warps (groups of
+    at most 2 tokens on the CUDA cores, the 800-thread build)."""
+    run_layer_case(6144, 1024, 8, 2, 5, 0, [0, 70], seed=75, gen_device="cuda", rmsnorm=True)
+
+
 def test_layer_mixtral_8x22b_shape_b2():
     """d=6144, f=16384, two tokens (the decode path), RMSNorm output."""
     run_layer_case(6144, 16384, 8, 2, 2, 0, [70], seed=6, gen_device="cuda", rmsnorm=True)
