@@ -1144,10 +1144,9 @@ __global__ void __launch_bounds__(MAXT, 1) decode_gather_kernel(DecodeParams p) 
   // before the barrier that precedes the reads (acquire).
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    const bool last = atomicAdd(&p.ctrl->gdone, 1) == (int)gridDim.x - 1;
-    if (last) __threadfence();
-    m->last = last;
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(&p.ctrl->gdone) : "memory");
+    m->last = old == gridDim.x - 1;
   }
   __syncthreads();
   if (m->last) {
