@@ -1140,8 +1140,9 @@ __global__ void __launch_bounds__(MAXT, 1) decode_gather_kernel(DecodeParams p) 
   }
   // the last CTA to finish: y = fp16(sum) or, for stacked layers, the RMSNorm
   // y / sqrt(mean(y^2) + 1e-6) of it.  The barrier orders every thread's additions
-  // before thread 0's fence and count (release); the last count is followed by a fence
-  // before the barrier that precedes the reads (acquire).
+  // before thread 0's count, an acq_rel atomic: its release publishes them, and in the
+  // last CTA its acquire, followed by the barrier, orders the reads below after every
+  // other CTA's additions.
   __syncthreads();
   if (tid == 0) {
     unsigned old;

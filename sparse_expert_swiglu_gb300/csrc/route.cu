@@ -277,13 +277,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
     __syncthreads();
   }
   if (gridDim.x > 1) {
-    // the last CTA to finish groups the pairs of every token
-    __threadfence();
+    // the last CTA to finish groups the pairs of every token.  The barrier orders this
+    // CTA's top-k stores before thread 0's count, whose release publishes them and whose
+    // acquire (in the last CTA) makes the other CTAs' stores visible to its reads below.
     __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(&p.ctrl->route_done, 1) == (int)gridDim.x - 1);
+    if (threadIdx.x == 0) {
+      unsigned old;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(&p.ctrl->route_done) : "memory");
+      s_last = old == gridDim.x - 1;
+    }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
   }
   router_group(p, local);
   if (threadIdx.x == 0) p.ctrl->route_done = 0;
