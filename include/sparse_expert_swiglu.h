@@ -303,7 +303,8 @@ moe_status_t moe_eamc_predict(const void* eamc, const int32_t* cur, int32_t laye
  *                     row sums to 0), is removed (ties: the earliest inserted) and the
  *                     requested expert appended.
  * evicted[2] receives the removed (layer, expert), or (-1, -1).  The EAMC must have the
- * cache's L and E.  moe_expert_cache_contents copies the (layer, expert) pairs in
+ * cache's L and E; a miss on a full cache needs L * E <= 4096 and n_match <= 1024
+ * (MOE_ERR_UNSUPPORTED_SHAPE otherwise, nothing changed).  moe_expert_cache_contents copies the (layer, expert) pairs in
  * insertion order to layer_expert[2 * n] (optional) and sets *n.
  */
 size_t moe_expert_cache_bytes(int32_t capacity);

@@ -101,3 +101,10 @@ def test_host_argument_checks(so):
     bad_a = _lib._Layer(2, 1, 0x50000, ex_odd, _lib._Experts(0, 4096, 14336, None, None, None, None))
     assert lib.moe_layer_decode(fake, 1, ctypes.byref(bad_a), fake, 0, None, fake, 0, None) == -3
     assert lib.moe_expert_sparse_swiglu(fake, 1, ctypes.byref(ex), 8, fake, None, fake, 0, None) == -1
+    # the host-rows layer call: the same checks, before any pointer is looked up
+    assert lib.moe_layer_decode_host_rows(fake, 0, ctypes.byref(layer), fake, 0, None, fake, 0, None) == 0
+    assert lib.moe_layer_decode_host_rows(fake, 1, ctypes.byref(bad), fake, 0, None, fake, 0, None) == -1
+    assert lib.moe_layer_decode_host_rows(fake, 1, ctypes.byref(bad_d), fake, 0, None, fake, 0, None) == -2
+    assert lib.moe_layer_decode_host_rows(fake, 1, ctypes.byref(bad_a), fake, 0, None, fake, 0, None) == -3
+    assert lib.moe_layer_decode_host_rows(fake, 1, None, fake, 0, None, fake, 0, None) == -1
+    assert lib.moe_layer_host_rows_workspace_bytes(ctypes.byref(bad), 1) == 0
