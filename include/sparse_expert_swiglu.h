@@ -329,6 +329,16 @@ moe_status_t moe_get_status(void* ws, void* stream);
 /* Static string for a status code. */
 const char* moe_status_string(moe_status_t status);
 
+/*
+ * moe_selftest_wait_timeout -- diagnostic of the timeout path of every kernel: enqueues
+ * on `stream` one thread that waits on a barrier nothing completes, for at most `tries`
+ * (1..4000) try_wait rounds of at most about 1 ms each, then records MOE_ERR_TIMEOUT in
+ * `ws` the way the kernels do.  moe_get_status then returns MOE_ERR_TIMEOUT (and clears
+ * it); the context stays usable.  ws: any workspace of this library (its control block
+ * is first), 256-byte aligned.  Nothing faults or hangs.
+ */
+moe_status_t moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t tries, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -101,6 +101,8 @@ _SIGS = {
                                                ctypes.c_void_p]),
     "moe_expert_cache_contents": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "moe_workspace_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint32,
+                                                 ctypes.c_void_p]),
     "moe_get_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }

@@ -108,3 +108,8 @@ def test_host_argument_checks(so):
     assert lib.moe_layer_decode_host_rows(fake, 1, ctypes.byref(bad_a), fake, 0, None, fake, 0, None) == -3
     assert lib.moe_layer_decode_host_rows(fake, 1, None, fake, 0, None, fake, 0, None) == -1
     assert lib.moe_layer_host_rows_workspace_bytes(ctypes.byref(bad), 1) == 0
+    # the timeout diagnostic: refused before anything is enqueued
+    assert lib.moe_selftest_wait_timeout(None, 1 << 20, 10, None) == -1
+    assert lib.moe_selftest_wait_timeout(fake, 1 << 20, 0, None) == -1
+    assert lib.moe_selftest_wait_timeout(fake, 4, 10, None) == -4
+    assert lib.moe_selftest_wait_timeout(odd, 1 << 20, 10, None) == -3

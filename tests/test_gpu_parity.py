@@ -7,6 +7,7 @@ rule of tests/parity.py.
 
 from __future__ import annotations
 
+import ctypes
 import math
 
 import numpy as np
@@ -466,6 +467,31 @@ def test_decode_host_rows_match_device_rows():
     x5 = synth.tokens(5, d, 96, device="cuda")
     with pytest.raises(ses.MoeError):
         ses.layer_decode_host_rows(x5, host_layer)
+
+
+def test_wait_timeout_is_reported_and_the_context_stays_usable():
+    """A bounded wait that runs out (a barrier nothing completes, 20 rounds of at most
+    about 1 ms) records MOE_ERR_TIMEOUT, which moe_get_status returns once and clears;
+    a layer then runs on the same stream and workspace and gives the result it gave
+    before."""
+    d, f, E, k = 1024, 512, 8, 2
+    de = synth.experts(E, d, f, 33)
+    ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(),
+                                torch.full((E,), 0.05, dtype=torch.float32).cuda())
+    layer = ses.Layer(synth.router(d, E, 33).cuda(), ex, k)
+    x = synth.tokens(2, d, 33).cuda()
+    ws = ses.Workspace(ses.layer_workspace_bytes(layer, 2))
+    y0 = ses.layer_decode(x, layer, ws=ws)
+    assert ws.status() == 0
+    lib = ses.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.moe_selftest_wait_timeout(ws.ptr(), ws.nbytes, 20, stream) == 0
+    assert ws.status() == -6  # MOE_ERR_TIMEOUT
+    assert ws.status() == 0   # read once, then cleared
+    y1 = ses.layer_decode(x, layer, ws=ws)
+    assert ws.status() == 0
+    assert _same_up_to_sum_order(y1, y0)
+    assert lib.moe_selftest_wait_timeout(ws.ptr(), ws.nbytes, 0, stream) == -1
 
 
 def test_decode_repeated_calls_share_the_workspace():
