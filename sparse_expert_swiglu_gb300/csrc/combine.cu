@@ -16,7 +16,10 @@ namespace cg = cooperative_groups;
 
 namespace sesg {
 
-constexpr int kCombThreads = 1024;
+// Threads per CTA: 1024 up to 8 tokens (more subsets of the partial rows, one round of
+// loads), 256 above (several CTAs per SM, so that 8 CTAs per token still run in one
+// wave); 256 threads cover the d / 32 float4 columns of a CTA for d <= 8192.
+__host__ __device__ constexpr int comb_threads(int B) { return B <= 8 ? 1024 : 256; }
 constexpr int kCombSlices = 8;
 
 __device__ __forceinline__ long long cta_first_item(long long N, int c, int P) { return N * c / P; }
@@ -24,8 +27,8 @@ __device__ __forceinline__ int cta_of_item(long long i, long long N, int P) {
   return (int)(((i + 1) * P + N - 1) / N) - 1;
 }
 
-template <bool RMS>
-__global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(ExpertParams p) {
+template <bool RMS, int kCombThreads>
+__global__ void __launch_bounds__(kCombThreads) combine_kernel(ExpertParams p) {
   extern __shared__ float4 comb_smem[];
   const int P = p.P3;
   float4* s_red = comb_smem;                                   // [kCombThreads]
@@ -177,14 +180,21 @@ __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(ExpertParams p
 
 size_t combine_smem_bytes(const ExpertParams& p) {
   const size_t ints = (size_t)p.P3 + 1 + p.G_max + 1 + (size_t)p.n_slots * p.P3 + 4;
-  return ints * 4 + (size_t)kCombThreads * 16;
+  return ints * 4 + (size_t)comb_threads(p.B) * 16;
+}
+
+template <bool RMS, int NT>
+static cudaError_t launch_comb(cudaLaunchConfig_t& cfg, const ExpertParams& p, size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(combine_kernel<RMS, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, combine_kernel<RMS, NT>, p);
 }
 
 cudaError_t launch_combine(const ExpertParams& p, cudaStream_t st, bool pdl) {
   const size_t smem = combine_smem_bytes(p);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kCombSlices, p.B);
-  cfg.blockDim = dim3(kCombThreads);
+  cfg.blockDim = dim3(comb_threads(p.B));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -203,15 +213,10 @@ cudaError_t launch_combine(const ExpertParams& p, cudaStream_t st, bool pdl) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  cudaError_t e;
   if (p.rmsnorm) {
-    e = cudaFuncSetAttribute(combine_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, combine_kernel<true>, p);
+    return comb_threads(p.B) == 1024 ? launch_comb<true, 1024>(cfg, p, smem) : launch_comb<true, 256>(cfg, p, smem);
   }
-  e = cudaFuncSetAttribute(combine_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<false>, p);
+  return comb_threads(p.B) == 1024 ? launch_comb<false, 1024>(cfg, p, smem) : launch_comb<false, 256>(cfg, p, smem);
 }
 
 }  // namespace sesg
