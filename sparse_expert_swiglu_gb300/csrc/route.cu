@@ -155,12 +155,17 @@ __device__ void router_topk(const RouteParams& p, int b, const float* logits, in
   }
 }
 
-// Last CTA: counting of tokens per expert and the expert work groups.
+// Last CTA: counting of tokens per expert and the expert work groups.  Every pair sets
+// its token's bit in its expert's token mask (a token's k experts are distinct), so an
+// expert's count is a popcount and its tokens come out in ascending order by walking
+// the set bits: no loop over all pairs per expert.
 __device__ void router_group(const RouteParams& p, bool local) {
   extern __shared__ float dyn[];
   int* s_idx = reinterpret_cast<int*>(dyn);   // [B*k]
   int* s_list = s_idx + p.B * p.k;            // [B*k] (token << 4 | slot) grouped by expert
   float* s_w = reinterpret_cast<float*>(s_list + p.B * p.k);  // [B*k]
+  uint32_t* s_em = reinterpret_cast<uint32_t*>(s_w + p.B * p.k);  // [E][ceil(B/32)] token masks
+  const int nw = (p.B + 31) / 32;
   __shared__ int s_cnt[256], s_off[257], s_goff[257];
   const int tid = threadIdx.x;
   const int npair = p.B * p.k;
@@ -170,10 +175,16 @@ __device__ void router_group(const RouteParams& p, bool local) {
       s_w[i] = __ldcg(p.topk_w + i);
     }
   }
+  for (int w = tid; w < p.E * nw; w += kRouteThreads) s_em[w] = 0u;
+  __syncthreads();
+  for (int i = tid; i < npair; i += kRouteThreads) {
+    const int b = i / p.k;
+    atomicOr(&s_em[s_idx[i] * nw + (b >> 5)], 1u << (b & 31));
+  }
   __syncthreads();
   for (int e = tid; e < p.E; e += kRouteThreads) {
     int c = 0;
-    for (int i = 0; i < npair; ++i) c += (s_idx[i] == e);
+    for (int w = 0; w < nw; ++w) c += __popc(s_em[e * nw + w]);
     s_cnt[e] = c;
     if (p.expert_count) p.expert_count[e] = c;
   }
@@ -207,11 +218,19 @@ __device__ void router_group(const RouteParams& p, bool local) {
   }
   __syncthreads();
   if (!p.group) return;
-  // tokens of expert e in ascending order
+  // tokens of expert e in ascending order, each with the slot j where it chose e
   for (int e = tid; e < p.E; e += kRouteThreads) {
     int o = s_off[e];
-    for (int i = 0; i < npair; ++i)
-      if (s_idx[i] == e) s_list[o++] = ((i / p.k) << 4) | (i % p.k);
+    for (int w = 0; w < nw; ++w) {
+      uint32_t m = s_em[e * nw + w];
+      while (m) {
+        const int b = w * 32 + __ffs(m) - 1;
+        m &= m - 1;
+        int j = 0;
+        while (j + 1 < p.k && s_idx[b * p.k + j] != e) ++j;
+        s_list[o++] = (b << 4) | j;
+      }
+    }
   }
   __syncthreads();
   const int g_routed = s_goff[p.E];
@@ -316,15 +335,18 @@ __global__ void expert_prep_kernel(int expert, int n, int gcap, GroupDesc* group
   if (threadIdx.x == 0) ctrl->G = G;
 }
 
-size_t route_group_smem(int B, int k) { return (size_t)3 * B * k * sizeof(int); }
+size_t route_group_smem(int B, int k, int E) {
+  return (size_t)3 * B * k * sizeof(int) + (size_t)E * ((B + 31) / 32) * sizeof(uint32_t);
+}
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.B);  // one CTA per token; the last one groups the pairs
   cfg.blockDim = dim3(kRouteThreads);
-  cfg.dynamicSmemBytes = route_group_smem(p.B, p.k);
+  cfg.dynamicSmemBytes = route_group_smem(p.B, p.k, p.E);
   cfg.stream = st;
-  if (cfg.dynamicSmemBytes > 48 * 1024) {
+  {
+    // always: the kernel's static shared memory counts against the default 48 KB too
     cudaError_t e = cudaFuncSetAttribute(
         p.E % 8 == 0 ? (const void*)route_kernel<8> : (const void*)route_kernel<1>,
         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
