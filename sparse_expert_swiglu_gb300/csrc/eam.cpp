@@ -96,20 +96,20 @@ int nearest(const EamcHeader* h, const int32_t* cur, int n, int32_t* idx, double
       for (int u = 0; u < nb; ++u) acc[u] += ct * (double)col[u];
     }
     for (int u = 0; u < nb; ++u) {
-    const int32_t i = b + u;
-    const double di = cosine_distance((int64_t)acc[u], cc, norms[i]);
-    // insertion into the sorted prefix [0, m) of at most n entries
-    int pos = m;
-    while (pos > 0 && dist[pos - 1] > di) --pos;  // equal distances keep the lower index first
-    if (pos >= n) continue;
-    const int last = m < n ? m : n - 1;
-    for (int t = last; t > pos; --t) {
-      dist[t] = dist[t - 1];
-      idx[t] = idx[t - 1];
-    }
-    dist[pos] = di;
-    idx[pos] = i;
-    if (m < n) ++m;
+      const int32_t i = b + u;
+      const double di = cosine_distance((int64_t)acc[u], cc, norms[i]);
+      // insertion into the sorted prefix [0, m) of at most n entries
+      int pos = m;
+      while (pos > 0 && dist[pos - 1] > di) --pos;  // equal distances keep the lower index first
+      if (pos >= n) continue;
+      const int last = m < n ? m : n - 1;
+      for (int t = last; t > pos; --t) {
+        dist[t] = dist[t - 1];
+        idx[t] = idx[t - 1];
+      }
+      dist[pos] = di;
+      idx[pos] = i;
+      if (m < n) ++m;
     }
   }
   return m;
