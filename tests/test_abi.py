@@ -113,3 +113,24 @@ def test_host_argument_checks(so):
     assert lib.moe_selftest_wait_timeout(fake, 1 << 20, 0, None) == -1
     assert lib.moe_selftest_wait_timeout(fake, 4, 10, None) == -4
     assert lib.moe_selftest_wait_timeout(odd, 1 << 20, 10, None) == -3
+
+
+def test_binding_refuses_host_memory_outside_the_host_rows_call():
+    """The binding hands only CUDA tensors to the device path; gate/down rows in host
+    memory must be page-locked and go through layer_decode_host_rows (no GPU needed:
+    the checks run before any call into the library)."""
+    import torch
+    from sparse_expert_swiglu_gb300 import _lib
+    t = torch.zeros(4)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        _lib._need(t, torch.float32, "x")
+    with pytest.raises(TypeError, match="page-locked"):
+        _lib._need(t, torch.float32, "x", host_ok=True)  # pageable host memory
+    ex = _lib.Experts(torch.zeros(1, 8, dtype=torch.uint8), torch.zeros(1, 16, 256, dtype=torch.float16),
+                      torch.zeros(1, 16, 256, dtype=torch.float16), torch.zeros(1))
+    assert ex.rows_on_host
+    with pytest.raises(TypeError):
+        ex.c_struct()
+    layer = _lib.Layer(torch.zeros(256, 1, dtype=torch.float16), ex, 1)
+    with pytest.raises(ValueError, match="layer_decode_host_rows"):
+        _lib.layer_decode(torch.zeros(1, 256, dtype=torch.float16), layer)
