@@ -212,3 +212,34 @@ def test_request_eam_from_router_counts():
     assert np.array_equal(ream, ref)
     assert ream.sum() == 3 * L * B * k
     torch.cuda.synchronize()
+
+
+def test_library_matches_oracle_on_random_shapes():
+    """Random shapes, capacities, match counts and request sequences (hypothesis):
+    the library's slots, matches, predictions and cache decisions equal the oracle's."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+    import sparse_expert_swiglu_gb300 as ses
+
+    @hyp.settings(max_examples=40, deadline=None)
+    @hyp.given(L=st.integers(1, 6), E=st.integers(1, 9), cap=st.integers(1, 5),
+               n_match=st.integers(1, 4), seed=st.integers(0, 2 ** 31 - 1))
+    def run(L, E, cap, n_match, seed):
+        rng = np.random.default_rng(seed)
+        lib_c, orc_c = ses.EAMC(L, E, cap), eo.Eamc(L, E, cap)
+        lib_k, orc_k = ses.ExpertCache(max(1, L), L, E), eo.ExpertCache(max(1, L), L, E)
+        for _ in range(2 * cap + 2):
+            m = rng.integers(0, 4, size=(L, E)).astype(np.int32)
+            layer = int(rng.integers(L))
+            assert np.array_equal(lib_c.predict(m, layer, n_match), eo.predict(orc_c, m, layer, n_match))
+            idx, dist = lib_c.match(m, n_match)
+            oi, od = eo.nearest(orc_c.entries, m, n_match)
+            assert idx.tolist() == oi and dist.tolist() == od
+            for _ in range(3):
+                e = int(rng.integers(E))
+                assert lib_k.lookup(lib_c, m, layer, e, n_match, 1e-4) == \
+                    orc_k.lookup(orc_c, m, layer, e, n_match, 1e-4)
+            assert lib_c.insert(m) == orc_c.insert(m)
+        assert lib_k.contents() == orc_k.items
+
+    run()
