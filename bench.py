@@ -382,6 +382,8 @@ def per_kernel_times(prof_graphs, events_list, stream, steps, path):
                 acc[j] += evs[j].elapsed_time(evs[j + 1])
             n += 1
     t = [acc[j] / n * 1e3 for j in range(4)]  # microseconds
+    if path == "decode_fused":
+        return {"decode_layer_kernel": t[1], "event_pair_us": t[0]}
     if path == "decode":
         return {"decode_up_kernel": t[1], "decode_gather_kernel": t[2], "event_pair_us": t[0]}
     return {"route_kernel": t[0], "up_kernel": t[1], "gather_kernel": t[2], "combine_kernel": t[3]}
@@ -562,7 +564,10 @@ def run_ours(args, world, rank, local):
     up_b = float(np.mean([b["up"] for b in byts]))
     ga_b = float(np.mean([b["gather"] for b in byts]))
     rt_b = float(np.mean([b["route"] for b in byts]))
-    if path == "decode":
+    if path == "decode_fused":
+        # one kernel: router, up projection, kept rows, combination
+        kernel_bytes = {"decode_layer_kernel": up_b + rt_b + ga_b}
+    elif path == "decode":
         # the up kernel also reads the router weight and the tokens
         kernel_bytes = {"decode_up_kernel": up_b + rt_b, "decode_gather_kernel": ga_b}
     else:
@@ -660,7 +665,7 @@ def run_ours(args, world, rank, local):
                        "copy after the last)",
                 "one_step_at_a_time": {"value": e2e_step_value, "unit": "expert-tokens/s",
                                        "how": "per step: copy in, one layer's graph, copy out, one stream"}},
-        "gpu_launches": (2 if path == "decode" else 4) * args.steps,
+        "gpu_launches": {"decode_fused": 1, "decode": 2}.get(path, 4) * args.steps,
         "path": path,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
@@ -810,7 +815,9 @@ def run_workload(args, world, rank, local):
             names = (["event_pair_us", "decode_up_kernel", "decode_fetch_and_gather_kernels", "event_pair_us_2"]
                      if host_rows else
                      ["event_pair_us", "decode_up_kernel", "decode_gather_kernel", "event_pair_us_2"]
-                     if path == "decode" else ["route_kernel", "up_kernel", "gather_kernel", "combine_kernel"])
+                     if path == "decode" else
+                     ["event_pair_us", "decode_layer_kernel", "event_pair_us_2", "event_pair_us_3"]
+                     if path == "decode_fused" else ["route_kernel", "up_kernel", "gather_kernel", "combine_kernel"])
             kt = {nm: float(v) / 10 for nm, v in zip(names, kacc)}
             extra = {}
             if host_rows:

@@ -410,11 +410,13 @@ def layer_workspace_bytes(layer: Layer, B: int) -> int:
 
 
 def layer_path(layer: Layer, B: int) -> str:
-    """'decode' (one or two tokens: up, gather, combine kernels) or 'general'."""
+    """Which kernels layer_decode runs: 'decode_fused' (one or two tokens, d <= 4096: one
+    kernel), 'decode' (one or two tokens, wider d: an up kernel and a gather kernel) or
+    'general' (router, up, gather and combine kernels)."""
     r = int(lib().moe_layer_path(ctypes.byref(layer.c_struct()), B))
     if r < 0:
         raise MoeError("moe_layer_path", r)
-    return "decode" if r == 1 else "general"
+    return {1: "decode", 2: "decode_fused"}.get(r, "general")
 
 
 def layer_decode(x: torch.Tensor, layer: Layer, rmsnorm: bool = False,

@@ -348,13 +348,21 @@ static bool use_decode_path(const moe_layer_t* layer, int B, const DeviceInfo& d
          decode_plan(B, layer->routed.d, layer->routed.E, umax, cap, P, di.smem_optin, su, sr);
 }
 
+// The decode path runs as one kernel: the shapes of use_decode_path with d <= 4096 whose
+// one-kernel shared-memory plan fits.
+static bool use_layer_kernel(const moe_layer_t* layer, int B, const DeviceInfo& di, int umax, int& su,
+                             int& sr) {
+  return decode_layer_plan(B, layer->routed.d, layer->routed.E, umax, di.smem_optin, su, sr) != 0;
+}
+
 int32_t moe_layer_path(const moe_layer_t* layer, int32_t B) {
   moe_status_t s = check_layer(layer, B);
   if (s != MOE_OK) return s;
   DeviceInfo di;
   if (device_info(di) != cudaSuccess) return MOE_ERR_CUDA;
   int su = 0, sr = 0, cap = 0, umax = 0;
-  return B >= 1 && use_decode_path(layer, B, di, su, sr, cap, umax) ? 1 : 0;
+  if (!(B >= 1 && use_decode_path(layer, B, di, su, sr, cap, umax))) return 0;
+  return use_layer_kernel(layer, B, di, umax, su, sr) ? 2 : 1;
 }
 
 // Kept-column entries each up CTA's list holds (16 per unit of its share).
@@ -422,8 +430,21 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
     // one or two tokens: up kernel, gather kernel
     DecodeParams dp;
     fill_decode_params(dp, x, B, layer, y, rmsnorm_out, dbg, ws, L, P, su, sr, cap, umax);
-    // the router runs inside the up kernel and the combination inside the gather kernel:
-    // events 0 and 1, and 3 and 4, mark the same points
+    int lsu = 0, lsr = 0;
+    if (use_layer_kernel(layer, B, di, umax, lsu, lsr)) {
+      // one kernel: events 0 and 1 mark its start, events 2, 3 and 4 its end
+      dp.su = lsu;
+      dp.sr = lsr;
+      cudaError_t e = record(dbg, 0, st);
+      if (e == cudaSuccess) e = record(dbg, 1, st);
+      if (e == cudaSuccess) e = launch_decode_layer(dp, st, true);
+      if (e == cudaSuccess) e = record(dbg, 2, st);
+      if (e == cudaSuccess) e = record(dbg, 3, st);
+      if (e == cudaSuccess) e = record(dbg, 4, st);
+      return cuda_status(e);
+    }
+    // two kernels: the router runs inside the up kernel and the combination inside the
+    // gather kernel: events 0 and 1, and 3 and 4, mark the same points
     cudaError_t e = record(dbg, 0, st);
     if (e == cudaSuccess) e = record(dbg, 1, st);
     if (e == cudaSuccess) e = launch_decode_up(dp, st, true);

@@ -242,10 +242,10 @@ __device__ __forceinline__ void route_prefetch(const DecodeParams& p, const Rout
   }
 }
 
-template <int B>
+template <int B, typename Misc>
 __device__ __forceinline__ void dec_route(const DecodeParams& p, int nthreads, const RouteSplit& rt,
                                           const uint4 (&wv0)[kRouteRows], const __half* xs, float* lred,
-                                          UpMisc* m, GroupDesc* grp) {
+                                          Misc* m, GroupDesc* grp) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = nthreads / 32;
   const int E = p.routed.E, d = p.d, k = p.k;
   const int nchunk = rt.nchunk;
@@ -479,13 +479,14 @@ __device__ __forceinline__ void dec_up_setup(const __half* xs, int d, const Grou
   __syncwarp();
 }
 
-template <int T, int PH, int GAM>
+// FULL: all 8 quantiser groups of the superblock exist (no per-group test)
+template <int T, int PH, int GAM, bool FULL>
 __device__ __forceinline__ void dec_groups(const uint4 (&w)[4], const uint32_t (&xr)[T][4][2],
                                            int cl, float (&D)[4][4], int ng) {
   constexpr int G = 8 / T;
   if constexpr (GAM < G) {
     constexpr int GI = PH * G + GAM;
-    if (GI < ng) {
+    if (FULL || GI < ng) {
       const bool on = cl == GAM;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -497,11 +498,11 @@ __device__ __forceinline__ void dec_groups(const uint4 (&w)[4], const uint32_t (
         mma_16816(D[t], a, on ? xr[PH][t][0] : 0u, on ? xr[PH][t][1] : 0u);
       }
     }
-    dec_groups<T, PH, GAM + 1>(w, xr, cl, D, ng);
+    dec_groups<T, PH, GAM + 1, FULL>(w, xr, cl, D, ng);
   }
 }
 
-template <int T, int PH>
+template <int T, int PH, bool FULL>
 __device__ __forceinline__ void dec_phases(const uint4 (&w)[4], const uint32_t (&xr)[T][4][2],
                                            const uint32_t (&sz)[T][2][2], const float* xgw,
                                            int ng, float (&vacc)[2][2]) {
@@ -511,12 +512,12 @@ __device__ __forceinline__ void dec_phases(const uint4 (&w)[4], const uint32_t (
     float D[4][4];
 #pragma unroll
     for (int t = 0; t < 4; ++t) D[t][0] = D[t][1] = D[t][2] = D[t][3] = 0.f;
-    dec_groups<T, PH, 0>(w, xr, gl % G, D, ng);
+    dec_groups<T, PH, 0, FULL>(w, xr, gl % G, D, ng);
     const int gi_lane = (2 * c) % G, tau = (2 * c) / G;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const int gi = PH * G + gi_lane + s;
-      if (gi < ng) {
+      if (FULL || gi < ng) {
         const float cs = pos_scale(gi);
         const float X = xgw[tau * 8 + gi];
 #pragma unroll
@@ -528,7 +529,7 @@ __device__ __forceinline__ void dec_phases(const uint4 (&w)[4], const uint32_t (
         }
       }
     }
-    dec_phases<T, PH + 1>(w, xr, sz, xgw, ng, vacc);
+    dec_phases<T, PH + 1, FULL>(w, xr, sz, xgw, ng, vacc);
   }
 }
 
@@ -619,6 +620,205 @@ __device__ __forceinline__ int dec_finalize(const DecodeParams& p, const float4*
   return cnt;
 }
 
+// The shared-memory objects of the up phase, common to the up kernel of the two-kernel
+// decode path and to the one-kernel decode layer.
+struct UpShared {
+  uint64_t *full, *empty;     // strip ring: [su] data landed / stage free (nsb warps)
+  uint64_t *vfull, *vfree;    // unit slots: [kDecNV] partials in (nsb warps) / finalized
+  int* abort;
+  int* pend;                  // [kDecMaxSu] strip in flight in the stage (issue index + 1) or 0
+  float (*vbuf)[16 * 2];      // [kDecNV] per-slot v staging of the finalize warps
+  int* ucnt;                  // [kDecMaxUnits] kept columns of each unit
+  uint8_t* ring;
+  const __half* xs;
+  float4* vpart;
+  float* xg;
+  const GroupDesc* grp;
+  int4* ent;                  // [unit][16] kept columns of each unit
+  size_t strip;
+  int su, nsb;
+  uint64_t* ufin;             // [kDecMaxUnits] single-use: unit j finalized (NULL: not signalled)
+};
+
+// Strip producer (one lane): the packed strips of units u0 .. u0 + n - 1, in order.
+__device__ __forceinline__ void dec_issue_strips(const DecodeParams& p, const UpShared& S, int u0, int n, int MT) {
+  const uint64_t pol = policy_evict_first();
+  int s = 0, ph = 0, g = u0 / MT, mt = u0 - g * MT;
+  for (int j = 0; j < n; ++j) {
+    if (j >= S.su && !mbar_wait(&S.empty[s], ph ^ 1)) {
+      dec_fail(p, S.abort);
+      break;
+    }
+    if (vload(S.abort)) break;
+    int el;
+    const ExpertSet& es = dec_set(p, S.grp[g].expert, el);
+    S.pend[s] = j + 1;
+    mbar_arrive_expect_tx(&S.full[s], (uint32_t)S.strip);
+    bulk_g2s(S.ring + (size_t)s * S.strip, es.up + (size_t)el * es.up_stride + (size_t)mt * S.strip,
+             (uint32_t)S.strip, &S.full[s], pol);
+    if (++s == S.su) {
+      s = 0;
+      ph ^= 1;
+    }
+    if (++mt == MT) {
+      mt = 0;
+      ++g;
+    }
+  }
+}
+
+// Finalize warp fl of NL: units j = fl, fl + NL, ... once all their superblock partials
+// are in; the unit's kept columns go to its 16 entries, then its count is published.
+template <int B>
+__device__ __forceinline__ void dec_finalize_units(const DecodeParams& p, const UpShared& S, int fl, int NL,
+                                                   int u0, int n, int MT) {
+  const int lane = threadIdx.x & 31;
+  int g = (u0 + fl) / MT, mt = (u0 + fl) - g * MT, cur_g = -1;
+  float thr = 0.f;
+  for (int j = fl; j < n; j += NL) {
+    const int slot = j & (kDecNV - 1);
+    if (!__all_sync(0xffffffffu, mbar_wait(&S.vfull[slot], (j >> 2) & 1))) {
+      if (lane == 0) dec_fail(p, S.abort);
+      break;
+    }
+    if (g != cur_g) {
+      int el;
+      const ExpertSet& es = dec_set(p, S.grp[g].expert, el);
+      thr = es.thr[el];
+      cur_g = g;
+    }
+    const int cnt = dec_finalize<B>(p, S.vpart + (size_t)slot * S.nsb * 32, S.nsb, S.grp[g], g, mt, thr,
+                                    S.vbuf[slot], S.ent + (size_t)j * 16);
+    __syncwarp();
+    if (lane == 0) {
+      // the entries before the count: the row producer of the one-kernel layer reads
+      // the count without a block barrier
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(S.ucnt + j) = cnt;
+      if (S.ufin) mbar_arrive(&S.ufin[j]);
+      mbar_arrive(&S.vfree[slot]);
+    }
+    mt += NL;
+    while (mt >= MT) {
+      mt -= MT;
+      ++g;
+    }
+  }
+}
+
+// Superblock warp (warp index uw < NL * nsb): unit lane ug = uw / nsb (units j = ug,
+// ug + NL, ...), superblock sb = uw % nsb of every unit.
+template <int B>
+__device__ __forceinline__ void dec_up_units(const DecodeParams& p, const UpShared& S, int NL, int u0, int n,
+                                             int MT) {
+  const int d = p.d, lane = threadIdx.x & 31, uw = threadIdx.x >> 5;
+  const int nsb = S.nsb, SU = S.su, ug = uw / nsb, sb = uw % nsb;
+  const int ng = min(8, (d - sb * kSuper) / kGroup);
+  float* xgw = S.xg + uw * 16;
+  uint32_t xr[B][4][2];
+  int cur_g = -1;
+  // stage s = j % SU with full-barrier parity ph = (j / SU) & 1, and unit u = u0 + j as
+  // (group g, M-tile mt), all advanced by NL units per iteration without divisions
+  int s = ug % SU, ph = (ug / SU) & 1;
+  int g = (u0 + ug) / MT, mt = (u0 + ug) - g * MT;
+  for (int j = ug; j < n; j += NL) {
+    const int slot = j & (kDecNV - 1);
+    const bool ab = vload(S.abort) != 0;
+    bool ok = __all_sync(0xffffffffu, !ab && mbar_wait(&S.full[s], ph));
+    if (!ok) {
+      if (!ab && lane == 0) dec_fail(p, S.abort);
+      break;
+    }
+    if (g != cur_g) {
+      dec_up_setup<B>(S.xs, d, S.grp[g], sb, ng, xr, xgw);
+      cur_g = g;
+    }
+    uint4 w[4];
+    uint32_t sz[B][2][2];
+    dec_load_block<B>(S.ring + (size_t)s * S.strip + (size_t)sb * kBlkBytes, w, sz);
+    __syncwarp();
+    if (lane == 0) {
+      if (sb == 0) S.pend[s] = 0;
+      mbar_arrive(&S.empty[s]);  // release: the copies above are done before the stage is reused
+    }
+    float vacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    if (ng == 8)
+      dec_phases<B, 0, true>(w, xr, sz, xgw, ng, vacc);
+    else
+      dec_phases<B, 0, false>(w, xr, sz, xgw, ng, vacc);
+    // the slot's previous unit must have been finalized
+    if (j >= kDecNV && !__all_sync(0xffffffffu, mbar_wait(&S.vfree[slot], ((j >> 2) - 1) & 1))) {
+      if (lane == 0) dec_fail(p, S.abort);
+      break;
+    }
+    S.vpart[((size_t)slot * nsb + sb) * 32 + lane] = make_float4(vacc[0][0], vacc[0][1], vacc[1][0], vacc[1][1]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.vfull[slot]);
+    s += NL;
+    if (s >= SU) {
+      s -= SU;
+      ph ^= 1;
+    }
+    mt += NL;
+    while (mt >= MT) {
+      mt -= MT;
+      ++g;
+    }
+  }
+}
+
+// The last CTA to finish: y = fp16(sum of the accumulator copies) or, for stacked
+// layers, the RMSNorm y / sqrt(mean(y^2) + 1e-6) of it.  It leaves the copies zeroed
+// and the finish counter reset for the next call on the workspace (every CTA's additions
+// and count precede this, and the next call starts after this kernel ends).
+// ss: [B][32] floats of shared memory; called by every thread of the CTA.
+template <int B>
+__device__ __forceinline__ void dec_last_cta(const DecodeParams& p, int nwarps, float* ss) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, d = p.d;
+  float4 v[B][2];
+  float sq[B];
+#pragma unroll
+  for (int b = 0; b < B; ++b) {
+    v[b][0] = v[b][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid < d / 8) {
+#pragma unroll
+      for (int r = 0; r < kDecYRep; ++r) {
+        float4* src = reinterpret_cast<float4*>(p.yacc + ((size_t)r * B + b) * d + tid * 8);
+        const float4 a0 = __ldcg(src), a1 = __ldcg(src + 1);
+        v[b][0] = make_float4(v[b][0].x + a0.x, v[b][0].y + a0.y, v[b][0].z + a0.z, v[b][0].w + a0.w);
+        v[b][1] = make_float4(v[b][1].x + a1.x, v[b][1].y + a1.y, v[b][1].z + a1.z, v[b][1].w + a1.w);
+        __stcg(src, make_float4(0.f, 0.f, 0.f, 0.f));
+        __stcg(src + 1, make_float4(0.f, 0.f, 0.f, 0.f));
+      }
+    }
+    const float4 v0 = v[b][0], v1 = v[b][1];
+    sq[b] = ((v0.x * v0.x + v0.y * v0.y) + (v0.z * v0.z + v0.w * v0.w)) +
+            ((v1.x * v1.x + v1.y * v1.y) + (v1.z * v1.z + v1.w * v1.w));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sq[b] += __shfl_xor_sync(0xffffffffu, sq[b], off);
+    if (lane == 0) ss[b * 32 + warp] = sq[b];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int b = 0; b < B; ++b) {
+    float rinv = 1.f;
+    if (p.rmsnorm) {
+      float t = 0.f;
+      for (int w = 0; w < nwarps; ++w) t += ss[b * 32 + w];
+      rinv = rsqrtf(t / (float)d + 1e-6f);
+    }
+    if (tid < d / 8) {
+      const float4 v0 = v[b][0], v1 = v[b][1];
+      __half2* yo = reinterpret_cast<__half2*>(p.y + (size_t)b * d + tid * 8);
+      yo[0] = __floats2half2_rn(v0.x * rinv, v0.y * rinv);
+      yo[1] = __floats2half2_rn(v0.z * rinv, v0.w * rinv);
+      yo[2] = __floats2half2_rn(v1.x * rinv, v1.y * rinv);
+      yo[3] = __floats2half2_rn(v1.z * rinv, v1.w * rinv);
+    }
+  }
+  if (tid == 0) p.ctrl->gdone = 0;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -687,115 +887,17 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_up_kernel(DecodeParam
 
   int4* ent = reinterpret_cast<int4*>(usm + L.off_ent);  // [unit][16] kept columns
   const int NL = dec_lanes(nsb);
+  const UpShared S{full, empty, vfull, vfree, &m->abort, m->pend, m->vbuf, m->ucnt, ring, xs, vpart, xg, grp,
+                   ent, L.strip, SU, nsb, nullptr};
   if (warp > NL * nsb) {
-    // ---- finalize warps, one per unit lane: each unit once all its superblock
-    // partials are in; its kept columns go to the unit's 16 entries
-    const int fl = warp - NL * nsb - 1;
-    int g = (u0 + fl) / MT, mt = (u0 + fl) - g * MT, cur_g = -1;
-    float thr = 0.f;
-    for (int j = fl; j < n; j += NL) {
-      const int slot = j & (kDecNV - 1);
-      if (!__all_sync(0xffffffffu, mbar_wait(&vfull[slot], (j >> 2) & 1))) {
-        if (lane == 0) dec_fail(p, &m->abort);
-        break;
-      }
-      if (g != cur_g) {
-        int el;
-        const ExpertSet& es = dec_set(p, grp[g].expert, el);
-        thr = es.thr[el];
-        cur_g = g;
-      }
-      const int cnt = dec_finalize<B>(p, vpart + (size_t)slot * nsb * 32, nsb, grp[g], g, mt, thr,
-                                      m->vbuf[slot], ent + (size_t)j * 16);
-      if (lane == 0) m->ucnt[j] = cnt;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&vfree[slot]);
-      mt += NL;
-      while (mt >= MT) {
-        mt -= MT;
-        ++g;
-      }
-    }
+    // ---- finalize warps, one per unit lane
+    dec_finalize_units<B>(p, S, warp - NL * nsb - 1, NL, u0, n, MT);
   } else if (warp == NL * nsb) {
     // ---- producer warp: the strips of this CTA's units, in order
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      int s = 0, ph = 0, g = u0 / MT, mt = u0 - g * MT;
-      for (int j = 0; j < n; ++j) {
-        if (j >= SU && !mbar_wait(&empty[s], ph ^ 1)) {
-          dec_fail(p, &m->abort);
-          break;
-        }
-        if (vload(&m->abort)) break;
-        int el;
-        const ExpertSet& es = dec_set(p, grp[g].expert, el);
-        m->pend[s] = j + 1;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)L.strip);
-        bulk_g2s(ring + (size_t)s * L.strip, es.up + (size_t)el * es.up_stride + (size_t)mt * L.strip,
-                 (uint32_t)L.strip, &full[s], pol);
-        if (++s == SU) {
-          s = 0;
-          ph ^= 1;
-        }
-        if (++mt == MT) {
-          mt = 0;
-          ++g;
-        }
-      }
-    }
+    if (lane == 0) dec_issue_strips(p, S, u0, n, MT);
   } else {
-    // ---- up warps: unit lane ug (units j = ug, ug + 2, ...), superblock sb
-    const int uw = warp, ug = uw / nsb, sb = uw % nsb;
-    const int ng = min(8, (d - sb * kSuper) / kGroup);
-    float* xgw = xg + uw * 16;
-    uint32_t xr[B][4][2];
-    int cur_g = -1;
-    // stage s = j % SU with full-barrier parity ph = (j / SU) & 1, and unit u = u0 + j as
-    // (group g, M-tile mt), all advanced by 2 units per iteration without divisions
-    int s = ug % SU, ph = (ug / SU) & 1;
-    int g = (u0 + ug) / MT, mt = (u0 + ug) - g * MT;
-    for (int j = ug; j < n; j += NL) {
-      const int slot = j & (kDecNV - 1);
-      const bool ab = vload(&m->abort) != 0;
-      bool ok = __all_sync(0xffffffffu, !ab && mbar_wait(&full[s], ph));
-      if (!ok) {
-        if (!ab && lane == 0) dec_fail(p, &m->abort);
-        break;
-      }
-      if (g != cur_g) {
-        dec_up_setup<B>(xs, d, grp[g], sb, ng, xr, xgw);
-        cur_g = g;
-      }
-      uint4 w[4];
-      uint32_t sz[B][2][2];
-      dec_load_block<B>(ring + (size_t)s * L.strip + (size_t)sb * kBlkBytes, w, sz);
-      __syncwarp();
-      if (lane == 0) {
-        if (sb == 0) m->pend[s] = 0;
-        mbar_arrive(&empty[s]);  // release: the copies above are done before the stage is reused
-      }
-      float vacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-      dec_phases<B, 0>(w, xr, sz, xgw, ng, vacc);
-      // the slot's previous unit must have been finalized
-      if (j >= kDecNV &&
-          !__all_sync(0xffffffffu, mbar_wait(&vfree[slot], ((j >> 2) - 1) & 1))) {
-        if (lane == 0) dec_fail(p, &m->abort);
-        break;
-      }
-      vpart[((size_t)slot * nsb + sb) * 32 + lane] = make_float4(vacc[0][0], vacc[0][1], vacc[1][0], vacc[1][1]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&vfull[slot]);
-      s += NL;
-      if (s >= SU) {
-        s -= SU;
-        ph ^= 1;
-      }
-      mt += NL;
-      while (mt >= MT) {
-        mt -= MT;
-        ++g;
-      }
-    }
+    // ---- up warps
+    dec_up_units<B>(p, S, NL, u0, n, MT);
   }
   __syncthreads();
   // this CTA's list: the units' kept columns in unit order
@@ -1150,52 +1252,519 @@ __global__ void __launch_bounds__(MAXT, 1) decode_gather_kernel(DecodeParams p) 
     m->last = old == gridDim.x - 1;
   }
   __syncthreads();
-  if (m->last) {
-    float* ss = red;  // [B][32]
-    float4 v[B][2];
-    float sq[B];
-#pragma unroll
-    for (int b = 0; b < B; ++b) {
-      v[b][0] = v[b][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (tid < d / 8) {
-#pragma unroll
-        for (int r = 0; r < kDecYRep; ++r) {
-          const float4* src = reinterpret_cast<const float4*>(p.yacc + ((size_t)r * B + b) * d + tid * 8);
-          const float4 a0 = __ldcg(src), a1 = __ldcg(src + 1);
-          v[b][0] = make_float4(v[b][0].x + a0.x, v[b][0].y + a0.y, v[b][0].z + a0.z, v[b][0].w + a0.w);
-          v[b][1] = make_float4(v[b][1].x + a1.x, v[b][1].y + a1.y, v[b][1].z + a1.z, v[b][1].w + a1.w);
-        }
-      }
-      const float4 v0 = v[b][0], v1 = v[b][1];
-      sq[b] = ((v0.x * v0.x + v0.y * v0.y) + (v0.z * v0.z + v0.w * v0.w)) +
-              ((v1.x * v1.x + v1.y * v1.y) + (v1.z * v1.z + v1.w * v1.w));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sq[b] += __shfl_xor_sync(0xffffffffu, sq[b], off);
-      if (lane == 0) ss[b * 32 + warp] = sq[b];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int b = 0; b < B; ++b) {
-      float rinv = 1.f;
-      if (p.rmsnorm) {
-        float t = 0.f;
-        for (int w = 0; w < L.nwarps; ++w) t += ss[b * 32 + w];
-        rinv = rsqrtf(t / (float)d + 1e-6f);
-      }
-      if (tid < d / 8) {
-        const float4 v0 = v[b][0], v1 = v[b][1];
-        __half2* yo = reinterpret_cast<__half2*>(p.y + (size_t)b * d + tid * 8);
-        yo[0] = __floats2half2_rn(v0.x * rinv, v0.y * rinv);
-        yo[1] = __floats2half2_rn(v0.z * rinv, v0.w * rinv);
-        yo[2] = __floats2half2_rn(v1.x * rinv, v1.y * rinv);
-        yo[3] = __floats2half2_rn(v1.z * rinv, v1.w * rinv);
-      }
-    }
-  }
+  if (m->last) dec_last_cta<B>(p, L.nwarps, red);
   if (m->abort && tid == 0) {
     // wait (bounded) for the rows still in flight before the CTA exits
     for (int i = max(m->consumed, m->issued - SR); i < m->issued; ++i)
       (void)mbar_wait(&full[i % SR], (i / SR) & 1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One-kernel decode layer (d <= 4096).  The up kernel's routing and up phase, then, in
+// the same CTA, the gather of exactly the kept columns of this CTA's own units: the
+// producer lane streams a unit's kept rows as soon as its finalize warp has published
+// them (interleaved with the remaining strips, which keep priority), and the compute
+// warps turn from superblocks to rows when their units are done.  There is no grid-wide
+// step between the up projection and the gather: a CTA never waits for another one.
+// Each CTA adds its share of y into the fp32 accumulator, and the last one to finish
+// rounds y (after the RMSNorm of stacked layers), leaving the accumulator zeroed.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kHB = 4;  // gather batches in flight between the gather warps and the h warp
+
+// Sums of v[q][b] over the warp's lanes by recursive halving (one value kept per lane
+// and round): for one token lane 8q + i ends with row q, for two tokens lane 8q + 4b + i
+// with (row q, token b).
+template <int B>
+__device__ __forceinline__ float warp_sum_rows(const float (&v)[kDecRows][B]) {
+  static_assert(kDecRows == 4, "four rows per batch");
+  const int lane = threadIdx.x & 31;
+  const bool u16 = (lane & 16) != 0, u8 = (lane & 8) != 0;
+  if constexpr (B == 1) {
+    const float a0 = (u16 ? v[2][0] : v[0][0]) + __shfl_xor_sync(0xffffffffu, u16 ? v[0][0] : v[2][0], 16);
+    const float a1 = (u16 ? v[3][0] : v[1][0]) + __shfl_xor_sync(0xffffffffu, u16 ? v[1][0] : v[3][0], 16);
+    float c = (u8 ? a1 : a0) + __shfl_xor_sync(0xffffffffu, u8 ? a0 : a1, 8);
+    c += __shfl_xor_sync(0xffffffffu, c, 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    return c;
+  } else {
+    const bool u4 = (lane & 4) != 0;
+    // rows (u16 ? 2 : 0) + {0, 1}, both tokens
+    const float a0 = (u16 ? v[2][0] : v[0][0]) + __shfl_xor_sync(0xffffffffu, u16 ? v[0][0] : v[2][0], 16);
+    const float a1 = (u16 ? v[2][1] : v[0][1]) + __shfl_xor_sync(0xffffffffu, u16 ? v[0][1] : v[2][1], 16);
+    const float a2 = (u16 ? v[3][0] : v[1][0]) + __shfl_xor_sync(0xffffffffu, u16 ? v[1][0] : v[3][0], 16);
+    const float a3 = (u16 ? v[3][1] : v[1][1]) + __shfl_xor_sync(0xffffffffu, u16 ? v[1][1] : v[3][1], 16);
+    // row (u16 ? 2 : 0) + (u8 ? 1 : 0), both tokens
+    const float c0 = (u8 ? a2 : a0) + __shfl_xor_sync(0xffffffffu, u8 ? a0 : a2, 8);
+    const float c1 = (u8 ? a3 : a1) + __shfl_xor_sync(0xffffffffu, u8 ? a1 : a3, 8);
+    // token u4
+    float e = (u4 ? c1 : c0) + __shfl_xor_sync(0xffffffffu, u4 ? c0 : c1, 4);
+    e += __shfl_xor_sync(0xffffffffu, e, 2);
+    e += __shfl_xor_sync(0xffffffffu, e, 1);
+    return e;
+  }
+}
+
+struct LyMisc {
+  int abort;
+  int G;
+  int last;                     // this CTA finished last
+  int rissued;                  // rows issued into the row ring (the end mark not counted)
+  int rconsumed;                // rows whose stages the gather warps have released
+  int pend[kDecMaxSu];          // strip in flight in the stage (issue index + 1) or 0
+  int tidx[2][kMaxTok];
+  float tw[2][kMaxTok];
+  float vbuf[kDecNV][16 * 2];
+  int ucnt[kDecMaxUnits];       // kept columns of unit j once it is finalized, -1 before
+  int tmap[kDecMaxG][2];        // group token of batch token b, -1 if none
+  float gw[kDecMaxG][2];        // its combine weight
+};
+
+struct LyLayoutD {
+  int nsb, nup, ngw, nc, nwarps, su, sr;
+  size_t strip, row;
+  size_t off_bar, off_misc, off_nbs, off_ring, off_rring, off_rdesc, off_bdesc, off_x, off_vpart, off_xg,
+      off_grp, off_lred, off_ent, off_red, total;
+};
+
+// warps: nc = max(up warps, gather warps) compute warps, then the strip producer, one
+// finalize warp per unit lane, and the row producer.  umax: units per CTA, at most.
+__host__ __device__ inline LyLayoutD ly_layout_d(int d, int B, int E, int su, int sr, int umax) {
+  LyLayoutD L;
+  L.nsb = n_superblocks(d);
+  L.nup = dec_lanes(L.nsb) * L.nsb;
+  L.ngw = d / 256;
+  L.nc = L.nup > L.ngw ? L.nup : L.ngw;
+  L.nwarps = L.nc + 1 + dec_lanes(L.nsb) + 1;
+  L.su = su;
+  L.sr = sr;
+  L.strip = (size_t)L.nsb * kBlkBytes;
+  L.row = (size_t)4 * d;
+  size_t o = 0;
+  L.off_bar = o;
+  o += 8 * (size_t)(2 * kDecMaxSu + 2 * kDecNV + 2 * kDecMaxSr + 2 * kHB + 1 + kDecMaxUnits);
+  o = al16(o);
+  L.off_misc = o;
+  o += al16(sizeof(LyMisc));
+  L.off_nbs = o;
+  o += al16(4 * (size_t)kHB);
+  o = (o + 127) & ~(size_t)127;
+  L.off_ring = o;
+  o += L.strip * su;
+  L.off_rring = o;
+  o += L.row * sr;
+  L.off_rdesc = o;
+  o += 16 * (size_t)kDecMaxSr;
+  L.off_bdesc = o;
+  o += 16 * (size_t)(kHB * kDecRows);
+  L.off_x = o;
+  o += al16((size_t)B * d * 2);
+  L.off_vpart = o;
+  o += (size_t)kDecNV * L.nsb * 32 * 16;
+  L.off_xg = o;
+  o += (size_t)2 * L.nsb * 16 * 4;
+  L.off_grp = o;
+  o += al16(sizeof(GroupDesc) * kDecMaxG);
+  L.off_lred = o;
+  o += al16((size_t)L.nwarps * 2 * E * 4);
+  L.off_ent = o;
+  o += (size_t)umax * 16 * 16;
+  L.off_red = o;
+  o += (size_t)kHB * kDecRows * 2 * (kDecMaxGw + 1) * 4;
+  L.total = o;
+  return L;
+}
+
+
+}  // namespace
+
+template <int B>
+__global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t lsm[];
+  const int d = p.d, SU = p.su, SR1 = p.sr;
+  const LyLayoutD L = ly_layout_d(d, B, p.routed.E, SU, SR1, p.umax);
+  // row ring: SR1 stages of its own, then, once every up warp is done with the strip
+  // ring, as many more stages in the strip ring's space
+  const int SR = min(kDecMaxSr, SR1 + (int)(L.strip * SU / L.row));
+  uint64_t* full = reinterpret_cast<uint64_t*>(lsm + L.off_bar);
+  uint64_t* empty = full + kDecMaxSu;
+  uint64_t* vfull = empty + kDecMaxSu;
+  uint64_t* vfree = vfull + kDecNV;
+  uint64_t* rfull = vfree + kDecNV;
+  uint64_t* rempty = rfull + kDecMaxSr;
+  uint64_t* dotsb = rempty + kDecMaxSr;  // [kHB] a batch's dot partials are in (gather warps)
+  uint64_t* hrdy = dotsb + kHB;          // [kHB] its h values are in (the h warp)
+  uint64_t* updone = hrdy + kHB;         // every up warp is done with the strip ring
+  uint64_t* ufin = updone + 1;           // [kDecMaxUnits] single-use: unit j finalized
+  LyMisc* m = reinterpret_cast<LyMisc*>(lsm + L.off_misc);
+  uint8_t* ring = lsm + L.off_ring;
+  uint8_t* rring = lsm + L.off_rring;
+  // stage s of the row ring
+  auto rstage = [&](int s) -> uint8_t* {
+    return s < SR1 ? rring + (size_t)s * L.row : ring + (size_t)(s - SR1) * L.row;
+  };
+  int4* rdesc = reinterpret_cast<int4*>(lsm + L.off_rdesc);  // [SR] descriptor of each row stage
+  int4* bdesc = reinterpret_cast<int4*>(lsm + L.off_bdesc);  // [kHB][kDecRows] descriptors of a batch's rows
+  __half* xs = reinterpret_cast<__half*>(lsm + L.off_x);
+  float4* vpart = reinterpret_cast<float4*>(lsm + L.off_vpart);
+  float* xg = reinterpret_cast<float*>(lsm + L.off_xg);
+  GroupDesc* grp = reinterpret_cast<GroupDesc*>(lsm + L.off_grp);
+  float* lred = reinterpret_cast<float*>(lsm + L.off_lred);
+  int4* ent = reinterpret_cast<int4*>(lsm + L.off_ent);
+  float* red = reinterpret_cast<float*>(lsm + L.off_red);
+  float* part = red;                                       // [kHB][kDecRows][2][kDecMaxGw] dot partials
+  float* hbuf = red + kHB * kDecRows * 2 * kDecMaxGw;      // [kHB][kDecRows][2] h values
+  int* nbs = reinterpret_cast<int*>(lsm + L.off_nbs);      // [kHB] rows of a batch
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nsb = L.nsb, NL = dec_lanes(nsb), nup = L.nup, ngw = L.ngw, NC = L.nc;
+  const int nthreads = L.nwarps * 32, nct = ngw * 32;
+  if (tid == 0) {
+    for (int s = 0; s < SU; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nsb);
+    }
+    for (int v = 0; v < kDecNV; ++v) {
+      mbar_init(&vfull[v], nsb);
+      mbar_init(&vfree[v], 1);
+    }
+    for (int s = 0; s < SR; ++s) {
+      mbar_init(&rfull[s], 1);
+      mbar_init(&rempty[s], ngw);
+    }
+    for (int h = 0; h < kHB; ++h) {
+      mbar_init(&dotsb[h], ngw);
+      mbar_init(&hrdy[h], 1);
+    }
+    mbar_init(updone, nup);
+    fence_barrier_init();
+    m->abort = 0;
+    m->rissued = 0;
+    m->rconsumed = 0;
+    for (int s = 0; s < kDecMaxSu; ++s) m->pend[s] = 0;
+  }
+  for (int j = tid; j < kDecMaxUnits; j += nthreads) {
+    m->ucnt[j] = -1;
+    mbar_init(&ufin[j], 1);
+  }
+  if (tid < kDecMaxUnits) fence_barrier_init();
+  for (int i = tid; i < kHB * kDecRows * 2 * (kDecMaxGw + 1); i += nthreads) red[i] = 0.f;
+  // the router weight is not written by the previous kernel: load this thread's rows
+  // of it before waiting
+  const RouteSplit rt = route_split(p.routed.E, nthreads);
+  uint4 wv[kRouteRows];
+  route_prefetch(p, rt, wv);
+  __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+  for (int i = tid; i < B * d / 8; i += nthreads)
+    reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
+  __syncthreads();
+  dec_route<B>(p, nthreads, rt, wv, xs, lred, m, grp);
+  const int G = m->G;
+  if (tid < G * 2) {
+    const int g = tid >> 1, b = tid & 1;
+    const GroupDesc& gd = grp[g];
+    int t_of_b = -1;
+    float w = 0.f;
+    for (int t = 0; t < gd.n_tok; ++t)
+      if (gd.tok[t] == b) {
+        t_of_b = t;
+        w = gd.w[t];
+      }
+    m->tmap[g][b] = t_of_b;
+    m->gw[g][b] = w;
+  }
+  __syncthreads();
+  const int MT = p.f / kMTile;
+  const int U = G * MT;
+  const int u0 = (int)muldiv(U, blockIdx.x, gridDim.x), u1 = (int)muldiv(U, blockIdx.x + 1, gridDim.x);
+  const int n = u1 - u0;
+  const UpShared S{full, empty, vfull, vfree, &m->abort, m->pend, m->vbuf, m->ucnt, ring, xs, vpart, xg, grp,
+                   ent, L.strip, SU, nsb, ufin};
+
+  if (warp == NC) {
+    // ---- strip producer: the packed strips of this CTA's units, in order
+    if (lane == 0) dec_issue_strips(p, S, u0, n, MT);
+  } else if (warp == NC + NL + 1) {
+    // ---- row producer: the kept rows of each unit once its finalize warp has published
+    // them, in unit order, then the end mark (a row stage without data whose descriptor
+    // column is -1).  A stage's first use: its own stages at once, those in the strip
+    // ring's space once the up phase is over; later uses: once the gather warps have
+    // released it.
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int rs = 0, rph = 0, issued = 0;
+      bool ok = true;
+      auto stage_wait = [&]() -> bool {
+        if (vload(&m->abort)) return false;
+        if (issued >= SR) return mbar_wait(&rempty[rs], rph ^ 1);
+        return rs < SR1 || mbar_wait(updone, 0);
+      };
+      for (int j = 0; j < n && ok; ++j) {
+        if (!mbar_wait(&ufin[j], 0)) {
+          ok = false;
+          break;
+        }
+        const int c = m->ucnt[j];
+        if (c == 0) continue;
+        // the unit's expert rows (every entry of a unit has the same group)
+        const int g = ent[j * 16].x >> 16;
+        int el;
+        const ExpertSet& es = dec_set(p, grp[g].expert, el);
+        const size_t rsb = (size_t)es.rs * 2;
+        const uint8_t* gbase = reinterpret_cast<const uint8_t*>(es.gate_t + (size_t)el * es.f * es.rs);
+        const uint8_t* dbase = reinterpret_cast<const uint8_t*>(es.down + (size_t)el * es.f * es.rs);
+        const bool inter = es.rs == 2 * d;
+        for (int r = 0; r < c; ++r) {
+          if (!stage_wait()) {
+            ok = false;
+            break;
+          }
+          const int4 e = ent[j * 16 + r];
+          const size_t off = (size_t)(e.x & 0xffff) * rsb;
+          uint8_t* st = rstage(rs);
+          rdesc[rs] = e;
+          mbar_arrive_expect_tx(&rfull[rs], (uint32_t)L.row);
+          if (inter) {
+            bulk_g2s(st, gbase + off, (uint32_t)(4 * d), &rfull[rs], pol);
+          } else {
+            bulk_g2s(st, gbase + off, (uint32_t)(2 * d), &rfull[rs], pol);
+            bulk_g2s(st + 2 * d, dbase + off, (uint32_t)(2 * d), &rfull[rs], pol);
+          }
+          ++issued;
+          if (++rs == SR) {
+            rs = 0;
+            rph ^= 1;
+          }
+        }
+      }
+      if (ok && stage_wait()) {
+        rdesc[rs] = make_int4(-1, 0, 0, 0);
+        mbar_arrive(&rfull[rs]);
+      } else {
+        dec_fail(p, &m->abort);
+      }
+      m->rissued = issued;
+    }
+  } else if (warp > NC) {
+    // ---- finalize warps, one per unit lane; then the first one forms the gather's h
+    dec_finalize_units<B>(p, S, warp - NC - 1, NL, u0, n, MT);
+    if (warp == NC + 1) {
+      // batch k: sum the gather warps' dot partials of each (row, token), then
+      // h = SiLU(sum) * v * router weight, for lane q * 2 + b
+      for (int k = 0;; ++k) {
+        const int hs = k & (kHB - 1);
+        if (vload(&m->abort) || !__all_sync(0xffffffffu, mbar_wait(&dotsb[hs], (k / kHB) & 1))) break;
+        const int nb = vload(&nbs[hs]);
+        if (lane < kDecRows * 2) {
+          const int q = lane >> 1, b = lane & 1;
+          float hq = 0.f;
+          if (q < nb && b < B) {
+            const int4 e = bdesc[hs * kDecRows + q];
+            const int g = e.x >> 16;
+            const int t = m->tmap[g][b];
+            if (t >= 0) {
+              const float4* pr = reinterpret_cast<const float4*>(part + ((hs * kDecRows + q) * 2 + b) * kDecMaxGw);
+              const float4 p0 = pr[0], p1 = pr[1], p2 = pr[2], p3 = pr[3];  // unused slots hold 0
+              float gs = (((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w))) +
+                         (((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w)));
+              if (ngw > 16) {
+                const float4 p4 = pr[4], p5 = pr[5];
+                gs += ((p4.x + p4.y) + (p4.z + p4.w)) + ((p5.x + p5.y) + (p5.z + p5.w));
+              }
+              hq = silu_fast(gs) * __int_as_float(t == 0 ? e.y : e.z) * m->gw[g][b];
+            }
+          }
+          hbuf[hs * kDecRows * 2 + lane] = hq;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hrdy[hs]);
+        if (nb < kDecRows) break;
+      }
+    }
+  } else {
+    // ---- compute warps: the superblocks of this CTA's units, then its kept rows
+    if (warp < nup) {
+      dec_up_units<B>(p, S, NL, u0, n, MT);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(updone);
+    }
+    if (warp < ngw) {
+      float acc[B][8];
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[b][e] = 0.f;
+      // this thread's 8 hidden elements of the tokens, fp16 pairs
+      uint32_t xh[B][4];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const uint4 xv = reinterpret_cast<const uint4*>(xs + (size_t)b * d)[tid];
+        xh[b][0] = xv.x;
+        xh[b][1] = xv.y;
+        xh[b][2] = xv.z;
+        xh[b][3] = xv.w;
+      }
+      int s0 = 0, ph0 = 0;  // stage and full-barrier parity of the batch's first row
+      // acc += h of batch k * this thread's slices of its down rows, once the h warp has
+      // published that h
+      auto apply = [&](int k, int nbq, const uint4 (&dn)[kDecRows]) -> bool {
+        const int hs = k & (kHB - 1);
+        if (!__all_sync(0xffffffffu, mbar_wait(&hrdy[hs], (k / kHB) & 1))) return false;
+        const float* hb = hbuf + hs * kDecRows * 2;
+#pragma unroll
+        for (int q = 0; q < kDecRows; ++q) {
+          if (q < nbq) {
+            const float2 hq = *reinterpret_cast<const float2*>(hb + q * 2);
+            const float hv[2] = {hq.x, hq.y};
+            const __half2* dh = reinterpret_cast<const __half2*>(&dn[q]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 df = __half22float2(dh[e]);
+#pragma unroll
+              for (int b = 0; b < B; ++b) {
+                acc[b][2 * e] = fmaf(hv[b], df.x, acc[b][2 * e]);
+                acc[b][2 * e + 1] = fmaf(hv[b], df.y, acc[b][2 * e + 1]);
+              }
+            }
+          }
+        }
+        return true;
+      };
+      // batch k of up to kDecRows rows: dot partials of this warp into slot k % kHB, then
+      // the previous batch applied; no warp waits for another one.  Returns the batch's
+      // rows (fewer than kDecRows: the end mark was reached), or -1 on a failure.
+      auto step = [&](int k, uint4 (&dcur)[kDecRows], const uint4 (&dprev)[kDecRows], int prev_nb) -> int {
+        const int hs = k & (kHB - 1);
+        int st[kDecRows];
+        bool ok = !vload(&m->abort);
+        int nb = 0;
+#pragma unroll
+        for (int q = 0; q < kDecRows; ++q) {
+          int sq = s0 + q, pq = ph0;
+          if (sq >= SR) {
+            sq -= SR;
+            pq ^= 1;
+          }
+          st[q] = sq;
+          if (ok && nb == q) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&rfull[sq], pq));
+            if (ok && rdesc[sq].x >= 0) nb = q + 1;
+          }
+        }
+        if (!ok) {
+          if (lane == 0) {
+            dec_fail(p, &m->abort);
+            mbar_arrive(&dotsb[hs]);
+          }
+          return -1;
+        }
+        // warp 0 hands the batch's descriptors to the h warp (the stages are released
+        // below, before it reads them)
+        if (warp == 0) {
+          if (lane < nb) {
+            int sq = s0 + lane;
+            if (sq >= SR) sq -= SR;
+            bdesc[hs * kDecRows + lane] = rdesc[sq];
+          }
+          if (lane == 0) nbs[hs] = nb;
+        }
+        float dot[kDecRows][B];
+#pragma unroll
+        for (int q = 0; q < kDecRows; ++q) {
+#pragma unroll
+          for (int b = 0; b < B; ++b) dot[q][b] = 0.f;
+          if (q < nb) {
+            const uint4 gr = reinterpret_cast<const uint4*>(rstage(st[q]))[tid];
+            const uint32_t gw4[4] = {gr.x, gr.y, gr.z, gr.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+#pragma unroll
+              for (int b = 0; b < B; ++b) {
+                dot[q][b] = fma_f16<0, 0>(xh[b][e], gw4[e], dot[q][b]);
+                dot[q][b] = fma_f16<1, 1>(xh[b][e], gw4[e], dot[q][b]);
+              }
+            }
+          }
+        }
+        // this thread's slice of every down row, then the stages can be refilled at once
+#pragma unroll
+        for (int q = 0; q < kDecRows; ++q)
+          dcur[q] = q < nb ? reinterpret_cast<const uint4*>(rstage(st[q]) + 2 * d)[tid]
+                           : make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        if (lane == 0) {
+          for (int q = 0; q < nb; ++q) mbar_arrive(&rempty[st[q]]);
+          if (warp == 0) m->rconsumed += nb;
+        }
+        // the warp's sums by recursive halving: lane 8q (+ 4b for two tokens) ends with
+        // (row q, token b)
+        const float r = warp_sum_rows<B>(dot);
+        if ((lane & (B == 1 ? 7 : 3)) == 0) {
+          const int q = lane >> 3, b = B == 1 ? 0 : (lane >> 2) & 1;
+          part[((hs * kDecRows + q) * 2 + b) * kDecMaxGw + warp] = r;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dotsb[hs]);
+        if (k > 0 && !apply(k - 1, prev_nb, dprev)) {
+          if (lane == 0) dec_fail(p, &m->abort);
+          return -1;
+        }
+        s0 += nb;
+        if (s0 >= SR) {
+          s0 -= SR;
+          ph0 ^= 1;
+        }
+        return nb;
+      };
+      uint4 dA[kDecRows], dB[kDecRows];
+      int k = 0, nb = kDecRows, last_nb = 0;
+      for (;;) {
+        nb = step(k, dA, dB, last_nb);
+        if (nb < 0) break;
+        last_nb = nb;
+        ++k;
+        if (nb < kDecRows) break;
+        nb = step(k, dB, dA, last_nb);
+        if (nb < 0) break;
+        last_nb = nb;
+        ++k;
+        if (nb < kDecRows) break;
+      }
+      // the last batch (k - 1), whose rows' down slices are in dA if k - 1 is even
+      if (nb >= 0 && !apply(k - 1, last_nb, ((k - 1) & 1) ? dB : dA) && lane == 0) dec_fail(p, &m->abort);
+      // this CTA's share of y, added in fp32 into copy blockIdx.x % kDecYRep of the
+      // accumulator (the order of the CTAs' additions varies)
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        float* dst = p.yacc + ((size_t)(blockIdx.x % kDecYRep) * B + b) * d + tid * 8;
+        red_add_v4(dst, acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
+        red_add_v4(dst + 4, acc[b][4], acc[b][5], acc[b][6], acc[b][7]);
+      }
+    }
+  }
+  // the last CTA to finish rounds y: the barrier orders every thread's additions before
+  // thread 0's count, an acq_rel atomic whose release publishes them; in the last CTA its
+  // acquire, followed by the barrier, orders the reads after every other CTA's additions
+  __syncthreads();
+  if (tid == 0) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(&p.ctrl->gdone) : "memory");
+    m->last = old == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (m->last) dec_last_cta<B>(p, L.nwarps, red);
+  if (m->abort && tid == 0) {
+    // wait (bounded) for the strips and rows still in flight before the CTA exits
+    for (int s = 0; s < SU; ++s) {
+      const int q = m->pend[s];
+      if (q > 0) (void)mbar_wait(&full[s], ((q - 1) / SU) & 1);
+    }
+    for (int i = max(m->rconsumed, m->rissued - SR); i < m->rissued; ++i)
+      (void)mbar_wait(&rfull[i % SR], (i / SR) & 1);
   }
 }
 
@@ -1225,6 +1794,10 @@ int decode_plan(int B, int d, int E, int umax, int list_cap, int P, int smem_opt
   size_t fixed = u0.total - al16(u0.ring);
   int s = (int)(((size_t)smem_optin - fixed - 256) / strip);
   if (s > kDecMaxSu) s = kDecMaxSu;
+  // a multiple of the unit lanes: stage s then only ever holds strips of lane s % lanes,
+  // so a warp's wait on a stage is always for the phase after the one it last waited for
+  // (a parity wait cannot tell a phase from the one two back)
+  s -= s % dec_lanes(u0.nsb);
   if (s < 2 || up_layout_d(d, B, E, s, umax).total > (size_t)smem_optin) return 0;
   su = s;
   const GaLayoutD g0 = ga_layout_d(d, 0, list_cap, P);
@@ -1284,6 +1857,46 @@ cudaError_t launch_decode_gather(const DecodeParams& p, cudaStream_t st, bool pd
   if (L.nwarps * 32 <= kGaSmallThreads)
     return p.B == 1 ? launch_ga<1, kGaSmallThreads>(cfg, p, L.total) : launch_ga<2, kGaSmallThreads>(cfg, p, L.total);
   return p.B == 1 ? launch_ga<1, kGaThreads>(cfg, p, L.total) : launch_ga<2, kGaThreads>(cfg, p, L.total);
+}
+
+int decode_layer_plan(int B, int d, int E, int umax, int smem_optin, int& su, int& sr) {
+  su = sr = 0;
+  if (d > 4096) return 0;
+  const LyLayoutD z = ly_layout_d(d, B, E, 0, 0, umax);
+  if (z.nwarps * 32 > kUpRegThreads || z.total + 1024 > (size_t)smem_optin) return 0;
+  const size_t budget = (size_t)smem_optin - z.total - 256;
+  // strips: about 40 % of the ring space, rounded up to a multiple of the unit lanes (stage
+  // s then only ever holds strips of lane s % lanes, so a warp's wait on a stage is always
+  // for the phase after the one it last waited for: a parity wait cannot tell a phase from
+  // the one two back); rows: the rest
+  const int NL = dec_lanes(z.nsb);
+  int s = (int)(budget * 2 / 5 / z.strip);
+  s += (NL - s % NL) % NL;
+  if (s < 2 * NL) s = 2 * NL;
+  if (s > kDecMaxSu) s = kDecMaxSu - kDecMaxSu % NL;
+  if ((size_t)s * z.strip >= budget) return 0;
+  int r = (int)((budget - (size_t)s * z.strip) / z.row);
+  if (r > kDecMaxSr) r = kDecMaxSr;
+  if (r < kDecRows + 2) return 0;
+  if (ly_layout_d(d, B, E, s, r, umax).total > (size_t)smem_optin) return 0;
+  su = s;
+  sr = r;
+  return 1;
+}
+
+size_t decode_layer_smem(const DecodeParams& p) {
+  return ly_layout_d(p.d, p.B, p.routed.E, p.su, p.sr, p.umax).total;
+}
+
+cudaError_t launch_decode_layer(const DecodeParams& p, cudaStream_t st, bool pdl) {
+  const LyLayoutD L = ly_layout_d(p.d, p.B, p.routed.E, p.su, p.sr, p.umax);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_cfg(dim3(p.P), dim3(L.nwarps * 32), L.total, st, attr, pdl);
+  const void* fn = p.B == 1 ? (const void*)decode_layer_kernel<1> : (const void*)decode_layer_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+  if (e != cudaSuccess) return e;
+  if (p.B == 1) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<1>, p);
+  return cudaLaunchKernelEx(&cfg, decode_layer_kernel<2>, p);
 }
 
 }  // namespace sesg

@@ -121,6 +121,8 @@ int decode_units_max(int B, int f, int k, int n_shared, int P);
 int decode_plan(int B, int d, int E, int umax, int list_cap, int P, int smem_optin, int& su, int& sr);
 cudaError_t launch_decode_up(const DecodeParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_decode_gather(const DecodeParams& p, cudaStream_t st, bool pdl);
+int decode_layer_plan(int B, int d, int E, int umax, int smem_optin, int& su, int& sr);
+cudaError_t launch_decode_layer(const DecodeParams& p, cudaStream_t st, bool pdl);
 // fetch.cu
 cudaError_t launch_decode_fetch(const DecodeParams& p, cudaStream_t st, bool pdl);
 

@@ -396,19 +396,20 @@ def test_layer_interleaved_gate_down(B):
 
 
 def test_layer_path_selection():
-    """One or two tokens with 8/16/32/64 routed experts and d <= 6144 take the decode
-    kernels; other shapes take the general path."""
+    """One or two tokens with 8/16/32/64 routed experts take the decode path: one kernel
+    up to d = 4096, two up to d = 6144; other shapes take the general path."""
     def layer(d, f, E):
         de = synth.experts(E, d, f, 50)
         ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(),
                                     torch.zeros(E, dtype=torch.float32).cuda())
         return ses.Layer(synth.router(d, E, 50).cuda(), ex, 2)
     small = layer(1024, 256, 8)
-    assert ses.layer_path(small, 1) == "decode"
-    assert ses.layer_path(small, 2) == "decode"
+    assert ses.layer_path(small, 1) == "decode_fused"
+    assert ses.layer_path(small, 2) == "decode_fused"
     assert ses.layer_path(small, 3) == "general"
-    assert ses.layer_path(layer(1024, 256, 64), 1) == "decode"
+    assert ses.layer_path(layer(1024, 256, 64), 1) == "decode_fused"
     assert ses.layer_path(layer(1024, 256, 128), 1) == "general"
+    assert ses.layer_path(layer(4096, 256, 8), 2) == "decode_fused"
     assert ses.layer_path(layer(6144, 256, 8), 1) == "decode"
     assert ses.layer_path(layer(6400, 256, 8), 1) == "general"
 
@@ -494,6 +495,30 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable():
     assert lib.moe_selftest_wait_timeout(ws.ptr(), ws.nbytes, 0, stream) == -1
 
 
+@pytest.mark.parametrize("B", [1, 2])
+def test_decode_up_projection_repeatable(B):
+    """v = x W~^up is formed in a fixed order on the decode path, so calls in a row must
+    give identical bits.  At the Mixtral-8x7B shape (two unit lanes sharing the packed-strip
+    ring) this catches a strip read before its copy landed: a parity wait on a ring stage
+    cannot tell a phase from the one two back, so no lane may skip a phase of a stage."""
+    d, f, E, k = 4096, 14336, 8, 2
+    de = synth.experts(E, d, f, 30, device="cuda")
+    ex = ses.Experts.from_dense(de.w_up, de.gate_t, de.down, torch.full((E,), 0.9, device="cuda"),
+                                interleave=True)
+    del de
+    layer = ses.Layer(synth.router(d, E, 30, device="cuda"), ex, k, True)
+    x = synth.tokens(B, d, 30, device="cuda")
+    ws = ses.Workspace(ses.layer_workspace_bytes(layer, B))
+    _, dbg = ses.layer_decode(x, layer, rmsnorm=True, ws=ws, debug=True)
+    v0, m0 = dbg["v"].clone(), dbg["mask"].clone()
+    differ = 0
+    for _ in range(300):
+        _, dbg = ses.layer_decode(x, layer, rmsnorm=True, ws=ws, debug=True)
+        differ += int(not (torch.equal(dbg["v"], v0) and torch.equal(dbg["mask"], m0)))
+    assert ws.status() == 0
+    assert differ == 0, f"{differ} of 300 calls gave a different v or mask"
+
+
 def test_decode_repeated_calls_share_the_workspace():
     """Many calls in a row on one workspace (the decode kernels reset their accumulator
     and counters) give the same output up to the order of the fp32 additions."""
@@ -525,7 +550,7 @@ def test_decode_workspace_shared_across_shapes():
     for rep in range(3):
         for li, lay in enumerate(layers):
             for B in (2, 1):
-                assert ses.layer_path(lay, B) == "decode"
+                assert ses.layer_path(lay, B) == "decode_fused"
                 x = synth.tokens(B, lay.w_router.shape[0], 70 + 4 * rep + 2 * li + B).cuda()
                 got = ses.layer_decode(x, lay, ws=ws, rmsnorm=(B == 1)).clone()
                 fresh = ses.Workspace(ses.layer_workspace_bytes(lay, B))
