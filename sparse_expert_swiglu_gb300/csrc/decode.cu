@@ -30,6 +30,8 @@
 // rounding boundary).  Every wait is bounded; on expiry a CTA records
 // MOE_ERR_TIMEOUT, stops, and waits (bounded) for its copies in flight before it
 // exits.
+#include <type_traits>
+
 #include "params.cuh"
 
 namespace sesg {
@@ -1272,7 +1274,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_gather_kernel(DecodeParams p) 
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr int kHB = 4;  // gather batches in flight between the gather warps and the h warp
+constexpr int kHB = 4;   // gather batches in flight between the gather warps and the h warp
+constexpr int kHD = 64;  // row descriptors kept for the h warp (rows ahead of it: < SR + 3 kDecRows)
 
 // Sums of v[q][b] over the warp's lanes by recursive halving (one value kept per lane
 // and round): for one token lane 8q + i ends with row q, for two tokens lane 8q + 4b + i
@@ -1312,8 +1315,10 @@ struct LyMisc {
   int abort;
   int G;
   int last;                     // this CTA finished last
-  int rissued;                  // rows issued into the row ring (the end mark not counted)
+  int rissued;                  // rows issued into the row ring
   int rconsumed;                // rows whose stages the gather warps have released
+  int known;                    // rows of the units finalized so far (the row producer's count)
+  int allknown;                 // 1 once every unit is finalized (known is then final)
   int pend[kDecMaxSu];          // strip in flight in the stage (issue index + 1) or 0
   int tidx[2][kMaxTok];
   float tw[2][kMaxTok];
@@ -1326,8 +1331,8 @@ struct LyMisc {
 struct LyLayoutD {
   int nsb, nup, ngw, nc, nwarps, su, sr;
   size_t strip, row;
-  size_t off_bar, off_misc, off_nbs, off_ring, off_rring, off_rdesc, off_bdesc, off_x, off_vpart, off_xg,
-      off_grp, off_lred, off_ent, off_red, total;
+  size_t off_bar, off_misc, off_nbs, off_ring, off_rring, off_hdesc, off_x, off_vpart, off_xg, off_grp,
+      off_lred, off_ent, off_red, total;
 };
 
 // warps: nc = max(up warps, gather warps) compute warps, then the strip producer, one
@@ -1356,10 +1361,8 @@ __host__ __device__ inline LyLayoutD ly_layout_d(int d, int B, int E, int su, in
   o += L.strip * su;
   L.off_rring = o;
   o += L.row * sr;
-  L.off_rdesc = o;
-  o += 16 * (size_t)kDecMaxSr;
-  L.off_bdesc = o;
-  o += 16 * (size_t)(kHB * kDecRows);
+  L.off_hdesc = o;
+  o += 16 * (size_t)kHD;
   L.off_x = o;
   o += al16((size_t)B * d * 2);
   L.off_vpart = o;
@@ -1406,8 +1409,7 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
   auto rstage = [&](int s) -> uint8_t* {
     return s < SR1 ? rring + (size_t)s * L.row : ring + (size_t)(s - SR1) * L.row;
   };
-  int4* rdesc = reinterpret_cast<int4*>(lsm + L.off_rdesc);  // [SR] descriptor of each row stage
-  int4* bdesc = reinterpret_cast<int4*>(lsm + L.off_bdesc);  // [kHB][kDecRows] descriptors of a batch's rows
+  int4* hdesc = reinterpret_cast<int4*>(lsm + L.off_hdesc);  // [kHD] descriptor of row i at i % kHD (for the h warp)
   __half* xs = reinterpret_cast<__half*>(lsm + L.off_x);
   float4* vpart = reinterpret_cast<float4*>(lsm + L.off_vpart);
   float* xg = reinterpret_cast<float*>(lsm + L.off_xg);
@@ -1443,6 +1445,8 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
     m->abort = 0;
     m->rissued = 0;
     m->rconsumed = 0;
+    m->known = 0;
+    m->allknown = 0;
     for (int s = 0; s < kDecMaxSu; ++s) m->pend[s] = 0;
   }
   for (int j = tid; j < kDecMaxUnits; j += nthreads) {
@@ -1490,19 +1494,14 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
     if (lane == 0) dec_issue_strips(p, S, u0, n, MT);
   } else if (warp == NC + NL + 1) {
     // ---- row producer: the kept rows of each unit once its finalize warp has published
-    // them, in unit order, then the end mark (a row stage without data whose descriptor
-    // column is -1).  A stage's first use: its own stages at once, those in the strip
-    // ring's space once the up phase is over; later uses: once the gather warps have
-    // released it.
+    // them, in unit order.  It first adds the unit's rows to the known count (the gather
+    // warps size their batches by it), and sets allknown after the last unit.  A stage's
+    // first use: its own stages at once, those in the strip ring's space once the up phase
+    // is over; later uses: once the gather warps have released it.
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int rs = 0, rph = 0, issued = 0;
+      int rs = 0, rph = 0, issued = 0, known = 0;
       bool ok = true;
-      auto stage_wait = [&]() -> bool {
-        if (vload(&m->abort)) return false;
-        if (issued >= SR) return mbar_wait(&rempty[rs], rph ^ 1);
-        return rs < SR1 || mbar_wait(updone, 0);
-      };
       for (int j = 0; j < n && ok; ++j) {
         if (!mbar_wait(&ufin[j], 0)) {
           ok = false;
@@ -1510,6 +1509,8 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
         }
         const int c = m->ucnt[j];
         if (c == 0) continue;
+        known += c;
+        *reinterpret_cast<volatile int*>(&m->known) = known;
         // the unit's expert rows (every entry of a unit has the same group)
         const int g = ent[j * 16].x >> 16;
         int el;
@@ -1519,14 +1520,18 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
         const uint8_t* dbase = reinterpret_cast<const uint8_t*>(es.down + (size_t)el * es.f * es.rs);
         const bool inter = es.rs == 2 * d;
         for (int r = 0; r < c; ++r) {
-          if (!stage_wait()) {
+          if (vload(&m->abort)) {
+            ok = false;
+            break;
+          }
+          if (issued >= SR ? !mbar_wait(&rempty[rs], rph ^ 1) : (rs >= SR1 && !mbar_wait(updone, 0))) {
             ok = false;
             break;
           }
           const int4 e = ent[j * 16 + r];
           const size_t off = (size_t)(e.x & 0xffff) * rsb;
           uint8_t* st = rstage(rs);
-          rdesc[rs] = e;
+          hdesc[issued & (kHD - 1)] = e;
           mbar_arrive_expect_tx(&rfull[rs], (uint32_t)L.row);
           if (inter) {
             bulk_g2s(st, gbase + off, (uint32_t)(4 * d), &rfull[rs], pol);
@@ -1541,29 +1546,31 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
           }
         }
       }
-      if (ok && stage_wait()) {
-        rdesc[rs] = make_int4(-1, 0, 0, 0);
-        mbar_arrive(&rfull[rs]);
+      m->rissued = issued;
+      if (ok) {
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(&m->allknown) = 1;
       } else {
         dec_fail(p, &m->abort);
       }
-      m->rissued = issued;
     }
   } else if (warp > NC) {
     // ---- finalize warps, one per unit lane; then the first one forms the gather's h
     dec_finalize_units<B>(p, S, warp - NC - 1, NL, u0, n, MT);
     if (warp == NC + 1) {
-      // batch k: sum the gather warps' dot partials of each (row, token), then
-      // h = SiLU(sum) * v * router weight, for lane q * 2 + b
+      // batch k (rows 4k ..): sum the gather warps' dot partials of each (row, token), then
+      // h = SiLU(sum) * v * router weight, for lane q * 2 + b; rows past the batch's count
+      // get h = 0
       for (int k = 0;; ++k) {
         const int hs = k & (kHB - 1);
         if (vload(&m->abort) || !__all_sync(0xffffffffu, mbar_wait(&dotsb[hs], (k / kHB) & 1))) break;
-        const int nb = vload(&nbs[hs]);
+        const int nbw = vload(&nbs[hs]);
+        const int nb = nbw & 0xff;
         if (lane < kDecRows * 2) {
           const int q = lane >> 1, b = lane & 1;
           float hq = 0.f;
           if (q < nb && b < B) {
-            const int4 e = bdesc[hs * kDecRows + q];
+            const int4 e = hdesc[(k * kDecRows + q) & (kHD - 1)];
             const int g = e.x >> 16;
             const int t = m->tmap[g][b];
             if (t >= 0) {
@@ -1582,7 +1589,7 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&hrdy[hs]);
-        if (nb < kDecRows) break;
+        if (nbw & 0x100) break;  // the last batch
       }
     }
   } else {
@@ -1609,39 +1616,39 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
         xh[b][3] = xv.w;
       }
       int s0 = 0, ph0 = 0;  // stage and full-barrier parity of the batch's first row
-      // acc += h of batch k * this thread's slices of its down rows, once the h warp has
-      // published that h
-      auto apply = [&](int k, int nbq, const uint4 (&dn)[kDecRows]) -> bool {
+      int cons = 0;         // rows consumed
+      // acc += h of batch k * this thread's slices of its down rows (all four: rows past a
+      // batch's count have h = 0 and zero slices), once the h warp has published that h
+      auto apply = [&](int k, const uint4 (&dn)[kDecRows]) -> bool {
         const int hs = k & (kHB - 1);
         if (!__all_sync(0xffffffffu, mbar_wait(&hrdy[hs], (k / kHB) & 1))) return false;
         const float* hb = hbuf + hs * kDecRows * 2;
 #pragma unroll
         for (int q = 0; q < kDecRows; ++q) {
-          if (q < nbq) {
-            const float2 hq = *reinterpret_cast<const float2*>(hb + q * 2);
-            const float hv[2] = {hq.x, hq.y};
-            const __half2* dh = reinterpret_cast<const __half2*>(&dn[q]);
+          const float2 hq = *reinterpret_cast<const float2*>(hb + q * 2);
+          const float hv[2] = {hq.x, hq.y};
+          const __half2* dh = reinterpret_cast<const __half2*>(&dn[q]);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 df = __half22float2(dh[e]);
+          for (int e = 0; e < 4; ++e) {
+            const float2 df = __half22float2(dh[e]);
 #pragma unroll
-              for (int b = 0; b < B; ++b) {
-                acc[b][2 * e] = fmaf(hv[b], df.x, acc[b][2 * e]);
-                acc[b][2 * e + 1] = fmaf(hv[b], df.y, acc[b][2 * e + 1]);
-              }
+            for (int b = 0; b < B; ++b) {
+              acc[b][2 * e] = fmaf(hv[b], df.x, acc[b][2 * e]);
+              acc[b][2 * e + 1] = fmaf(hv[b], df.y, acc[b][2 * e + 1]);
             }
           }
         }
         return true;
       };
-      // batch k of up to kDecRows rows: dot partials of this warp into slot k % kHB, then
-      // the previous batch applied; no warp waits for another one.  Returns the batch's
-      // rows (fewer than kDecRows: the end mark was reached), or -1 on a failure.
-      auto step = [&](int k, uint4 (&dcur)[kDecRows], const uint4 (&dprev)[kDecRows], int prev_nb) -> int {
+      // batch k: kDecRows rows when that many more are known, else (once every unit is
+      // finalized) the remaining 0 .. kDecRows - 1 rows as the last batch.  Dot partials of
+      // this warp into slot k % kHB, then the previous batch applied; no warp waits for
+      // another one.  Returns the batch's rows plus 0x100 for the last batch, or -1.
+      auto step = [&](auto full_t, int k, int nb, uint4 (&dcur)[kDecRows], const uint4 (&dprev)[kDecRows]) -> int {
+        constexpr bool FULLB = decltype(full_t)::value;
         const int hs = k & (kHB - 1);
         int st[kDecRows];
-        bool ok = !vload(&m->abort);
-        int nb = 0;
+        bool ok = true;
 #pragma unroll
         for (int q = 0; q < kDecRows; ++q) {
           int sq = s0 + q, pq = ph0;
@@ -1650,34 +1657,22 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
             pq ^= 1;
           }
           st[q] = sq;
-          if (ok && nb == q) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&rfull[sq], pq));
-            if (ok && rdesc[sq].x >= 0) nb = q + 1;
-          }
+          if (FULLB || q < nb) ok = mbar_wait(&rfull[sq], pq) && ok;
         }
-        if (!ok) {
+        if (!__all_sync(0xffffffffu, ok)) {
           if (lane == 0) {
             dec_fail(p, &m->abort);
             mbar_arrive(&dotsb[hs]);
           }
           return -1;
         }
-        // warp 0 hands the batch's descriptors to the h warp (the stages are released
-        // below, before it reads them)
-        if (warp == 0) {
-          if (lane < nb) {
-            int sq = s0 + lane;
-            if (sq >= SR) sq -= SR;
-            bdesc[hs * kDecRows + lane] = rdesc[sq];
-          }
-          if (lane == 0) nbs[hs] = nb;
-        }
+        if (warp == 0 && lane == 0) nbs[hs] = FULLB ? kDecRows : (nb | 0x100);
         float dot[kDecRows][B];
 #pragma unroll
         for (int q = 0; q < kDecRows; ++q) {
 #pragma unroll
           for (int b = 0; b < B; ++b) dot[q][b] = 0.f;
-          if (q < nb) {
+          if (FULLB || q < nb) {
             const uint4 gr = reinterpret_cast<const uint4*>(rstage(st[q]))[tid];
             const uint32_t gw4[4] = {gr.x, gr.y, gr.z, gr.w};
 #pragma unroll
@@ -1693,12 +1688,13 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
         // this thread's slice of every down row, then the stages can be refilled at once
 #pragma unroll
         for (int q = 0; q < kDecRows; ++q)
-          dcur[q] = q < nb ? reinterpret_cast<const uint4*>(rstage(st[q]) + 2 * d)[tid]
-                           : make_uint4(0, 0, 0, 0);
+          dcur[q] = (FULLB || q < nb) ? reinterpret_cast<const uint4*>(rstage(st[q]) + 2 * d)[tid]
+                                      : make_uint4(0, 0, 0, 0);
         __syncwarp();
         if (lane == 0) {
-          for (int q = 0; q < nb; ++q) mbar_arrive(&rempty[st[q]]);
-          if (warp == 0) m->rconsumed += nb;
+#pragma unroll
+          for (int q = 0; q < kDecRows; ++q)
+            if (FULLB || q < nb) mbar_arrive(&rempty[st[q]]);
         }
         // the warp's sums by recursive halving: lane 8q (+ 4b for two tokens) ends with
         // (row q, token b)
@@ -1709,33 +1705,64 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&dotsb[hs]);
-        if (k > 0 && !apply(k - 1, prev_nb, dprev)) {
+        if (k > 0 && !apply(k - 1, dprev)) {
           if (lane == 0) dec_fail(p, &m->abort);
           return -1;
         }
-        s0 += nb;
+        s0 += FULLB ? kDecRows : nb;
         if (s0 >= SR) {
           s0 -= SR;
           ph0 ^= 1;
         }
-        return nb;
+        cons += FULLB ? kDecRows : nb;
+        return FULLB ? kDecRows : (nb | 0x100);
+      };
+      // rows of the next batch: kDecRows if known, else the rest once all are known
+      auto next_rows = [&]() -> int {
+        for (uint32_t tries = 0;; ++tries) {
+          int ak = 0, kn = 0;
+          if (lane == 0) {
+            ak = vload(&m->allknown);
+            __threadfence_block();
+            kn = vload(&m->known);
+          }
+          ak = __shfl_sync(0xffffffffu, ak, 0);
+          kn = __shfl_sync(0xffffffffu, kn, 0);
+          if (kn - cons >= kDecRows) return kDecRows;
+          if (ak) return kn - cons;
+          if (vload(&m->abort) || tries > kWaitTries * 1000u) return -1;
+          __nanosleep(32);
+        }
       };
       uint4 dA[kDecRows], dB[kDecRows];
-      int k = 0, nb = kDecRows, last_nb = 0;
+      int k = 0, res = 0;
+      const std::integral_constant<bool, true> kFull;
+      const std::integral_constant<bool, false> kPart;
       for (;;) {
-        nb = step(k, dA, dB, last_nb);
-        if (nb < 0) break;
-        last_nb = nb;
+        int nb = next_rows();
+        if (nb < 0) {
+          res = -1;
+          if (lane == 0) dec_fail(p, &m->abort);
+          break;
+        }
+        res = nb == kDecRows ? step(kFull, k, nb, dA, dB) : step(kPart, k, nb, dA, dB);
+        if (res < 0) break;
         ++k;
-        if (nb < kDecRows) break;
-        nb = step(k, dB, dA, last_nb);
-        if (nb < 0) break;
-        last_nb = nb;
+        if (res & 0x100) break;
+        nb = next_rows();
+        if (nb < 0) {
+          res = -1;
+          if (lane == 0) dec_fail(p, &m->abort);
+          break;
+        }
+        res = nb == kDecRows ? step(kFull, k, nb, dB, dA) : step(kPart, k, nb, dB, dA);
+        if (res < 0) break;
         ++k;
-        if (nb < kDecRows) break;
+        if (res & 0x100) break;
       }
       // the last batch (k - 1), whose rows' down slices are in dA if k - 1 is even
-      if (nb >= 0 && !apply(k - 1, last_nb, ((k - 1) & 1) ? dB : dA) && lane == 0) dec_fail(p, &m->abort);
+      if (res >= 0 && !apply(k - 1, ((k - 1) & 1) ? dB : dA) && lane == 0) dec_fail(p, &m->abort);
+      if (tid == 0) m->rconsumed = cons;
       // this CTA's share of y, added in fp32 into copy blockIdx.x % kDecYRep of the
       // accumulator (the order of the CTAs' additions varies)
 #pragma unroll
