@@ -36,6 +36,7 @@ import torch  # noqa: E402
 WORKLOAD = dict(name="mixtral-8x7b-moe-layer-decode", d=4096, f=14336, E=8, k=2, B=1,
                 calib_tokens=1024)
 SPARSITIES = (0, 50, 70, 90)
+INF_PCT = 101  # --sparsity 101: t = +inf (nothing kept: only the up projection's bytes)
 
 # Further layer shapes, timed with --workload (one JSON line per point; the default run
 # above is the headline).  Shared experts have the routed experts' d and f.
@@ -74,7 +75,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--sparsity", type=int, default=HEADLINE_PCT)
+    ap.add_argument("--sparsity", type=int, default=HEADLINE_PCT,
+                    help="0/50/70/90 (the calibrated points) or 101 for t = +inf")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=N_LAYER_COPIES,
                     help="rotating layer copies (fewer: a small case for profiling; below 8 the "
@@ -233,7 +235,27 @@ def calibrate(layers, dev):
                     thr[p][e] = a[(p * n + 99) // 100 - 1]
         for p in SPARSITIES:
             table[p].append(thr[p])
+        table.setdefault(INF_PCT, []).append(torch.full((W["E"],), float("inf"), dtype=torch.float32, device=dev))
     return table
+
+
+def pct_label(pct):
+    return "t=+inf" if pct == INF_PCT else f"{pct}%"
+
+
+def config_dict(pct, R, world):
+    """The workload both arms report (identical keys and values)."""
+    W = WORKLOAD
+    d, f, E = W["d"], W["f"], W["E"]
+    copy_gb = E * (4 * d * f + d * f * 5 / 16) / 1e9  # gate + down fp16, packed INT2 up
+    return {"workload": W["name"], "d": d, "f": f, "experts": E, "top_k": W["k"],
+            "tokens_per_step": W["B"], "sparsity_pct": pct, "up_projection": "int2 g64 fp16 scale/zero",
+            "gate_down": "fp16", "rmsnorm": True, "parallelism": f"replicas x{world}",
+            "calibration_tokens": W["calib_tokens"],
+            "l2": f"inputs larger than L2: {R} rotating layer copies ({R * copy_gb:.1f} GB), "
+                  f"each reused only after {R - 1} others",
+            "graphs": f"the {R} layer copies back to back in one CUDA graph, as a stack of "
+                      "layers runs (PDL between all kernels); each copy keeps its own token"}
 
 
 def set_thresholds(layers, table, pct):
@@ -458,23 +480,24 @@ def run_reference(args, world, rank, local):
         return
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     W = WORKLOAD
-    # the thresholds need the library's v only for the calibration statistics; the
-    # oracle arm uses the percentile of its own |v| over the same calibration tokens
     from oracle import moe_oracle as orc
     from sparse_expert_swiglu_gb300 import synth
     d, f, E, k = W["d"], W["f"], W["E"], W["k"]
     xs_n = 4
     wr = synth.router(d, E, 100, device=dev, layer=0).cpu().numpy()
-    xs = synth.tokens(xs_n, d, 555, device=dev).cpu().numpy()
+    # the GPU arm's tokens of its first layer copies (one token each), on layer copy 0
+    xs = np.concatenate([synth.tokens(W["B"], d, 1000 + i, device=dev).cpu().numpy() for i in range(xs_n)])
     idx, _, _ = orc.route_topk(xs, wr, k)
     need = sorted(set(idx.ravel().tolist()))
     de = synth.experts(E, d, f, 100, device=dev, layer=0)
-    xcal = synth.calibration_tokens(64, d, 7, device=dev).cpu().numpy()
+    # thresholds as the GPU arm sets them: the nearest-rank percentile of |v| over the same
+    # calibration tokens (here with the oracle's own fp64 v)
+    xcal = synth.calibration_tokens(W["calib_tokens"], d, 7, device=dev).cpu().numpy()
     experts = [None] * E
     for e in need:
         q, s, z = orc.quantize_int2(de.w_up[e].cpu().numpy())
         wdeq = orc.dequantize_int2(q, s, z)
-        t = orc.quantile_threshold(orc.expert_up(xcal, wdeq), args.sparsity)
+        t = np.inf if args.sparsity == INF_PCT else orc.quantile_threshold(orc.expert_up(xcal, wdeq), args.sparsity)
         experts[e] = dict(w_gate=de.gate_t[e].cpu().numpy().T, w_up_deq=wdeq,
                           w_down=de.down[e].cpu().numpy(), thr=float(np.float32(t)))
     del de
@@ -482,15 +505,15 @@ def run_reference(args, world, rank, local):
     value = W["B"] * k * args.steps / secs
     cores = oracle_threads()
     line = {
-        "impl": "reference", "metric": METRIC.replace("70%", f"{args.sparsity}%"), "value": value,
+        "impl": "reference", "metric": METRIC.replace("70%", pct_label(args.sparsity)), "value": value,
         "unit": "expert-tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": W["name"], "d": d, "f": f, "experts": E, "top_k": k,
-                   "tokens_per_step": W["B"], "sparsity_pct": args.sparsity},
+        "config": config_dict(args.sparsity, max(1, args.copies), args.gpus),
         "cpu_baseline": {"value": value, "unit": "expert-tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} single-token layer decodes over {xs_n} tokens of layer copy 0 "
-                                   f"(fp64 numpy oracle, {args.sparsity}% thresholds from 64 calibration tokens)"},
+                                   f"(fp64 numpy oracle, {pct_label(args.sparsity)} thresholds from "
+                                   f"{W['calib_tokens']} calibration tokens)"},
         "e2e": {"value": value, "unit": "expert-tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -541,7 +564,7 @@ def run_ours(args, world, rank, local):
         t_start = time.perf_counter()
         secs = time_steps(graphs, stream, args.steps, args.warmup, world, dev, stack=stack)
         # keep the same load running until the sampler has seen >= 1 s of it
-        while args.steps >= 1000 and time.perf_counter() - t_start < 1.2:
+        while time.perf_counter() - t_start < 1.2:
             time_steps(graphs, stream, 2000, 0, 1, dev, stack=stack)
     secs = max_over_ranks(world, secs, dev)
     # the same steps with one graph launch per layer (no dependent launch across layers)
@@ -635,18 +658,11 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return
     line = {
-        "metric": METRIC.replace("70%", f"{pct}%"), "value": value, "unit": "expert-tokens/s",
+        "metric": METRIC.replace("70%", pct_label(pct)), "value": value, "unit": "expert-tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": W["name"], "d": d, "f": f, "experts": E, "top_k": k,
-                   "tokens_per_step": B, "sparsity_pct": pct, "up_projection": "int2 g64 fp16 scale/zero",
-                   "gate_down": "fp16", "rmsnorm": True, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {R} rotating layer copies "
-                         f"({sum(l.routed.gate_t.numel() * 4 + l.routed.up_packed.numel() for l in layers) / 1e9:.1f} GB), "
-                         f"each reused only after {R - 1} others",
-                   "graphs": "the 8 layer copies back to back in one CUDA graph, as a stack of "
-                             "layers runs (PDL between all kernels); each copy keeps its own token"},
+        "config": config_dict(pct, R, world),
         "layer_us": ms_per_step * 1e3,
         "layer_us_one_graph_per_layer": secs_single / args.steps * 1e6,
         "layer_us_distribution": dist,

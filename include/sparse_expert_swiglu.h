@@ -163,7 +163,9 @@ moe_status_t moe_route_topk(const uint16_t* x, int32_t B, int32_t d, const uint1
  *   Arguments, layouts and results are those of moe_route_topk.
  *   B * k > MOE_ROUTE_NOALLOC_MAX_PAIRS: MOE_ERR_WORKSPACE_TOO_SMALL, nothing enqueued.
  *   The first call on a device looks up the scratch address (with that device
- *   current); make it before capturing a stream.  Every call clears the scratch's
+ *   current); make it before capturing a stream.  The address is kept per device and
+ *   context: the first call in a context created later on the device (after
+ *   cudaDeviceReset, say) looks it up again.  Every call clears the scratch's
  *   control block on `stream` before the kernel.  Calls that overlap in time on
  *   one device (different streams or host threads) share the scratch and race:
  *   order them on one stream.
@@ -212,13 +214,15 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
 
 /*
  * moe_layer_path -- which kernels moe_layer_decode runs for this layer and B tokens on
- * the current device: 1 = the decode path (one or two tokens, 8/16/32/64 routed experts,
- * d <= 6144: an up-projection kernel that also routes and a gather kernel that also
- * combines), 0 = the general path (router, up-projection, gather and combine kernels),
- * or a negative moe_status_t for an invalid layer.  Both paths compute the same layer.
- * The general path is bitwise reproducible; on the decode path the experts' shares
- * reach the fp32 sum of y in a varying order, so two calls can differ in the last
- * bits of that sum (at most one fp16 ulp of y).
+ * the current device: 2 = the one-kernel decode path (one or two tokens, 8/16/32/64
+ * routed experts, d <= 4096: one kernel routes, projects, thresholds, gathers the kept
+ * rows and combines), 1 = the two-kernel decode path (the same shapes with
+ * 4096 < d <= 6144: an up-projection kernel that also routes and a gather kernel that
+ * also combines), 0 = the general path (router, up-projection, gather and combine
+ * kernels), or a negative moe_status_t for an invalid layer.  Every path computes the
+ * same layer.  The general path is bitwise reproducible; on the decode paths the CTAs'
+ * shares reach the fp32 sum of y in a varying order, so two calls can differ in the
+ * last bits of that sum (at most one fp16 ulp of y).
  */
 int32_t moe_layer_path(const moe_layer_t* layer, int32_t B);
 
@@ -231,7 +235,8 @@ int32_t moe_layer_path(const moe_layer_t* layer, int32_t B);
  *   layer: the router weight, up_packed and thr of both expert sets are device
  *     pointers; gate_t and down (routed and shared) are host pointers to memory from
  *     cudaHostAlloc / cudaMallocHost or registered with cudaHostRegister (device
- *     pointers are accepted too); any other memory returns MOE_ERR_INVALID_ARG.
+ *     pointers are accepted too), the whole extent of each (E * f rows) in one mapping;
+ *     any other memory, or a buffer registered only in part, returns MOE_ERR_INVALID_ARG.
  *   ws / ws_bytes: at least moe_layer_host_rows_workspace_bytes(layer, B) bytes: the
  *     workspace of moe_layer_decode followed by a staging area for the kept rows (4d
  *     bytes per row, room for at least (B k + shared E) f rows: the dense worst case).

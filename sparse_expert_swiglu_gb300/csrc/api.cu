@@ -495,21 +495,33 @@ size_t moe_layer_host_rows_workspace_bytes(const moe_layer_t* layer, int32_t B) 
   return align_up(L.total, kWsAlign) + host_rows_staging_bytes(layer, L, di.sms);
 }
 
-// The device's address of a buffer in page-locked host memory (or in device memory).
-static moe_status_t device_view(const __half* p, const __half*& out) {
-  cudaPointerAttributes a;
-  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+// The device's address of a buffer of `bytes` bytes in page-locked host memory (or in
+// device memory): both its first and its last byte must be registered, in one mapping
+// (the last byte's device address is the first one's plus the distance), so that every
+// row the fetch kernel may read is covered.
+static moe_status_t device_view(const __half* p, size_t bytes, const __half*& out) {
+  cudaPointerAttributes a, z;
+  const char* last = reinterpret_cast<const char*>(p) + (bytes ? bytes - 1 : 0);
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess || cudaPointerGetAttributes(&z, last) != cudaSuccess) {
     (void)cudaGetLastError();
     return MOE_ERR_INVALID_ARG;
   }
   if (a.type == cudaMemoryTypeUnregistered || a.devicePointer == nullptr) return MOE_ERR_INVALID_ARG;
+  if (z.type == cudaMemoryTypeUnregistered || z.devicePointer == nullptr) return MOE_ERR_INVALID_ARG;
+  if (static_cast<const char*>(z.devicePointer) != static_cast<const char*>(a.devicePointer) + (bytes ? bytes - 1 : 0))
+    return MOE_ERR_INVALID_ARG;
   out = reinterpret_cast<const __half*>(a.devicePointer);
   return MOE_OK;
 }
 
+// gate_t and down of a set: E * f rows of rs elements each from the buffer start (an
+// interleaved down buffer starts d elements later and ends where gate_t ends).
 static moe_status_t device_view_rows(ExpertSet& es) {
-  moe_status_t s = device_view(es.gate_t, es.gate_t);
-  if (s == MOE_OK) s = device_view(es.down, es.down);
+  const size_t span = (size_t)es.E * es.f * es.rs * sizeof(__half);
+  const size_t down_off = (size_t)(es.down - es.gate_t) * sizeof(__half);
+  const bool inter = es.rs == 2 * es.d;
+  moe_status_t s = device_view(es.gate_t, span, es.gate_t);
+  if (s == MOE_OK) s = device_view(es.down, inter ? span - down_off : span, es.down);
   return s;
 }
 

@@ -10,7 +10,10 @@
 // result) lives in a file-scope device array that every GPU loading the library
 // holds until the process exits.  The router kernel and its launch are the same as
 // moe_route_topk's; only where its scratch lives differs.
+#include <cuda.h>
+
 #include <atomic>
+#include <mutex>
 
 #include "params.cuh"
 
@@ -25,9 +28,41 @@ constexpr size_t kScratchBytes = kCtrlBytes + (size_t)kNoAllocMaxPairs * (sizeof
 // Shared by every call on a device; keeps the last call's contents.
 static __device__ __align__(256) uint8_t g_route_scratch[kScratchBytes];
 
-// Device address of g_route_scratch per device (its name is only a host-side stand-in).
+// Device address of g_route_scratch per device (its name is only a host-side stand-in),
+// with the id of the context it was looked up in: a context created later on the device
+// (after cudaDeviceReset, say) loads the module again, possibly elsewhere, so the address
+// is looked up again when the current context's id differs.
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+ScratchEntry g_scratch[kMaxDevices];
+std::mutex g_scratch_mu;
+
+// The current context's id, through the driver entry points the runtime hands out (the
+// library links no driver library).  0 if unavailable.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static std::atomic<void*> get_current{nullptr}, get_id{nullptr};
+  void* gc = get_current.load(std::memory_order_acquire);
+  void* gi = get_id.load(std::memory_order_acquire);
+  if (!gc || !gi) {
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &gc, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &gi, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !gc || !gi)
+      return 0;
+    get_current.store(gc, std::memory_order_release);
+    get_id.store(gi, std::memory_order_release);
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (reinterpret_cast<GetCurrent>(gc)(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (reinterpret_cast<GetId>(gi)(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p % 16) == 0; }
 
@@ -46,11 +81,22 @@ extern "C" moe_status_t moe_route_topk_noalloc(const uint16_t* x, int32_t B, int
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED_SHAPE;
-  void* base = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (!base) {
-    // once per device, with that device current
-    if (cudaGetSymbolAddress(&base, g_route_scratch) != cudaSuccess || !base) return MOE_ERR_CUDA;
-    g_scratch_addr[dev].store(base, std::memory_order_release);
+  // (the caller's device pointers imply a current context; without one, or without the
+  // driver entry points, the id is 0 and the address is looked up on every call)
+  const unsigned long long ctx = current_context_id();
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    ScratchEntry& en = g_scratch[dev];
+    if (!en.addr || en.ctx_id != ctx || ctx == 0) {
+      // once per device and context, with that device current
+      if (cudaGetSymbolAddress(&en.addr, g_route_scratch) != cudaSuccess || !en.addr) {
+        en.addr = nullptr;
+        return MOE_ERR_CUDA;
+      }
+      en.ctx_id = ctx;
+    }
+    base = en.addr;
   }
   uint8_t* ws = static_cast<uint8_t*>(base);
   cudaStream_t st = (cudaStream_t)stream;

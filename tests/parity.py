@@ -44,6 +44,13 @@ def check_mask(mask_gpu, v_ref, S, t):
     return int(((mask_gpu != ref) & ~band).sum()), int(band.sum())
 
 
+def mask_excused(mask_gpu, v_ref, S, t):
+    """#decisions the band excuses: inside it, and the kernel's differs from the oracle's."""
+    ref = np.abs(v_ref) > t
+    band = np.abs(np.abs(v_ref) - t) <= TAU * S
+    return int(((mask_gpu != ref) & band).sum())
+
+
 def check_v(v_gpu, v_ref, S):
     """Largest |v_gpu - v| / S (must stay below TAU for the band rule to hold)."""
     return float(np.max(np.abs(v_gpu.astype(np.float64) - v_ref) / np.maximum(S, 1e-300)))

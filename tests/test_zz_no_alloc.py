@@ -5,9 +5,9 @@ after every other test has used the device.
 Both entry points launch the same router kernel on the same inputs, so the
 expert indices and counts must be equal and the weights equal within 2e-6 (the
 router test tolerance).  Consecutive calls share the static scratch: the cases
-below run back to back, from one CTA (B <= 4) to the multi-CTA hand-off that
-depends on the scratch's counter starting at zero, up to the stated maximum of
-B * k pairs.
+below run back to back, from one token (one CTA) to the multi-CTA hand-off of two
+or more tokens (one CTA per token, the last one to finish found with the scratch's
+counter, which must start at zero), up to the stated maximum of B * k pairs.
 """
 
 from __future__ import annotations
