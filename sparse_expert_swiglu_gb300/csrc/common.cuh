@@ -132,6 +132,14 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// b * m for fp16x2 b and m = (1, 1) or (0, 0): b or zeros, exactly (x is finite).  Used to
+// zero an mma B operand on the FMA pipe rather than by a select on the integer pipe.
+__device__ __forceinline__ uint32_t hmul2_mask(uint32_t b, uint32_t m) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(b), "r"(m));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }

@@ -489,7 +489,8 @@ __device__ __forceinline__ void dec_groups(const uint4 (&w)[4], const uint32_t (
   if constexpr (GAM < G) {
     constexpr int GI = PH * G + GAM;
     if (FULL || GI < ng) {
-      const bool on = cl == GAM;
+      // x only in the slots of class GAM (the integer pipe is busy unpacking the codes)
+      const uint32_t on = cl == GAM ? 0x3C003C00u : 0u;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         uint32_t a[4];
@@ -497,7 +498,7 @@ __device__ __forceinline__ void dec_groups(const uint4 (&w)[4], const uint32_t (
         a[1] = code_pair<GI>(w[t].y);
         a[2] = code_pair<GI>(w[t].z);
         a[3] = code_pair<GI>(w[t].w);
-        mma_16816(D[t], a, on ? xr[PH][t][0] : 0u, on ? xr[PH][t][1] : 0u);
+        mma_16816(D[t], a, hmul2_mask(xr[PH][t][0], on), hmul2_mask(xr[PH][t][1], on));
       }
     }
     dec_groups<T, PH, GAM + 1, FULL>(w, xr, cl, D, ng);
@@ -1550,9 +1551,15 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
       if (ok) {
         __threadfence_block();
         *reinterpret_cast<volatile int*>(&m->allknown) = 1;
-      } else {
-        dec_fail(p, &m->abort);
+        // end marker: a plain arrival on the stage of row `issued` (no row comes there), so
+        // that a gather warp waiting for that row wakes and sees allknown; the stage's
+        // previous row must have been consumed first, as for a row
+        if (issued >= SR && !mbar_wait(&rempty[rs], rph ^ 1))
+          ok = false;
+        else
+          mbar_arrive(&rfull[rs]);
       }
+      if (!ok) dec_fail(p, &m->abort);
     }
   } else if (warp > NC) {
     // ---- finalize warps, one per unit lane; then the first one forms the gather's h
@@ -1717,7 +1724,10 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
         cons += FULLB ? kDecRows : nb;
         return FULLB ? kDecRows : (nb | 0x100);
       };
-      // rows of the next batch: kDecRows if known, else the rest once all are known
+      // rows of the next batch: kDecRows if known, else the rest once all are known.  While
+      // neither, wait for row kn (the first one not known yet) to land: the row producer
+      // publishes a unit's count before issuing its rows, and after the last unit it puts
+      // an end marker on the stage of the row past the last one.
       auto next_rows = [&]() -> int {
         for (uint32_t tries = 0;; ++tries) {
           int ak = 0, kn = 0;
@@ -1730,8 +1740,13 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
           kn = __shfl_sync(0xffffffffu, kn, 0);
           if (kn - cons >= kDecRows) return kDecRows;
           if (ak) return kn - cons;
-          if (vload(&m->abort) || tries > kWaitTries * 1000u) return -1;
-          __nanosleep(32);
+          if (vload(&m->abort) || tries > (uint32_t)kDecMaxUnits * 16) return -1;
+          int sq = s0 + (kn - cons), pq = ph0;
+          if (sq >= SR) {
+            sq -= SR;
+            pq ^= 1;
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait(&rfull[sq], pq))) return -1;
         }
       };
       uint4 dA[kDecRows], dB[kDecRows];
@@ -1886,6 +1901,10 @@ cudaError_t launch_decode_gather(const DecodeParams& p, cudaStream_t st, bool pd
   return p.B == 1 ? launch_ga<1, kGaThreads>(cfg, p, L.total) : launch_ga<2, kGaThreads>(cfg, p, L.total);
 }
 
+// ring space of the one-kernel layer given to the strips, in tenths; own row stages, at least
+constexpr int kLyStripShare = 4;
+constexpr int kLyMinRowStages = kDecRows + 2;
+
 int decode_layer_plan(int B, int d, int E, int umax, int smem_optin, int& su, int& sr) {
   su = sr = 0;
   if (d > 4096) return 0;
@@ -1897,14 +1916,14 @@ int decode_layer_plan(int B, int d, int E, int umax, int smem_optin, int& su, in
   // for the phase after the one it last waited for: a parity wait cannot tell a phase from
   // the one two back); rows: the rest
   const int NL = dec_lanes(z.nsb);
-  int s = (int)(budget * 2 / 5 / z.strip);
+  int s = (int)(budget * kLyStripShare / 10 / z.strip);
   s += (NL - s % NL) % NL;
   if (s < 2 * NL) s = 2 * NL;
   if (s > kDecMaxSu) s = kDecMaxSu - kDecMaxSu % NL;
   if ((size_t)s * z.strip >= budget) return 0;
   int r = (int)((budget - (size_t)s * z.strip) / z.row);
   if (r > kDecMaxSr) r = kDecMaxSr;
-  if (r < kDecRows + 2) return 0;
+  if (r < kLyMinRowStages) return 0;
   if (ly_layout_d(d, B, E, s, r, umax).total > (size_t)smem_optin) return 0;
   su = s;
   sr = r;
