@@ -345,6 +345,73 @@ def capture_stack_e2e(layers, x_all, y_all, ws_list, stream, x_pin, y_pin):
     return g
 
 
+def capture_stack_prefetch(layers, xs, ys, ws_list, stream, pred):
+    """The stacked graph with the inter-expert prefetch hook: while layer copy r runs, a
+    second stream prefetches into L2 the packed up projections of the experts predicted
+    for copy r + 1 (the next replay's copy 0 after the last).  The side branch waits
+    only for layer r - 1, so the layers' dependent launches are unchanged; it rejoins
+    at the end of the graph."""
+    import sparse_expert_swiglu_gb300 as ses
+    R = len(layers)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    c_layers = [layer.c_struct() for layer in layers]
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for r, layer in enumerate(layers):
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                ses.prefetch_experts(layers[(r + 1) % R].routed, pred[(r + 1) % R])
+            ses.layer_decode(xs[r], layer, rmsnorm=True, ws=ws_list[r], out=ys[r], c_layer=c_layers[r])
+        stream.wait_stream(side)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_stack(stack, stream, R, steps, warmup):
+    """Microseconds per layer over whole replays of a stacked graph."""
+    reps = max(1, steps // R)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, warmup // R)):
+            stack.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            stack.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * R)
+
+
+def prefetch_hook_times(layers, xs, ys, ws_list, stream, steps, warmup):
+    """Layer time in the stacked graph without the prefetch hook, with it on an exact
+    prediction (each copy's own router on its own token: the copies are not chained, so
+    this is the best a predictor can do) and with it on a prediction that misses every
+    routed expert."""
+    import sparse_expert_swiglu_gb300 as ses
+    W = WORKLOAD
+    R, E, k = len(layers), W["E"], W["k"]
+    exact = [ses.route_topk(xs[r], layers[r].w_router, k)[0].reshape(-1).contiguous() for r in range(R)]
+    miss = []
+    for r in range(R):
+        chosen = set(exact[r].tolist())
+        miss.append(torch.tensor([e for e in range(E) if e not in chosen][:k], dtype=torch.int32,
+                                 device=xs[r].device))
+    plain = capture_stack(layers, xs, ys, ws_list, stream)
+    with_exact = capture_stack_prefetch(layers, xs, ys, ws_list, stream, exact)
+    with_miss = capture_stack_prefetch(layers, xs, ys, ws_list, stream, miss)
+    out = {}
+    for name, g in (("without", plain), ("exact_prediction", with_exact), ("missed_prediction", with_miss)):
+        out[f"layer_us_{name}"] = time_stack(g, stream, R, steps, warmup)
+    out["prefetch_bytes_per_layer"] = k * ses.packed_bytes(W["d"], W["f"])
+    out["how"] = ("stacked graph of the layer copies; a second stream L2-prefetches the packed up "
+                  "projections of the experts predicted for the next copy while a copy runs "
+                  "(moe_prefetch_experts); exact = each copy's own router on its own token, "
+                  "missed = k experts that copy does not route to")
+    return out
+
+
 def time_steps(graphs, stream, steps, warmup, world, dev, stack=None):
     """Device time of `steps` layer passes: whole replays of the stacked graph (R layers
     each), the remainder from the single-layer graphs."""
@@ -645,6 +712,8 @@ def run_ours(args, world, rank, local):
     e2e_step_secs = max_over_ranks(world, e0.elapsed_time(e1) / 1e3, dev)
     e2e_step_value = sum_over_ranks(world, B * k * args.steps, dev) / e2e_step_secs
 
+    hook = prefetch_hook_times(layers, xs, ys, ws_list, stream, max(R * 50, args.steps // 4), args.warmup)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xs_o, wr_o, experts_o = oracle_prepare(dev, 2, table, pct)
@@ -681,6 +750,7 @@ def run_ours(args, world, rank, local):
                        "copy after the last)",
                 "one_step_at_a_time": {"value": e2e_step_value, "unit": "expert-tokens/s",
                                        "how": "per step: copy in, one layer's graph, copy out, one stream"}},
+        "prefetch_hook": hook,
         "gpu_launches": {"decode_fused": 1, "decode": 2}.get(path, 4) * args.steps,
         "path": path,
         "clocks": clk.summary(),

@@ -251,6 +251,34 @@ moe_status_t moe_layer_decode_host_rows(const uint16_t* x, int32_t B, const moe_
                                         uint16_t* y, int32_t rmsnorm_out, const moe_debug_t* dbg,
                                         void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * moe_prefetch_experts -- the data movement behind an inter-expert predictor ("FloE:
+ * On-the-Fly MoE Inference on Memory-constrained GPU", sec. "双稀疏预测器", Inter-expert
+ * Predictor).  FloE's predictor guesses a later layer's experts from an earlier hidden
+ * state.  The page gives its core observation: consecutive MoE layers' hidden states
+ * have cosine similarity above 0.95.  This call L2-prefetches the packed up projections
+ * of the predicted experts, the part that every token routed to an expert reads whole,
+ * so that the layer's up-projection reads hit in L2.  The prediction is the caller's:
+ * a trained predictor, or moe_route_topk on the current hidden state with the next
+ * layer's router weight.  The call only enqueues bulk L2 prefetches on `stream` and
+ * returns.  No result of any call changes; only timing can.
+ *   experts    the expert stack of the layer that the prediction is for (d, f, E and
+ *              up_packed are read; gate_t, down and thr are not)
+ *   idx        device int32 [n]: predicted expert ids; repeats and ids outside [0, E)
+ *              are ignored
+ *   n          0..1024 (0: nothing is enqueued, idx may be NULL)
+ *   max_bytes  prefetch whole experts in ascending id order while the total stays
+ *              <= max_bytes (0: no limit); GB300's L2 holds 129 MB
+ *   stream     cudaStream_t or NULL.  The kernel uses one warp per SM and no workspace,
+ *              so it can run on a second stream beside a decode layer
+ * Errors: MOE_ERR_INVALID_ARG (experts NULL, n < 0, up_packed NULL, idx NULL with
+ * n > 0), MOE_ERR_UNSUPPORTED_SHAPE (n > 1024, E outside 1..256, d or f outside the
+ * shape limits), MOE_ERR_ALIGNMENT (up_packed not 16-byte or idx not 4-byte aligned),
+ * MOE_ERR_CUDA.  Argument errors are found before any CUDA call.
+ */
+moe_status_t moe_prefetch_experts(const moe_experts_t* experts, const int32_t* idx, int32_t n,
+                                  size_t max_bytes, void* stream);
+
 /* ---------------- expert activation tracking and expert cache (host) ----------------
  *
  * "MoE-Infinity" (sec. 4.3, 4.5, 4.7 Algorithm 1 "专家缓存检索", appendix B.1): request-level

@@ -25,6 +25,7 @@ from ._lib import (  # noqa: F401
     lib_path,
     pack_int2_up,
     packed_bytes,
+    prefetch_experts,
     route_topk,
     route_topk_noalloc,
     route_workspace_bytes,

@@ -81,6 +81,8 @@ _SIGS = {
     "moe_layer_decode_host_rows": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(_Layer),
                                                   ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(_Debug),
                                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_prefetch_experts": (ctypes.c_int, [ctypes.POINTER(_Experts), ctypes.c_void_p, ctypes.c_int32,
+                                            ctypes.c_size_t, ctypes.c_void_p]),
     "moe_eam_add_counts": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.c_void_p]),
     "moe_eamc_bytes": (ctypes.c_size_t, [ctypes.c_int32] * 3),
@@ -441,6 +443,16 @@ def layer_decode(x: torch.Tensor, layer: Layer, rmsnorm: bool = False,
                                   ctypes.byref(dbg) if dbg is not None else None,
                                   ws.ptr(), ws.nbytes, _stream()))
     return (y, dt) if debug else y
+
+
+def prefetch_experts(experts: Experts, idx: torch.Tensor, max_bytes: int = 0) -> None:
+    """L2-prefetch the packed up projections of the experts listed in idx (device int32,
+    any shape; repeats and ids outside [0, E) ignored) on the current stream."""
+    _need(idx, torch.int32, "idx")
+    n = idx.numel()
+    _check("moe_prefetch_experts",
+           lib().moe_prefetch_experts(ctypes.byref(experts.c_struct()), _ptr(idx) if n else None, n,
+                                      max_bytes, _stream()))
 
 
 def layer_host_rows_workspace_bytes(layer: Layer, B: int) -> int:

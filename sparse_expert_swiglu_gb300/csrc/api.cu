@@ -7,6 +7,8 @@ using namespace sesg;
 
 namespace sesg {
 size_t gather_ring_scratch_bytes(int d, int f);  // gather.cu
+cudaError_t launch_expert_prefetch(const uint8_t* up, size_t up_bytes, int E, const int32_t* idx, int n,
+                                   int max_experts, int P, cudaStream_t st);  // prefetch.cu
 int gather_round_stages(int d, int nt, int stages);  // gather.cu
 }
 
@@ -559,6 +561,29 @@ moe_status_t moe_layer_decode_host_rows(const uint16_t* x, int32_t B, const moe_
   if (e == cudaSuccess) e = record(dbg, 3, st);
   if (e == cudaSuccess) e = record(dbg, 4, st);
   return cuda_status(e);
+}
+
+moe_status_t moe_prefetch_experts(const moe_experts_t* experts, const int32_t* idx, int32_t n,
+                                  size_t max_bytes, void* stream) {
+  if (!experts || n < 0) return MOE_ERR_INVALID_ARG;
+  if (n > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+  moe_status_t s = check_dims(experts->d, experts->f);
+  if (s != MOE_OK) return s;
+  if (experts->E < 1 || experts->E > 256) return experts->E < 0 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!experts->up_packed) return MOE_ERR_INVALID_ARG;
+  if (!aligned(experts->up_packed, 16)) return MOE_ERR_ALIGNMENT;
+  if (n == 0) return MOE_OK;
+  if (!idx) return MOE_ERR_INVALID_ARG;
+  if (!aligned(idx, 4)) return MOE_ERR_ALIGNMENT;
+  const size_t per = packed_bytes_per_expert(experts->d, experts->f);
+  long long max_experts = 256;
+  if (max_bytes > 0) max_experts = (long long)(max_bytes / per);
+  if (max_experts == 0) return MOE_OK;
+  DeviceInfo di;
+  if (device_info(di) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_expert_prefetch(reinterpret_cast<const uint8_t*>(experts->up_packed), per,
+                                            experts->E, idx, n, (int)(max_experts > 256 ? 256 : max_experts),
+                                            di.sms, (cudaStream_t)stream));
 }
 
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {

@@ -108,6 +108,20 @@ def test_host_argument_checks(so):
     assert lib.moe_layer_decode_host_rows(fake, 1, ctypes.byref(bad_a), fake, 0, None, fake, 0, None) == -3
     assert lib.moe_layer_decode_host_rows(fake, 1, None, fake, 0, None, fake, 0, None) == -1
     assert lib.moe_layer_host_rows_workspace_bytes(ctypes.byref(bad), 1) == 0
+    # the expert prefetch hook: argument errors before any CUDA call; nothing to do is OK
+    pf = lib.moe_prefetch_experts
+    assert pf(None, fake, 4, 0, None) == -1
+    assert pf(ctypes.byref(ex), fake, -1, 0, None) == -1
+    assert pf(ctypes.byref(ex), fake, 1025, 0, None) == -2
+    assert pf(ctypes.byref(ex_bad_d), fake, 4, 0, None) == -2
+    assert pf(ctypes.byref(ex_odd), fake, 4, 0, None) == -3
+    assert pf(ctypes.byref(ex), None, 4, 0, None) == -1
+    assert pf(ctypes.byref(ex), ctypes.c_void_p(0x10002), 4, 0, None) == -3
+    assert pf(ctypes.byref(_lib._Experts(0, 4096, 14336, 0x10000, None, None, None)), fake, 4, 0, None) == -2
+    assert pf(ctypes.byref(_lib._Experts(8, 4096, 14336, None, None, None, None)), fake, 4, 0, None) == -1
+    assert pf(ctypes.byref(ex), None, 0, 0, None) == 0
+    # a byte cap below one expert's packed up projection leaves nothing to prefetch
+    assert pf(ctypes.byref(ex), fake, 4, lib.expert_int2_up_packed_bytes(4096, 14336) - 1, None) == 0
     # the timeout diagnostic: refused before anything is enqueued
     assert lib.moe_selftest_wait_timeout(None, 1 << 20, 10, None) == -1
     assert lib.moe_selftest_wait_timeout(fake, 1 << 20, 0, None) == -1

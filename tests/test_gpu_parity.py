@@ -643,6 +643,47 @@ def test_decode_up_projection_repeatable(B):
     assert differ == 0, f"{differ} of 300 calls gave a different v or mask"
 
 
+def test_prefetch_hook_leaves_results_unchanged():
+    """The inter-expert prefetch hook only moves the predicted experts' packed up
+    projections into L2: v and the masks are bit-identical with and without it, y agrees up
+    to the order of its fp32 additions, also when the prefetch runs on a second stream
+    beside the layer, with repeated, out-of-range and negative ids, and with a byte cap."""
+    d, f, E, k = 4096, 2048, 8, 2
+    de = synth.experts(E, d, f, 32, device="cuda")
+    ex = ses.Experts.from_dense(de.w_up, de.gate_t, de.down, torch.full((E,), 0.5, device="cuda"),
+                                interleave=True)
+    del de
+    layer = ses.Layer(synth.router(d, E, 32, device="cuda"), ex, k, True)
+    x = synth.tokens(1, d, 32, device="cuda")
+    ws = ses.Workspace(ses.layer_workspace_bytes(layer, 1))
+    y0, dbg = ses.layer_decode(x, layer, rmsnorm=True, ws=ws, debug=True)
+    y0, v0, m0 = y0.clone(), dbg["v"].clone(), dbg["mask"].clone()
+    assert int(dbg["mask"].ne(0).sum()) > 0
+    idx, _, _ = ses.route_topk(x, layer.w_router, k)
+    junk = torch.tensor([-1, E, 3, 3, 1000, int(idx[0, 0])], dtype=torch.int32, device="cuda")
+    per = ses.packed_bytes(d, f)
+
+    def check():
+        y, dbg = ses.layer_decode(x, layer, rmsnorm=True, ws=ws, debug=True)
+        assert torch.equal(dbg["v"], v0) and torch.equal(dbg["mask"], m0)
+        assert _same_up_to_sum_order(y, y0)
+
+    for ids, cap in [(idx, 0), (junk, 0), (torch.arange(E, dtype=torch.int32, device="cuda"), 3 * per),
+                     (idx, per - 1), (idx[:0], 0)]:
+        ses.prefetch_experts(ex, ids, max_bytes=cap)
+        check()
+    # beside the layer, on a second stream
+    side = torch.cuda.Stream()
+    for _ in range(5):
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            ses.prefetch_experts(ex, torch.arange(E, dtype=torch.int32, device="cuda"))
+        check()
+        torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+
+
 def test_decode_repeated_calls_share_the_workspace():
     """Many calls in a row on one workspace (the decode kernels reset their accumulator
     and counters) give the same output up to the order of the fp32 additions."""
