@@ -214,11 +214,11 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
 
 /*
  * moe_layer_path -- which kernels moe_layer_decode runs for this layer and B tokens on
- * the current device: 2 = the one-kernel decode path (one or two tokens, 8/16/32/64
- * routed experts, d <= 4096: one kernel routes, projects, thresholds, gathers the kept
- * rows and combines), 1 = the two-kernel decode path (the same shapes with
- * 4096 < d <= 6144: an up-projection kernel that also routes and a gather kernel that
- * also combines), 0 = the general path (router, up-projection, gather and combine
+ * the current device: 2 = the one-kernel decode path (one token, 8/16/32/64 routed
+ * experts, d <= 4096: one kernel routes, projects, thresholds, gathers the kept rows
+ * and combines), 1 = the two-kernel decode path (two tokens with those experts and
+ * d <= 6144, or one token with 4096 < d <= 6144: an up-projection kernel that also
+ * routes and a gather kernel that also combines), 0 = the general path (router, up-projection, gather and combine
  * kernels), or a negative moe_status_t for an invalid layer.  Every path computes the
  * same layer.  The general path is bitwise reproducible; on the decode paths the CTAs'
  * shares reach the fp32 sum of y in a varying order, so two calls can differ in the
@@ -240,8 +240,9 @@ int32_t moe_layer_path(const moe_layer_t* layer, int32_t B);
  *   ws / ws_bytes: at least moe_layer_host_rows_workspace_bytes(layer, B) bytes: the
  *     workspace of moe_layer_decode followed by a staging area for the kept rows (4d
  *     bytes per row, room for at least (B k + shared E) f rows: the dense worst case).
- * Only the decode path is supported (moe_layer_path(layer, B) == 1); other shapes
- * return MOE_ERR_UNSUPPORTED_SHAPE.  Three kernels run: the up-projection kernel, a
+ * Only the decode shapes are supported (moe_layer_path(layer, B) == 1 or 2; the
+ * two-kernel form runs either way); other shapes return MOE_ERR_UNSUPPORTED_SHAPE.
+ * Three kernels run: the up-projection kernel, a
  * fetch kernel that copies each kept row (4d bytes) from host memory into the staging
  * area, and the gather kernel, which streams the staging area.  dbg->events[2] marks
  * the start of the fetch kernel.  The host rows must not change while the call runs.

@@ -412,9 +412,9 @@ def layer_workspace_bytes(layer: Layer, B: int) -> int:
 
 
 def layer_path(layer: Layer, B: int) -> str:
-    """Which kernels layer_decode runs: 'decode_fused' (one or two tokens, d <= 4096: one
-    kernel), 'decode' (one or two tokens, wider d: an up kernel and a gather kernel) or
-    'general' (router, up, gather and combine kernels)."""
+    """Which kernels layer_decode runs: 'decode_fused' (one token, d <= 4096: one kernel),
+    'decode' (two tokens, or one token with 4096 < d <= 6144: an up kernel and a gather
+    kernel) or 'general' (router, up, gather and combine kernels)."""
     r = int(lib().moe_layer_path(ctypes.byref(layer.c_struct()), B))
     if r < 0:
         raise MoeError("moe_layer_path", r)

@@ -1907,7 +1907,10 @@ constexpr int kLyMinRowStages = kDecRows + 2;
 
 int decode_layer_plan(int B, int d, int E, int umax, int smem_optin, int& su, int& sr) {
   su = sr = 0;
-  if (d > 4096) return 0;
+  // one token, d <= 4096.  Two tokens take the two-kernel path: their up phase is twice
+  // as long, and the gather kernel's globally balanced rows then win (Mixtral-8x7B at
+  // 70 %: 85.6 against 96.3 us per layer)
+  if (d > 4096 || B != 1) return 0;
   const LyLayoutD z = ly_layout_d(d, B, E, 0, 0, umax);
   if (z.nwarps * 32 > kUpRegThreads || z.total + 1024 > (size_t)smem_optin) return 0;
   const size_t budget = (size_t)smem_optin - z.total - 256;
@@ -1938,11 +1941,11 @@ cudaError_t launch_decode_layer(const DecodeParams& p, cudaStream_t st, bool pdl
   const LyLayoutD L = ly_layout_d(p.d, p.B, p.routed.E, p.su, p.sr, p.umax);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_cfg(dim3(p.P), dim3(L.nwarps * 32), L.total, st, attr, pdl);
-  const void* fn = p.B == 1 ? (const void*)decode_layer_kernel<1> : (const void*)decode_layer_kernel<2>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+  if (p.B != 1) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute((const void*)decode_layer_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)L.total);
   if (e != cudaSuccess) return e;
-  if (p.B == 1) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<1>, p);
-  return cudaLaunchKernelEx(&cfg, decode_layer_kernel<2>, p);
+  return cudaLaunchKernelEx(&cfg, decode_layer_kernel<1>, p);
 }
 
 }  // namespace sesg

@@ -494,8 +494,9 @@ def test_layer_interleaved_gate_down(B):
 
 
 def test_layer_path_selection():
-    """One or two tokens with 8/16/32/64 routed experts take the decode path: one kernel
-    up to d = 4096, two up to d = 6144; other shapes take the general path."""
+    """One or two tokens with 8/16/32/64 routed experts take a decode path: one kernel for
+    one token up to d = 4096, else two kernels up to d = 6144; other shapes take the
+    general path."""
     def layer(d, f, E):
         de = synth.experts(E, d, f, 50)
         ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(),
@@ -503,11 +504,12 @@ def test_layer_path_selection():
         return ses.Layer(synth.router(d, E, 50).cuda(), ex, 2)
     small = layer(1024, 256, 8)
     assert ses.layer_path(small, 1) == "decode_fused"
-    assert ses.layer_path(small, 2) == "decode_fused"
+    assert ses.layer_path(small, 2) == "decode"
     assert ses.layer_path(small, 3) == "general"
     assert ses.layer_path(layer(1024, 256, 64), 1) == "decode_fused"
     assert ses.layer_path(layer(1024, 256, 128), 1) == "general"
-    assert ses.layer_path(layer(4096, 256, 8), 2) == "decode_fused"
+    assert ses.layer_path(layer(4096, 256, 8), 1) == "decode_fused"
+    assert ses.layer_path(layer(4096, 256, 8), 2) == "decode"
     assert ses.layer_path(layer(6144, 256, 8), 1) == "decode"
     assert ses.layer_path(layer(6400, 256, 8), 1) == "general"
 
@@ -715,7 +717,7 @@ def test_decode_workspace_shared_across_shapes():
     for rep in range(3):
         for li, lay in enumerate(layers):
             for B in (2, 1):
-                assert ses.layer_path(lay, B) == "decode_fused"
+                assert ses.layer_path(lay, B) == ("decode_fused" if B == 1 else "decode")
                 x = synth.tokens(B, lay.w_router.shape[0], 70 + 4 * rep + 2 * li + B).cuda()
                 got = ses.layer_decode(x, lay, ws=ws, rmsnorm=(B == 1)).clone()
                 fresh = ses.Workspace(ses.layer_workspace_bytes(lay, B))
