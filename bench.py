@@ -56,6 +56,10 @@ WORKLOADS = {
     # per-query time at 1K stored matrices of the Mixtral-8x7B shape (32 MoE layers x 8)
     "eamc-lookup": dict(L=32, E=8, capacity=1000, host_only=True),
 }
+# the further configurations the default run also times (every sparsity of the workload)
+FURTHER_POINTS = (("mixtral-8x7b-batch", (1, 2, 4, 8, 16, 32)),
+                  ("deepseek-v2-lite", (1, 2, 8, 64)),
+                  ("mixtral-8x22b-stack", (1, 8)))
 HEADLINE_PCT = 70
 N_LAYER_COPIES = 8
 METRIC = "MoE decode layer expert-tokens/s (Mixtral-8x7B-shaped layer, 1 token, 70% sparsity)"
@@ -82,6 +86,8 @@ def parse_args():
                     help="rotating layer copies (fewer: a small case for profiling; below 8 the "
                          "weights no longer exceed L2 by a wide margin)")
     ap.add_argument("--no-sweep", action="store_true", help="time only the headline sparsity")
+    ap.add_argument("--no-further", action="store_true",
+                    help="skip the further configurations in the default run's line")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=None,
                     help="time one of the further layer shapes instead of the headline")
     ap.add_argument("--tokens", type=int, default=None, help="with --workload: only this batch size")
@@ -714,6 +720,17 @@ def run_ours(args, world, rank, local):
 
     hook = prefetch_hook_times(layers, xs, ys, ws_list, stream, max(R * 50, args.steps // 4), args.warmup)
 
+    # the further configurations, measured in this run too (one GPU, replicas only)
+    further = []
+    if world == 1 and not args.no_further:
+        def keep(rec):
+            further.append({key: rec[key] for key in ("workload", "tokens", "sparsity_pct", "path", "layer_us",
+                                                      "expert_tokens_per_s", "bytes_per_step",
+                                                      "frac_of_measured_hbm", "kept_fraction",
+                                                      "layers_per_graph", "chained")})
+        for wname, toks in FURTHER_POINTS:
+            run_workload(args, world, rank, local, workload=wname, tokens=toks, emit=keep)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xs_o, wr_o, experts_o = oracle_prepare(dev, 2, table, pct)
@@ -751,6 +768,7 @@ def run_ours(args, world, rank, local):
                 "one_step_at_a_time": {"value": e2e_step_value, "unit": "expert-tokens/s",
                                        "how": "per step: copy in, one layer's graph, copy out, one stream"}},
         "prefetch_hook": hook,
+        "further_configs": further,
         "gpu_launches": {"decode_fused": 1, "decode": 2}.get(path, 4) * args.steps,
         "path": path,
         "clocks": clk.summary(),
@@ -759,19 +777,21 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
-def run_workload(args, world, rank, local):
+def run_workload(args, world, rank, local, workload=None, tokens=None, emit=None):
     """The further shapes: for every batch size and sparsity of the workload, the layer
     copies back to back in one CUDA graph (a stack: each copy's input is the previous
     copy's RMS-normalised output when `chained`, else its own tokens), timed on the
-    device; algorithmic bytes from the realised masks."""
+    device; algorithmic bytes from the realised masks.  One JSON line per point, or
+    one dict per point to `emit` (the default run's further configurations)."""
     import sparse_expert_swiglu_gb300 as ses
     from sparse_expert_swiglu_gb300 import synth
     ses.build_library()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    W = dict(WORKLOADS[args.workload])
+    name = workload or args.workload
+    W = dict(WORKLOADS[name])
     d, f, E, k, ns = W["d"], W["f"], W["E"], W["k"], W["shared"]
-    R = W["copies"] if args.copies == N_LAYER_COPIES else max(1, args.copies)
+    R = W["copies"] if (args.copies == N_LAYER_COPIES or workload) else max(1, args.copies)
     peak, peak_kind = measured_peaks()
     layers, tables = [], []
     xcal = synth.calibration_tokens(W["calib_tokens"], d, 7, device=dev)
@@ -825,13 +845,15 @@ def run_workload(args, world, rank, local):
                      (l.shared.gate_t.numel() * 4 + l.shared.up_packed.numel() if l.shared else 0)
                      for l in layers) / 1e9
     stream = torch.cuda.Stream()
-    for B in ([args.tokens] if args.tokens else W["tokens"]):
+    for B in (tokens if tokens else [args.tokens] if args.tokens else W["tokens"]):
         xs = [synth.tokens(B, d, 3000 + r + 100 * rank, device=dev) for r in range(R)]
         ys = [torch.empty_like(x) for x in xs]
         if W["chained"]:
             xs = [xs[0]] + ys[:-1]
         wss = [ses.Workspace(ws_bytes(layers[r], B), dev) for r in range(R)]
         path = "decode (host rows)" if host_rows else ses.layer_path(layers[0], B)
+        # the tokens and workspaces are written on the current stream
+        stream.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(stream):
             for r in range(R):
                 decode(xs[r], layers[r], rmsnorm=True, ws=wss[r], out=ys[r])
@@ -911,18 +933,23 @@ def run_workload(args, world, rank, local):
                 extra = {"link_bytes_per_step": link, "link_gbs": link / (us * 1e-6) / 1e9,
                          "h2d_copy_gbs": h2d_gbs, "frac_of_h2d_copy": link / (us * 1e-6) / 1e9 / h2d_gbs,
                          "h2d_copy_how": "1 GiB page-locked host -> device copy in this run, best of 3"}
-            if rank == 0:
-                print(json.dumps({
-                    "workload": args.workload, "tokens": B, "sparsity_pct": pct, "path": path, **extra,
+            rec = {
+                    "workload": name, "tokens": B, "sparsity_pct": pct, "path": path, **extra,
                     "layer_us": us, "expert_tokens_per_s": world * B * k * steps / secs,
                     "bytes_per_step": mean_bytes, "hbm_gbs": mean_bytes / (us * 1e-6) / 1e9,
                     "frac_of_measured_hbm": mean_bytes / (us * 1e-6) / 1e9 / peak, "peak_kind": peak_kind,
                     "kept_fraction": kept / max(cols, 1), "layers_per_graph": R, "chained": W["chained"],
                     "steps": steps, "weights_gb": weights_gb, "kernel_us": kt,
                     "config": {"d": d, "f": f, "experts": E, "top_k": k, "shared": ns,
-                               "calib_tokens": W["calib_tokens"]}}), flush=True)
+                               "calib_tokens": W["calib_tokens"]}}
+            if emit is not None:
+                emit(rec)
+            elif rank == 0:
+                print(json.dumps(rec), flush=True)
         del g, wss
         torch.cuda.empty_cache()
+    del layers, tables
+    torch.cuda.empty_cache()
 
 
 def run_eamc(args):

@@ -321,7 +321,9 @@ __device__ __forceinline__ void dec_route(const DecodeParams& p, int nthreads, c
         float s = 0.f;
 #pragma unroll 6
         for (int w = 0; w < nw; ++w) s += lred[(w * B + b) * E + e];
-        l[h] = s;
+        // a NaN logit (from a non-finite token) ranks as -inf: the ranks then stay a
+        // total order and the k chosen experts k distinct valid ones
+        l[h] = isnan(s) ? -INFINITY : s;
       }
     }
     // top-k by rank: an expert's rank counts the experts with a larger logit, or an

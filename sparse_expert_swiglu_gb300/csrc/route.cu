@@ -95,7 +95,10 @@ __device__ void router_topk(const RouteParams& p, int b, const float* logits, in
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int e = lane + 32 * i;
-    l[i] = e < p.E ? logits[e] : -INFINITY;
+    // a NaN logit (from a non-finite token) ranks as -inf, so that the k chosen experts
+    // are always k distinct valid ones
+    const float le = e < p.E ? logits[e] : -INFINITY;
+    l[i] = isnan(le) ? -INFINITY : le;
     taken[i] = e >= p.E;
   }
   float lmax = -INFINITY;

@@ -686,6 +686,37 @@ def test_prefetch_hook_leaves_results_unchanged():
     assert ws.status() == 0
 
 
+def test_nonfinite_tokens_keep_expert_ids_valid():
+    """A token with NaN or infinite entries (an overflow upstream) must not become an
+    invalid expert index: every router ranks a NaN logit as -inf, so each token's k
+    experts stay k distinct valid ones on all three paths, and the layer finishes with a
+    clean status (its output for such a token is not finite, as the oracle's would be)."""
+    for d, f, E, k, B, path in [(1024, 512, 8, 2, 1, "decode_fused"), (1024, 512, 8, 2, 2, "decode"),
+                                (256, 512, 8, 2, 4, "general")]:
+        de = synth.experts(E, d, f, 33, device="cuda")
+        ex = ses.Experts.from_dense(de.w_up, de.gate_t, de.down, torch.full((E,), 0.05, device="cuda"))
+        layer = ses.Layer(synth.router(d, E, 33, device="cuda"), ex, k, True)
+        assert ses.layer_path(layer, B) == path
+        x = synth.tokens(B, d, 33, device="cuda")
+        x[0] = float("nan")
+        if B > 1:
+            x[1, 5] = float("inf")
+            x[1, 6] = -float("inf")
+        for idx in (ses.route_topk(x, layer.w_router, k)[0], ses.route_topk_noalloc(x, layer.w_router, k)[0]):
+            idx = idx.cpu()
+            assert int(idx.min()) >= 0 and int(idx.max()) < E
+            assert all(len(set(row.tolist())) == k for row in idx)
+        ws = ses.Workspace(ses.layer_workspace_bytes(layer, B))
+        y, dbg = ses.layer_decode(x, layer, rmsnorm=False, ws=ws, debug=True)
+        idx = dbg["topk_idx"].cpu()
+        assert int(idx.min()) >= 0 and int(idx.max()) < E
+        assert all(len(set(row.tolist())) == k for row in idx)
+        assert ws.status() == 0
+        if B > 2:
+            # the other tokens are unaffected on the general path (own groups or exact sums)
+            assert torch.isfinite(y[2:].float()).all()
+
+
 def test_decode_repeated_calls_share_the_workspace():
     """Many calls in a row on one workspace (the decode kernels reset their accumulator
     and counters) give the same output up to the order of the fp32 additions."""
