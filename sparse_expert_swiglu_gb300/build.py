@@ -21,7 +21,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libsparse_expert_swiglu.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 SOURCES = ["pack.cu", "route.cu", "up.cu", "gather.cu", "combine.cu", "decode.cu", "fetch.cu", "api.cu",
-           "noalloc.cu", "selftest.cu", "prefetch.cu", "eam.cpp"]
+           "noalloc.cu", "selftest.cu", "prefetch.cu", "batched.cu",
+           "eam.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

@@ -54,6 +54,9 @@ int groups_max_routed(int B, int E, int k, int gcap) {
 struct WsLayout {
   size_t ctrl, groups, tok_groups, topk_idx, topk_w, group_total, unit_cnt, item_col, item_v,
       part, yacc, cta_total, klist, total;
+  // the batched path only (0 otherwise): dense v and masks, per-expert lists, h, outputs
+  size_t bv = 0, bmask = 0, seg_n = 0, seg_t = 0, seg_tok = 0, seg_slot = 0, seg_w = 0, seg_col = 0,
+         ht = 0, ypart = 0;
   int G_max, P3, list_cap;
 };
 
@@ -230,15 +233,13 @@ moe_status_t moe_route_topk(const uint16_t* x, int32_t B, int32_t d, const uint1
 
 // ---------------------------------------------------------------------------
 
-static moe_status_t run_experts(const uint16_t* x, int B, const moe_experts_t* routed,
-                                const moe_experts_t* shared, int n_slots, uint16_t* y,
-                                int rmsnorm, const moe_debug_t* dbg, void* ws,
-                                const WsLayout& L, const DeviceInfo& di, int max_tok,
-                                cudaStream_t st) {
-  Plan pl;
+static moe_status_t expert_params(const uint16_t* x, int B, const moe_experts_t* routed,
+                                  const moe_experts_t* shared, int n_slots, uint16_t* y, int rmsnorm,
+                                  const moe_debug_t* dbg, void* ws, const WsLayout& L, const DeviceInfo& di,
+                                  int max_tok, ExpertParams& p, Plan& pl) {
   moe_status_t s = plan(di, L, routed->d, routed->f, max_tok, pl);
   if (s != MOE_OK) return s;
-  ExpertParams p = {};
+  p = ExpertParams{};
   p.routed = to_set(*routed);
   if (shared && shared->E > 0) p.shared = to_set(*shared);
   p.x = reinterpret_cast<const __half*>(x);
@@ -263,6 +264,18 @@ static moe_status_t run_experts(const uint16_t* x, int B, const moe_experts_t* r
   p.list_cap = L.list_cap;
   p.G_max = L.G_max;
   p.max_tok = max_tok;
+  return MOE_OK;
+}
+
+static moe_status_t run_experts(const uint16_t* x, int B, const moe_experts_t* routed,
+                                const moe_experts_t* shared, int n_slots, uint16_t* y,
+                                int rmsnorm, const moe_debug_t* dbg, void* ws,
+                                const WsLayout& L, const DeviceInfo& di, int max_tok,
+                                cudaStream_t st) {
+  ExpertParams p;
+  Plan pl;
+  moe_status_t s = expert_params(x, B, routed, shared, n_slots, y, rmsnorm, dbg, ws, L, di, max_tok, p, pl);
+  if (s != MOE_OK) return s;
   cudaError_t e = record(dbg, 1, st);
   if (e == cudaSuccess) e = launch_up(p, pl.up_grid, st, true);
   if (e == cudaSuccess) e = record(dbg, 2, st);
@@ -326,11 +339,43 @@ static moe_status_t check_layer(const moe_layer_t* layer, int B) {
   return MOE_OK;
 }
 
+// The batched path applies: 16 to 64 tokens, d <= 4096, and at least 8 tokens per routed
+// expert on average (B k / E >= 8).  There the general path has to split most experts'
+// tokens into groups of 8 and read their kept rows once per group; with fewer tokens per
+// expert it measured faster (Mixtral-8x7B at 70 %: 16 tokens 474 against 554 us, 32 tokens
+// 720 against 675 us; DeepSeek-V2-Lite at 64 tokens, 6 per expert: 307-558 against
+// 362-540 us).
+static bool use_batched(const moe_layer_t* layer, int B) {
+  return B >= kBatchMinTok && B <= kBatchMaxTok && layer->routed.d <= 4096 &&
+         (long long)B * layer->k >= 8LL * layer->routed.E;
+}
+
 static WsLayout layer_layout(const moe_layer_t* layer, int B, int sms) {
   const int k = layer->k, E = layer->routed.E, ns = layer->shared.E;
   const int gcap = group_cap(layer->routed.d);
   const int G_max = groups_max_routed(B, E, k, gcap) + ns * ((B + gcap - 1) / gcap);
-  return ws_layout(B, B * k, G_max, layer->routed.d, layer->routed.f, sms);
+  WsLayout L = ws_layout(B, B * k, G_max, layer->routed.d, layer->routed.f, sms);
+  if (use_batched(layer, B)) {
+    const size_t d = layer->routed.d, f = layer->routed.f, S = k + ns, fw = (f + 31) / 32, nseg = E + ns;
+    size_t o = L.total;
+    auto take = [&](size_t bytes) {
+      const size_t at = o;
+      o = align_up(o + bytes, kWsAlign);
+      return at;
+    };
+    L.bv = take(4 * (size_t)B * S * f);
+    L.bmask = take(4 * (size_t)B * S * fw);
+    L.seg_n = take(4 * nseg);
+    L.seg_t = take(4 * nseg);
+    L.seg_tok = take(4 * nseg * kBatchMaxTok);
+    L.seg_slot = take(4 * nseg * kBatchMaxTok);
+    L.seg_w = take(4 * nseg * kBatchMaxTok);
+    L.seg_col = take(4 * nseg * f);
+    L.ht = take(2 * nseg * kBatchMaxTok * 2 * f);  // [nseg][4 groups][f][2][16] halves
+    L.ypart = take(4 * (size_t)batch_max_parts((int)f) * B * S * d);
+    L.total = o;
+  }
+  return L;
 }
 
 size_t moe_layer_workspace_bytes(const moe_layer_t* layer, int32_t B) {
@@ -363,7 +408,7 @@ int32_t moe_layer_path(const moe_layer_t* layer, int32_t B) {
   DeviceInfo di;
   if (device_info(di) != cudaSuccess) return MOE_ERR_CUDA;
   int su = 0, sr = 0, cap = 0, umax = 0;
-  if (!(B >= 1 && use_decode_path(layer, B, di, su, sr, cap, umax))) return 0;
+  if (!(B >= 1 && use_decode_path(layer, B, di, su, sr, cap, umax))) return use_batched(layer, B) ? 3 : 0;
   return use_layer_kernel(layer, B, di, umax, su, sr) ? 2 : 1;
 }
 
@@ -479,8 +524,59 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
   rp.G_max = L.G_max;
   if (record(dbg, 0, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_route(rp, st, true) != cudaSuccess) return MOE_ERR_CUDA;
-  return run_experts(x, B, &layer->routed, &layer->shared, k + layer->shared.E, y,
-                     rmsnorm_out ? 1 : 0, dbg, ws, L, di, B < rp.gcap ? B : rp.gcap, st);
+  const int n_slots = k + layer->shared.E;
+  const int max_tok = B < rp.gcap ? B : rp.gcap;
+  if (!use_batched(layer, B))
+    return run_experts(x, B, &layer->routed, &layer->shared, n_slots, y, rmsnorm_out ? 1 : 0, dbg, ws, L, di,
+                       max_tok, st);
+  // batched: the up kernel writes dense v and masks into the workspace, then the
+  // per-expert kept-row lists, the gate pass, the down pass and the final sum
+  ExpertParams p;
+  Plan pl;
+  s = expert_params(x, B, &layer->routed, &layer->shared, n_slots, y, rmsnorm_out ? 1 : 0, nullptr, ws, L, di,
+                    max_tok, p, pl);
+  if (s != MOE_OK) return s;
+  const size_t f = layer->routed.f, fw = (f + 31) / 32;
+  p.dbg_v = at<float>(ws, L.bv);
+  p.dbg_mask = at<uint32_t>(ws, L.bmask);
+  BatchParams bp = {};
+  bp.routed = p.routed;
+  bp.shared = p.shared;
+  bp.x = p.x;
+  bp.B = B;
+  bp.d = layer->routed.d;
+  bp.f = (int)f;
+  bp.k = k;
+  bp.n_shared = layer->shared.E;
+  bp.n_slots = n_slots;
+  bp.topk_idx = rp.topk_idx;
+  bp.topk_w = rp.topk_w;
+  bp.v = p.dbg_v;
+  bp.mask = p.dbg_mask;
+  bp.fw = (int)fw;
+  bp.seg_n = at<int>(ws, L.seg_n);
+  bp.seg_t = at<int>(ws, L.seg_t);
+  bp.seg_tok = at<int>(ws, L.seg_tok);
+  bp.seg_slot = at<int>(ws, L.seg_slot);
+  bp.seg_w = at<float>(ws, L.seg_w);
+  bp.seg_col = at<int>(ws, L.seg_col);
+  bp.ht = at<__half>(ws, L.ht);
+  bp.ypart = at<float>(ws, L.ypart);
+  bp.ctrl = at<Ctrl>(ws, L.ctrl);
+  bp.y = reinterpret_cast<__half*>(y);
+  bp.rmsnorm = rmsnorm_out ? 1 : 0;
+  cudaError_t e = record(dbg, 1, st);
+  if (e == cudaSuccess) e = launch_up(p, pl.up_grid, st, true);
+  if (e == cudaSuccess) e = record(dbg, 2, st);
+  if (e == cudaSuccess) e = launch_batched(bp, di.sms, st);
+  if (e == cudaSuccess) e = record(dbg, 3, st);
+  if (e == cudaSuccess) e = record(dbg, 4, st);
+  // the caller's copies of v and the masks
+  if (e == cudaSuccess && dbg && dbg->v)
+    e = cudaMemcpyAsync(dbg->v, p.dbg_v, 4 * (size_t)B * n_slots * f, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && dbg && dbg->mask)
+    e = cudaMemcpyAsync(dbg->mask, p.dbg_mask, 4 * (size_t)B * n_slots * fw, cudaMemcpyDeviceToDevice, st);
+  return cuda_status(e);
 }
 
 // Staging area of a host-rows call: one 4d-byte row for every entry the up CTAs' lists

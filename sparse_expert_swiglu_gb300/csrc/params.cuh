@@ -85,6 +85,32 @@ struct DecodeParams {
                             // the gather kernel then streams these instead of the experts
 };
 
+// The batched path (16 to 64 tokens): per-expert kept-row lists over the union of the
+// expert's tokens' masks, then a gate pass and a down pass that read every kept row
+// once per expert (batched.cu).
+struct BatchParams {
+  ExpertSet routed, shared;
+  const __half* x;          // [B][d]
+  int B, d, f, k, n_shared, n_slots;  // n_slots = k + n_shared
+  const int32_t* topk_idx;  // [B][k] the router's choice
+  const float* topk_w;      // [B][k]
+  const float* v;           // [B][n_slots][f] dense v of the up kernel
+  const uint32_t* mask;     // [B][n_slots][fw] mask words of the up kernel
+  int fw;                   // (f + 31) / 32
+  int* seg_n;               // [E + n_shared] kept rows of each expert
+  int* seg_t;               // [E + n_shared] its tokens
+  int* seg_tok;             // [E + n_shared][64] token, ascending
+  int* seg_slot;            // [E + n_shared][64] the token's slot for the expert
+  float* seg_w;             // [E + n_shared][64] combine weight (1 for shared experts)
+  int* seg_col;             // [E + n_shared][f] kept columns, ascending
+  __half* ht;               // [E + n_shared][4 groups][f][hi/lo][16 tokens] h as fp16 hi + lo
+  float* ypart;             // [parts][B][n_slots][d] each (token, slot)'s weighted expert
+                            // output, one row per 512-kept-row part of the expert
+  __half* y;                // [B][d]
+  int rmsnorm;
+  Ctrl* ctrl;               // status of a timed-out wait
+};
+
 __device__ __forceinline__ const ExpertSet& expert_set(const ExpertParams& p, int expert,
                                                        int& local) {
   if (expert < p.routed.E) {
@@ -125,5 +151,10 @@ int decode_layer_plan(int B, int d, int E, int umax, int smem_optin, int& su, in
 cudaError_t launch_decode_layer(const DecodeParams& p, cudaStream_t st, bool pdl);
 // fetch.cu
 cudaError_t launch_decode_fetch(const DecodeParams& p, cudaStream_t st, bool pdl);
+// batched.cu
+constexpr int kBatchMinTok = 16;  // the batched path serves 16 ..
+constexpr int kBatchMaxTok = 64;  // .. 64 tokens (and d <= 4096)
+int batch_max_parts(int f);
+cudaError_t launch_batched(const BatchParams& p, int P, cudaStream_t st);
 
 }  // namespace sesg

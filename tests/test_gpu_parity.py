@@ -341,6 +341,38 @@ def test_layer_ragged_with_shared():
     run_layer_case(768, 208, 4, 2, 9, 1, [0, 50, 101], seed=2)
 
 
+@pytest.mark.parametrize("B,pcts", [(20, [0, 50, 101]), (64, [50])])
+def test_layer_batched_ragged_with_shared(B, pcts):
+    """The batched path (16 to 64 tokens) on a ragged layer: d=768 (a partial 512-input
+    superblock, 3 slices of 256), f=208 (13 column tiles: an odd number, so the last mask
+    word is half written; 4 row tiles of 64 with a short last one), 4 experts top-2 (up to
+    64 tokens per expert), one shared expert serving every token."""
+    run_layer_case(768, 208, 4, 2, B, 1, pcts, seed=21)
+
+
+def test_layer_batched_d2048_shared():
+    """The batched path at d = 2048 (one 2048-column chunk over 16 warps), f = 1408 as in
+    DeepSeek-V2-Lite, 8 routed experts top-2 and 2 shared experts, 32 tokens (8 per routed
+    expert on average, 32 per shared expert: two groups of 16)."""
+    run_layer_case(2048, 1408, 8, 2, 32, 2, [0, 90], seed=23, gen_device="cuda")
+
+
+def test_layer_batched_reproducible():
+    """The batched path sums in fixed orders: two calls give identical bits."""
+    d, f, E, k, B = 1024, 512, 8, 2, 32
+    de = synth.experts(E, d, f, 22)
+    ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(),
+                                torch.full((E,), 0.05, dtype=torch.float32).cuda(), interleave=True)
+    layer = ses.Layer(synth.router(d, E, 22).cuda(), ex, k)
+    assert ses.layer_path(layer, B) == "batched"
+    x = synth.tokens(B, d, 22).cuda()
+    ws = ses.Workspace(ses.layer_workspace_bytes(layer, B))
+    y1 = ses.layer_decode(x, layer, ws=ws, rmsnorm=True).clone()
+    y2 = ses.layer_decode(x, layer, ws=ws, rmsnorm=True)
+    assert torch.equal(y1, y2)
+    assert ws.status() == 0
+
+
 def test_layer_deepseek_v2_lite_shape():
     """d=2048, f=1408, 64 routed experts top-6, 2 shared experts."""
     run_layer_case(2048, 1408, 64, 6, 8, 2, [0, 50, 90], seed=3, gen_device="cuda")
@@ -372,8 +404,8 @@ def _drop_big_oracle():
 
 @pytest.mark.parametrize("B", [16, 32])
 def test_layer_mixtral_8x7b_batch_sweep(B):
-    """The Mixtral-8x7B batch sweep's largest batches (16 and 32 tokens, 70 %: the general
-    path), one set of experts for both."""
+    """The Mixtral-8x7B batch sweep's largest batches (70 %): 16 tokens on the general path,
+    32 tokens (8 per expert) on the batched path; one set of experts for both."""
     run_layer_case(4096, 14336, 8, 2, B, 0, [70], seed=8, gen_device="cuda", oracle_cache=_BIG_ORACLE)
 
 
@@ -512,6 +544,14 @@ def test_layer_path_selection():
     assert ses.layer_path(layer(4096, 256, 8), 2) == "decode"
     assert ses.layer_path(layer(6144, 256, 8), 1) == "decode"
     assert ses.layer_path(layer(6400, 256, 8), 1) == "general"
+    # 16 to 64 tokens with d <= 4096 and at least 8 tokens per routed expert on average:
+    # the batched path
+    assert ses.layer_path(small, 8) == "general"
+    assert ses.layer_path(small, 16) == "general"
+    assert ses.layer_path(small, 32) == "batched"
+    assert ses.layer_path(small, 64) == "batched"
+    assert ses.layer_path(small, 65) == "general"
+    assert ses.layer_path(layer(6144, 256, 8), 16) == "general"
 
 
 def _same_up_to_sum_order(a, b):
