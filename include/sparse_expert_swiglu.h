@@ -219,7 +219,7 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
  * and combines), 1 = the two-kernel decode path (two tokens with those experts and
  * d <= 6144, or one token with 4096 < d <= 6144: an up-projection kernel that also
  * routes and a gather kernel that also combines), 3 = the batched path (16 to 64
- * tokens, d <= 4096, B k >= 8 E: the router and the up-projection kernel, then per expert the
+ * tokens, d <= 4096, B k >= 6 E: the router and the up-projection kernel, then per expert the
  * union of its tokens' masks as one kept-row list, a gate pass and a down pass that read
  * every kept row once per expert, and a per-token sum; bitwise reproducible), 0 = the
  * general path (router, up-projection, gather and combine

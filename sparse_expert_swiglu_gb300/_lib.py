@@ -414,7 +414,7 @@ def layer_workspace_bytes(layer: Layer, B: int) -> int:
 def layer_path(layer: Layer, B: int) -> str:
     """Which kernels layer_decode runs: 'decode_fused' (one token, d <= 4096: one kernel),
     'decode' (two tokens, or one token with 4096 < d <= 6144: an up kernel and a gather
-    kernel), 'batched' (16 to 64 tokens, d <= 4096, at least 8 tokens per routed expert
+    kernel), 'batched' (16 to 64 tokens, d <= 4096, at least 6 tokens per routed expert
     on average: router, up kernel, then per-expert kept-row lists and gate and down passes
     that read each kept row once per expert) or
     'general' (router, up, gather and combine kernels)."""

@@ -339,15 +339,15 @@ static moe_status_t check_layer(const moe_layer_t* layer, int B) {
   return MOE_OK;
 }
 
-// The batched path applies: 16 to 64 tokens, d <= 4096, and at least 8 tokens per routed
-// expert on average (B k / E >= 8).  There the general path has to split most experts'
-// tokens into groups of 8 and read their kept rows once per group; with fewer tokens per
-// expert it measured faster (Mixtral-8x7B at 70 %: 16 tokens 474 against 554 us, 32 tokens
-// 720 against 675 us; DeepSeek-V2-Lite at 64 tokens, 6 per expert: 307-558 against
-// 362-540 us).
+// The batched path applies: 16 to 64 tokens, d <= 4096, and at least 6 tokens per routed
+// expert on average (B k / E >= 6).  There the general path splits many experts' tokens
+// (and every shared expert's) into groups of 8 and reads their kept rows once per group.
+// Measured per layer, general against batched: Mixtral-8x7B at 70 %, 16 tokens (4 per
+// expert) 474 against 495 us, 32 tokens 720 against 622 us; DeepSeek-V2-Lite at 64 tokens
+// (6 per expert) 558 / 530 / 307 against 493 / 490 / 335 us at 0 / 50 / 90 %.
 static bool use_batched(const moe_layer_t* layer, int B) {
   return B >= kBatchMinTok && B <= kBatchMaxTok && layer->routed.d <= 4096 &&
-         (long long)B * layer->k >= 8LL * layer->routed.E;
+         (long long)B * layer->k >= 6LL * layer->routed.E;
 }
 
 static WsLayout layer_layout(const moe_layer_t* layer, int B, int sms) {

@@ -236,31 +236,33 @@ __global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(Ba
     nr = min(kBtTileRows, K - r0);
   };
   if (warp == ncw) {
-    // ---- producer: the gate rows of this CTA's tiles, in order
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      int s = 0, ph = 0, issued = 0;
-      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        int e, g, r0, nr, el;
-        tile_of(tile, e, g, r0, nr);
-        const ExpertSet& es = bt_set(p, e, el);
-        const __half* gbase = es.gate_t + (size_t)el * es.f * es.rs;
-        for (int r = 0; r < nr; ++r) {
-          if (issued >= kGateST && !mbar_wait(&empty[s], ph ^ 1)) {
-            atomicExch(&s_abort, 1);
-            break;
-          }
-          if (*reinterpret_cast<volatile int*>(&s_abort)) break;
-          const int col = p.seg_col[(size_t)e * f + r0 + r];
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * d));
-          bulk_g2s(ring + (size_t)s * stage_b, gbase + (size_t)col * es.rs, (uint32_t)(2 * d), &full[s], pol);
-          ++issued;
-          if (++s == kGateST) {
-            s = 0;
-            ph ^= 1;
+    // ---- producer: the gate rows of this CTA's tiles, in order, in the consumers'
+    // batches of 8: lane i copies the batch's row i into its own stage
+    const uint64_t pol = policy_evict_first();
+    int issued = 0;
+    bool stop = false;
+    for (int tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x) {
+      int e, g, r0, nr, el;
+      tile_of(tile, e, g, r0, nr);
+      const ExpertSet& es = bt_set(p, e, el);
+      const __half* gbase = es.gate_t + (size_t)el * es.f * es.rs;
+      for (int rb = 0; rb < nr && !stop; rb += kGateBatch) {
+        const int cnt = min(kGateBatch, nr - rb);
+        bool ok = !*reinterpret_cast<volatile int*>(&s_abort);
+        if (ok && lane < cnt) {
+          const int q = issued + lane, st = q % kGateST;
+          if (q >= kGateST) ok = mbar_wait(&empty[st], ((q / kGateST) & 1) ^ 1);
+          if (ok) {
+            const int col = p.seg_col[(size_t)e * f + r0 + rb + lane];
+            mbar_arrive_expect_tx(&full[st], (uint32_t)(2 * d));
+            bulk_g2s(ring + (size_t)st * stage_b, gbase + (size_t)col * es.rs, (uint32_t)(2 * d), &full[st], pol);
           }
         }
-        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) atomicExch(&s_abort, 1);
+          stop = true;
+        }
+        issued += cnt;
       }
     }
   } else {
@@ -451,37 +453,43 @@ __global__ void __launch_bounds__((kDownWarps + 1) * 32, 1) batch_down_kernel(Ba
     re = min(K, rb + kBtPartRows);
   };
   if (warp == ncw) {
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      int s = 0, ph = 0, issued = 0;
-      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        int e, g, c, part, rb, re, el;
-        tile_of(tile, e, g, c, part, rb, re);
-        const ExpertSet& es = bt_set(p, e, el);
-        const __half* dbase = es.down + (size_t)el * es.f * es.rs + (size_t)c * W;
-        for (int r0 = rb; r0 < re; r0 += kDownRowsB) {
-          if (issued >= kDownST && !mbar_wait(&empty[s], ph ^ 1)) {
-            atomicExch(&s_abort, 1);
-            break;
-          }
-          if (*reinterpret_cast<volatile int*>(&s_abort)) break;
-          uint8_t* st = ring + (size_t)s * stage_b;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(kDownRowsB * 2 * W + 2 * kBtGroupTok * 2 * kDownRowsB));
-          for (int i = 0; i < kDownRowsB; ++i) {
-            // rows past the part's end (only at K): a real row with h = 0 (finite * 0)
-            const int r = r0 + i < re ? r0 + i : re - 1;
-            const int col = p.seg_col[(size_t)e * f + r];
-            bulk_g2s(st + (size_t)i * row_b, dbase + (size_t)col * es.rs, (uint32_t)(2 * W), &full[s], pol);
-          }
+    // ---- producer: per batch, lane 0 arms the stage, then lanes 0-15 copy one row each
+    // and lane 16 the batch's h
+    const uint64_t pol = policy_evict_first();
+    int s = 0, ph = 0, issued = 0;
+    bool stop = false;
+    for (int tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x) {
+      int e, g, c, part, rb, re, el;
+      tile_of(tile, e, g, c, part, rb, re);
+      const ExpertSet& es = bt_set(p, e, el);
+      const __half* dbase = es.down + (size_t)el * es.f * es.rs + (size_t)c * W;
+      for (int r0 = rb; r0 < re && !stop; r0 += kDownRowsB) {
+        bool ok = !*reinterpret_cast<volatile int*>(&s_abort);
+        if (lane == 0 && ok) {
+          if (issued >= kDownST) ok = mbar_wait(&empty[s], ph ^ 1);
+          if (ok)
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(kDownRowsB * 2 * W + 2 * kBtGroupTok * 2 * kDownRowsB));
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+          if (lane == 0) atomicExch(&s_abort, 1);
+          stop = true;
+          break;
+        }
+        uint8_t* st = ring + (size_t)s * stage_b;
+        if (lane < kDownRowsB) {
+          // rows past the part's end (only at K): a real row with h = 0 (finite * 0)
+          const int r = r0 + lane < re ? r0 + lane : re - 1;
+          const int col = p.seg_col[(size_t)e * f + r];
+          bulk_g2s(st + (size_t)lane * row_b, dbase + (size_t)col * es.rs, (uint32_t)(2 * W), &full[s], pol);
+        } else if (lane == kDownRowsB) {
           bulk_g2s(st + kDownRowsB * row_b, p.ht + bt_ht_index(e, g, f, r0),
                    (uint32_t)(2 * kBtGroupTok * 2 * kDownRowsB), &full[s], pol);
-          ++issued;
-          if (++s == kDownST) {
-            s = 0;
-            ph ^= 1;
-          }
         }
-        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
+        ++issued;
+        if (++s == kDownST) {
+          s = 0;
+          ph ^= 1;
+        }
       }
     }
   } else {

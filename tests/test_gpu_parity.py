@@ -412,7 +412,7 @@ def test_layer_mixtral_8x7b_batch_sweep(B):
 @pytest.mark.parametrize("B", [16, 32, 64])
 def test_layer_deepseek_v2_lite_batches(B):
     """DeepSeek-V2-Lite shape (64 experts top-6, 2 shared experts) at 16, 32 and 64 tokens,
-    0 % and 90 %."""
+    0 % and 90 % (16 and 32 tokens on the general path, 64 on the batched path)."""
     run_layer_case(2048, 1408, 64, 6, B, 2, [0, 90], seed=9, gen_device="cuda", oracle_cache=_BIG_ORACLE)
 
 
@@ -544,10 +544,11 @@ def test_layer_path_selection():
     assert ses.layer_path(layer(4096, 256, 8), 2) == "decode"
     assert ses.layer_path(layer(6144, 256, 8), 1) == "decode"
     assert ses.layer_path(layer(6400, 256, 8), 1) == "general"
-    # 16 to 64 tokens with d <= 4096 and at least 8 tokens per routed expert on average:
+    # 16 to 64 tokens with d <= 4096 and at least 6 tokens per routed expert on average:
     # the batched path
     assert ses.layer_path(small, 8) == "general"
     assert ses.layer_path(small, 16) == "general"
+    assert ses.layer_path(small, 24) == "batched"
     assert ses.layer_path(small, 32) == "batched"
     assert ses.layer_path(small, 64) == "batched"
     assert ses.layer_path(small, 65) == "general"
