@@ -19,7 +19,7 @@
 //                         through a TMA ring; 16 warps form x . gate for a batch of
 //                         rows (one barrier per batch), h = SiLU(.) * v * router
 //                         weight, acc += h * down; each CTA adds its share of y to
-//                         one of four fp32 accumulator copies with vector atomics
+//                         the fp32 accumulator (kDecYRep copies) with vector atomics
 //                         (fewer additions per address) and the last CTA to
 //                         finish rounds y to fp16 once, after the RMSNorm of stacked
 //                         layers.
