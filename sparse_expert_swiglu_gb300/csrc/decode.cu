@@ -41,7 +41,10 @@ namespace {
 constexpr int kDecMaxG = 24;     // groups: 2 tokens x 8 experts + 8 shared experts
 constexpr int kDecMaxE = 64;     // routed experts of the in-kernel router
 constexpr int kDecMaxSb = 12;    // superblocks of 512 inputs (d <= 6144)
-constexpr int kDecNV = 4;        // unit slots of superblock partials (a power of two)
+// unit slots of superblock partials (a power of two): the up warps run up to kDecNV units
+// ahead of the finalize warps; 2 measured faster than 4 (Mixtral-8x7B one-token layer at
+// 70 %: 44.47 against 44.73 us), 8 does not fit the one-kernel layer's shared memory
+constexpr int kDecNV = 2;
 constexpr int kDecMaxSu = 12;    // up-ring stages
 constexpr int kDecMaxSr = 16;    // row-ring stages
 constexpr int kDecMaxUnits = 128;  // units per CTA
@@ -682,7 +685,7 @@ __device__ __forceinline__ void dec_finalize_units(const DecodeParams& p, const 
   float thr = 0.f;
   for (int j = fl; j < n; j += NL) {
     const int slot = j & (kDecNV - 1);
-    if (!__all_sync(0xffffffffu, mbar_wait(&S.vfull[slot], (j >> 2) & 1))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&S.vfull[slot], (j / kDecNV) & 1))) {
       if (lane == 0) dec_fail(p, S.abort);
       break;
     }
@@ -752,7 +755,7 @@ __device__ __forceinline__ void dec_up_units(const DecodeParams& p, const UpShar
     else
       dec_phases<B, 0, false>(w, xr, sz, xgw, ng, vacc);
     // the slot's previous unit must have been finalized
-    if (j >= kDecNV && !__all_sync(0xffffffffu, mbar_wait(&S.vfree[slot], ((j >> 2) - 1) & 1))) {
+    if (j >= kDecNV && !__all_sync(0xffffffffu, mbar_wait(&S.vfree[slot], ((j / kDecNV) - 1) & 1))) {
       if (lane == 0) dec_fail(p, S.abort);
       break;
     }
