@@ -46,9 +46,16 @@ constexpr int kDecMaxSb = 12;    // superblocks of 512 inputs (d <= 6144)
 // 70 %: 44.47 against 44.73 us), 8 does not fit the one-kernel layer's shared memory
 constexpr int kDecNV = 2;
 constexpr int kDecMaxSu = 12;    // up-ring stages
-constexpr int kDecMaxSr = 16;    // row-ring stages
+constexpr int kDecMaxSr = 16;    // row-ring stages (the h warp's descriptor ring needs kDecMaxSr + 3 kDecRows <= kHD)
 constexpr int kDecMaxUnits = 128;  // units per CTA
 constexpr int kDecRows = 4;      // kept rows per gather batch
+// producer lanes that issue the kept rows' bulk copies, in rounds of one row per lane: one
+// thread issues about 2.8 bulk copies per us whatever their size (measured on all SMs at
+// once: 8 KB copies 22.7 GB/s per SM from one lane, 33-38 GB/s from four).  Two lanes
+// measured best on the one-token Mixtral-8x7B layer (70 %: 42.7 us, four lanes 42.9-43.3,
+// one 44.4); rounds aligned to the gather batches or lanes that run independently of
+// each other were slower.
+constexpr int kRowLanes = 2;
 constexpr int kDecMaxGw = 24;    // gather warps
 // up kernel: two unit lanes of up to 8 superblock warps (d <= 4096) or one lane of up to 12,
 // plus the strip producer and one finalize warp per lane
@@ -1056,40 +1063,48 @@ __global__ void __launch_bounds__(MAXT, 1) decode_gather_kernel(DecodeParams p) 
   }
   __syncthreads();
   if (warp == ngw) {
-    // ---- producer warp: the kept rows, in order
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      int s = 0, ph = 0;
-      for (int i = 0; i < nrows; ++i) {
-        if (i >= SR && !mbar_wait(&empty[s], ph ^ 1)) {
-          dec_fail(p, &m->abort);
-          break;
-        }
-        if (vload(&m->abort)) break;
+    // ---- producer warp: the kept rows, in order, in rounds of up to kRowLanes rows (one
+    // per lane); a round is issued only once every lane has its row's stage, so the
+    // issued rows stay contiguous
+    const uint64_t pol = policy_evict_first();
+    int s = 0, ph = 0;  // stage and parity of row i0
+    for (int i0 = 0; i0 < nrows; i0 += kRowLanes) {
+      const int nr = min(kRowLanes, nrows - i0);
+      int sq = s + lane, pq = ph;
+      if (sq >= SR) {
+        sq -= SR;
+        pq ^= 1;
+      }
+      const bool w = lane >= nr || i0 + lane < SR || mbar_wait(&empty[sq], pq ^ 1);
+      if (!__all_sync(0xffffffffu, w && !vload(&m->abort))) {
+        if (lane == 0) dec_fail(p, &m->abort);
+        break;
+      }
+      if (lane < nr) {
+        uint8_t* st = ring + (size_t)sq * L.row;
         if constexpr (STAGED) {
           // rows copied from host memory: row a + i of the staging area
-          uint8_t* st = ring + (size_t)s * L.row;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)L.row);
-          bulk_g2s(st, p.staging + (size_t)(a + i) * (4 * d), (uint32_t)(4 * d), &full[s], pol);
+          mbar_arrive_expect_tx(&full[sq], (uint32_t)L.row);
+          bulk_g2s(st, p.staging + (size_t)(a + i0 + lane) * (4 * d), (uint32_t)(4 * d), &full[sq], pol);
         } else {
-          const GaRow gr = list[i];
+          const GaRow gr = list[i0 + lane];
           int el;
           const ExpertSet& es = dec_set(p, grp[gr.g].expert, el);
           const size_t roff = ((size_t)el * es.f + gr.col) * es.rs;
-          uint8_t* st = ring + (size_t)s * L.row;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)L.row);
+          mbar_arrive_expect_tx(&full[sq], (uint32_t)L.row);
           if (es.rs == 2 * d) {
-            bulk_g2s(st, es.gate_t + roff, (uint32_t)(4 * d), &full[s], pol);
+            bulk_g2s(st, es.gate_t + roff, (uint32_t)(4 * d), &full[sq], pol);
           } else {
-            bulk_g2s(st, es.gate_t + roff, (uint32_t)(2 * d), &full[s], pol);
-            bulk_g2s(st + 2 * d, es.down + roff, (uint32_t)(2 * d), &full[s], pol);
+            bulk_g2s(st, es.gate_t + roff, (uint32_t)(2 * d), &full[sq], pol);
+            bulk_g2s(st + 2 * d, es.down + roff, (uint32_t)(2 * d), &full[sq], pol);
           }
         }
-        m->issued = i + 1;
-        if (++s == SR) {
-          s = 0;
-          ph ^= 1;
-        }
+      }
+      if (lane == 0) m->issued = i0 + nr;
+      s += nr;
+      if (s >= SR) {
+        s -= SR;
+        ph ^= 1;
       }
     }
   } else {
@@ -1282,6 +1297,7 @@ namespace {
 
 constexpr int kHB = 4;   // gather batches in flight between the gather warps and the h warp
 constexpr int kHD = 64;  // row descriptors kept for the h warp (rows ahead of it: < SR + 3 kDecRows)
+static_assert(kDecMaxSr + 3 * kDecRows <= kHD, "the row producer may run kDecMaxSr + 3 kDecRows rows ahead of the h warp");
 
 // Sums of v[q][b] over the warp's lanes by recursive halving (one value kept per lane
 // and round): for one token lane 8q + i ends with row q, for two tokens lane 8q + 4b + i
@@ -1503,55 +1519,64 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
     // them, in unit order.  It first adds the unit's rows to the known count (the gather
     // warps size their batches by it), and sets allknown after the last unit.  A stage's
     // first use: its own stages at once, those in the strip ring's space once the up phase
-    // is over; later uses: once the gather warps have released it.
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      int rs = 0, rph = 0, issued = 0, known = 0;
-      bool ok = true;
-      for (int j = 0; j < n && ok; ++j) {
-        if (!mbar_wait(&ufin[j], 0)) {
+    // is over; later uses: once the gather warps have released it.  Rows go out in rounds
+    // of up to kRowLanes, one per lane: every lane waits for its row's stage, and the round
+    // is issued only if all of them got theirs, so the issued rows stay contiguous.
+    const uint64_t pol = policy_evict_first();
+    int rs = 0, rph = 0, issued = 0, known = 0;  // stage and parity of row `issued`
+    bool ok = true;
+    for (int j = 0; j < n && ok; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&ufin[j], 0))) {
+        ok = false;
+        break;
+      }
+      const int c = m->ucnt[j];
+      if (c == 0) continue;
+      known += c;
+      if (lane == 0) *reinterpret_cast<volatile int*>(&m->known) = known;
+      // the unit's expert rows (every entry of a unit has the same group)
+      const int g = ent[j * 16].x >> 16;
+      int el;
+      const ExpertSet& es = dec_set(p, grp[g].expert, el);
+      const size_t rsb = (size_t)es.rs * 2;
+      const uint8_t* gbase = reinterpret_cast<const uint8_t*>(es.gate_t + (size_t)el * es.f * es.rs);
+      const uint8_t* dbase = reinterpret_cast<const uint8_t*>(es.down + (size_t)el * es.f * es.rs);
+      const bool inter = es.rs == 2 * d;
+      for (int r0 = 0; r0 < c; r0 += kRowLanes) {
+        const int nr = min(kRowLanes, c - r0);
+        int sq = rs + lane, pq = rph;  // this lane's row issued + lane
+        if (sq >= SR) {
+          sq -= SR;
+          pq ^= 1;
+        }
+        bool w = true;
+        if (lane < nr) w = issued + lane >= SR ? mbar_wait(&rempty[sq], pq ^ 1) : (sq < SR1 || mbar_wait(updone, 0));
+        if (!__all_sync(0xffffffffu, w && !vload(&m->abort))) {
           ok = false;
           break;
         }
-        const int c = m->ucnt[j];
-        if (c == 0) continue;
-        known += c;
-        *reinterpret_cast<volatile int*>(&m->known) = known;
-        // the unit's expert rows (every entry of a unit has the same group)
-        const int g = ent[j * 16].x >> 16;
-        int el;
-        const ExpertSet& es = dec_set(p, grp[g].expert, el);
-        const size_t rsb = (size_t)es.rs * 2;
-        const uint8_t* gbase = reinterpret_cast<const uint8_t*>(es.gate_t + (size_t)el * es.f * es.rs);
-        const uint8_t* dbase = reinterpret_cast<const uint8_t*>(es.down + (size_t)el * es.f * es.rs);
-        const bool inter = es.rs == 2 * d;
-        for (int r = 0; r < c; ++r) {
-          if (vload(&m->abort)) {
-            ok = false;
-            break;
-          }
-          if (issued >= SR ? !mbar_wait(&rempty[rs], rph ^ 1) : (rs >= SR1 && !mbar_wait(updone, 0))) {
-            ok = false;
-            break;
-          }
-          const int4 e = ent[j * 16 + r];
+        if (lane < nr) {
+          const int4 e = ent[j * 16 + r0 + lane];
           const size_t off = (size_t)(e.x & 0xffff) * rsb;
-          uint8_t* st = rstage(rs);
-          hdesc[issued & (kHD - 1)] = e;
-          mbar_arrive_expect_tx(&rfull[rs], (uint32_t)L.row);
+          uint8_t* st = rstage(sq);
+          hdesc[(issued + lane) & (kHD - 1)] = e;
+          mbar_arrive_expect_tx(&rfull[sq], (uint32_t)L.row);
           if (inter) {
-            bulk_g2s(st, gbase + off, (uint32_t)(4 * d), &rfull[rs], pol);
+            bulk_g2s(st, gbase + off, (uint32_t)(4 * d), &rfull[sq], pol);
           } else {
-            bulk_g2s(st, gbase + off, (uint32_t)(2 * d), &rfull[rs], pol);
-            bulk_g2s(st + 2 * d, dbase + off, (uint32_t)(2 * d), &rfull[rs], pol);
-          }
-          ++issued;
-          if (++rs == SR) {
-            rs = 0;
-            rph ^= 1;
+            bulk_g2s(st, gbase + off, (uint32_t)(2 * d), &rfull[sq], pol);
+            bulk_g2s(st + 2 * d, dbase + off, (uint32_t)(2 * d), &rfull[sq], pol);
           }
         }
+        issued += nr;
+        rs += nr;
+        if (rs >= SR) {
+          rs -= SR;
+          rph ^= 1;
+        }
       }
+    }
+    if (lane == 0) {
       m->rissued = issued;
       if (ok) {
         __threadfence_block();
