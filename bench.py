@@ -929,7 +929,9 @@ def run_workload(args, world, rank, local, workload=None, tokens=None, emit=None
                      ["event_pair_us", "decode_up_kernel", "decode_gather_kernel", "event_pair_us_2"]
                      if path == "decode" else
                      ["event_pair_us", "decode_layer_kernel", "event_pair_us_2", "event_pair_us_3"]
-                     if path == "decode_fused" else ["route_kernel", "up_kernel", "gather_kernel", "combine_kernel"])
+                     if path == "decode_fused" else
+                     ["event_pair_us", "first_pair", "other_pairs", "event_pair_us_2"]
+                     if path == "decode_pairs" else ["route_kernel", "up_kernel", "gather_kernel", "combine_kernel"])
             kt = {nm: float(v) / 10 for nm, v in zip(names, kacc)}
             extra = {}
             if host_rows:

@@ -205,7 +205,8 @@ moe_status_t moe_expert_sparse_swiglu(const uint16_t* x, int32_t n, const moe_ex
  *   x fp16 [B][d];  y out fp16 [B][d] (may not alias x);  layer: host pointer to the
  *   description (its tensor members are device pointers);  dbg: optional.
  *   ws / ws_bytes: at least moe_layer_workspace_bytes(layer, B) bytes, 256-byte
- *   aligned, zero-filled once before its first use (moe_workspace_init).
+ *   aligned, zero-filled once before its first use (moe_workspace_init).  Calls with
+ *   different B may share a workspace that is large enough for each of them.
  */
 size_t moe_layer_workspace_bytes(const moe_layer_t* layer, int32_t B);
 moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* layer, uint16_t* y,
@@ -221,8 +222,11 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
  * routes and a gather kernel that also combines), 3 = the batched path (16 to 64
  * tokens, d <= 4096, B k >= 6 E: the router and the up-projection kernel, then per expert the
  * union of its tokens' masks as one kept-row list, a gate pass and a down pass that read
- * every kept row once per expert, and a per-token sum; bitwise reproducible), 0 = the
- * general path (router, up-projection, gather and combine
+ * every kept row once per expert, and a per-token sum; bitwise reproducible), 4 = the
+ * decode path in pairs (three to six tokens of a shape that paths 1 and 2 take: tokens
+ * 2i and 2i + 1 through the decode path, one call after the other, the last token of an
+ * odd count alone; the tokens are independent, and two pairs that route to one expert
+ * read its rows twice), 0 = the general path (router, up-projection, gather and combine
  * kernels), or a negative moe_status_t for an invalid layer.  Every path computes the
  * same layer.  The general path is bitwise reproducible; on the decode paths the CTAs'
  * shares reach the fp32 sum of y in a varying order, so two calls can differ in the

@@ -416,12 +416,13 @@ def layer_path(layer: Layer, B: int) -> str:
     'decode' (two tokens, or one token with 4096 < d <= 6144: an up kernel and a gather
     kernel), 'batched' (16 to 64 tokens, d <= 4096, at least 6 tokens per routed expert
     on average: router, up kernel, then per-expert kept-row lists and gate and down passes
-    that read each kept row once per expert) or
+    that read each kept row once per expert), 'decode_pairs' (three to six tokens of a
+    shape the decode path takes: two at a time through it) or
     'general' (router, up, gather and combine kernels)."""
     r = int(lib().moe_layer_path(ctypes.byref(layer.c_struct()), B))
     if r < 0:
         raise MoeError("moe_layer_path", r)
-    return {1: "decode", 2: "decode_fused", 3: "batched"}.get(r, "general")
+    return {1: "decode", 2: "decode_fused", 3: "batched", 4: "decode_pairs"}.get(r, "general")
 
 
 def layer_decode(x: torch.Tensor, layer: Layer, rmsnorm: bool = False,

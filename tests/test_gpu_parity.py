@@ -388,9 +388,44 @@ def test_layer_mixtral_8x7b_batch8():
 
 
 def test_layer_mixtral_8x7b_batch3():
-    """Three tokens: groups of at most 3 tokens on the tensor-core gather with the
-    4-row x buffer, 16 consumer warps."""
+    """Three tokens: a pair through the two-kernel decode path, then the third token
+    through the one-kernel layer, on one workspace."""
     run_layer_case(4096, 14336, 8, 2, 3, 0, [70], seed=7, gen_device="cuda")
+
+
+def test_layer_general_path_3_tokens():
+    """Three tokens with 128 routed experts (more than the decode paths route): the
+    general path, groups of at most 3 tokens on the tensor-core gather with the 4-row x
+    buffer."""
+    run_layer_case(1024, 512, 128, 2, 3, 0, [0, 70], seed=17)
+
+
+def test_layer_deepseek_v2_lite_pairs():
+    """Four tokens of the DeepSeek-V2-Lite shape (64 routed experts top-6, 2 shared):
+    two pairs through the two-kernel decode path, each pair's routing, v and masks
+    written at its tokens."""
+    run_layer_case(2048, 1408, 64, 6, 4, 2, [0, 90], seed=18, gen_device="cuda")
+
+
+def test_workspace_shared_across_token_counts():
+    """One workspace (sized for the largest call) used by calls with 4, 1, 2, 8 and 3
+    tokens in turn: every result equals that of a call on a fresh workspace, up to the
+    order of the decode paths' fp32 additions."""
+    d, f, E, k = 1024, 512, 8, 2
+    de = synth.experts(E, d, f, 19, device="cuda")
+    ex = ses.Experts.from_dense(de.w_up, de.gate_t, de.down, torch.full((E,), 0.05, device="cuda"))
+    layer = ses.Layer(synth.router(d, E, 19, device="cuda"), ex, k, True)
+    counts = [4, 1, 2, 8, 3]
+    paths = [ses.layer_path(layer, B) for B in counts]
+    assert paths == ["decode_pairs", "decode_fused", "decode", "general", "decode_pairs"], paths
+    shared_ws = ses.Workspace(max(ses.layer_workspace_bytes(layer, B) for B in counts))
+    for i, B in enumerate(counts):
+        x = synth.tokens(B, d, 190 + i, device="cuda")
+        y_shared = ses.layer_decode(x, layer, rmsnorm=True, ws=shared_ws)
+        y_fresh = ses.layer_decode(x, layer, rmsnorm=True, ws=ses.Workspace(ses.layer_workspace_bytes(layer, B)))
+        torch.cuda.synchronize()
+        assert shared_ws.status() == 0
+        assert _same_up_to_sum_order(y_shared, y_fresh), (B, paths[i])
 
 
 _BIG_ORACLE = {}
@@ -515,10 +550,11 @@ def test_decode_mixtral_8x7b_b2():
     run_layer_case(4096, 14336, 8, 2, 2, 0, [50, 90], seed=30, gen_device="cuda", rmsnorm=True)
 
 
-@pytest.mark.parametrize("B", [1, 2, 5])
+@pytest.mark.parametrize("B", [1, 2, 5, 8])
 def test_layer_interleaved_gate_down(B):
     """gate and down rows interleaved in one buffer (one read per kept column), on the
-    decode path (1 or 2 tokens) and on the general path (5 tokens), with a shared expert."""
+    decode path (1 or 2 tokens), in pairs (5 tokens) and on the general path (8 tokens),
+    with a shared expert."""
     assert ses.Experts.from_dense(*[torch.zeros(s, dtype=torch.float16, device="cuda")
                                     for s in [(1, 256, 16), (1, 16, 256), (1, 16, 256)]],
                                   torch.zeros(1, device="cuda"), interleave=True).interleaved
@@ -527,8 +563,8 @@ def test_layer_interleaved_gate_down(B):
 
 def test_layer_path_selection():
     """One or two tokens with 8/16/32/64 routed experts take a decode path: one kernel for
-    one token up to d = 4096, else two kernels up to d = 6144; other shapes take the
-    general path."""
+    one token up to d = 4096, else two kernels up to d = 6144; three or four such tokens
+    (up to six) go through it in pairs; other shapes take the general path."""
     def layer(d, f, E):
         de = synth.experts(E, d, f, 50)
         ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(),
@@ -537,7 +573,12 @@ def test_layer_path_selection():
     small = layer(1024, 256, 8)
     assert ses.layer_path(small, 1) == "decode_fused"
     assert ses.layer_path(small, 2) == "decode"
-    assert ses.layer_path(small, 3) == "general"
+    # three to six tokens: two at a time through the decode path
+    assert ses.layer_path(small, 3) == "decode_pairs"
+    assert ses.layer_path(small, 6) == "decode_pairs"
+    assert ses.layer_path(small, 7) == "general"
+    assert ses.layer_path(layer(6144, 256, 8), 4) == "decode_pairs"
+    assert ses.layer_path(layer(1024, 256, 128), 3) == "general"
     assert ses.layer_path(layer(1024, 256, 64), 1) == "decode_fused"
     assert ses.layer_path(layer(1024, 256, 128), 1) == "general"
     assert ses.layer_path(layer(4096, 256, 8), 1) == "decode_fused"
@@ -733,7 +774,7 @@ def test_nonfinite_tokens_keep_expert_ids_valid():
     experts stay k distinct valid ones on all three paths, and the layer finishes with a
     clean status (its output for such a token is not finite, as the oracle's would be)."""
     for d, f, E, k, B, path in [(1024, 512, 8, 2, 1, "decode_fused"), (1024, 512, 8, 2, 2, "decode"),
-                                (256, 512, 8, 2, 4, "general")]:
+                                (1024, 512, 8, 2, 3, "decode_pairs"), (256, 512, 8, 2, 8, "general")]:
         de = synth.experts(E, d, f, 33, device="cuda")
         ex = ses.Experts.from_dense(de.w_up, de.gate_t, de.down, torch.full((E,), 0.05, device="cuda"))
         layer = ses.Layer(synth.router(d, E, 33, device="cuda"), ex, k, True)
