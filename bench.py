@@ -70,10 +70,10 @@ NCU_TRAFFIC = {
     # decode_gather_kernel: 147.50 MB (read + write) captured on layer copy 0 at 70% (the
     # 1-copy small case, 143.97 MB algorithmic), scaled to the 8-copy mean of 139.12 MB
     ("decode_gather_kernel", "345fe56b4667b2fa"): 147.50e6 * 139.12 / 143.97,
-    # decode_layer_kernel: 180.87 MB read + 3.08 MB written (dram__bytes_read.sum,
+    # decode_layer_kernel: 180.87 MB read + 2.98 MB written (dram__bytes_read.sum,
     # dram__bytes_write.sum) captured on layer copy 0 at 70% (the 1-copy case, 180.75 MB
     # algorithmic), scaled to the 8-copy mean of 175.90 MB
-    ("decode_layer_kernel", "ee23736f3b12169f"): (180872448 + 3078656) * 175.90 / 180.75,
+    ("decode_layer_kernel", "e8119c3d95a213fd"): (180873216 + 2975488) * 175.90 / 180.75,
 }
 
 
