@@ -223,7 +223,8 @@ moe_status_t moe_layer_decode(const uint16_t* x, int32_t B, const moe_layer_t* l
  * tokens, d <= 4096, B k >= 6 E: the router and the up-projection kernel, then per expert the
  * union of its tokens' masks as one kept-row list, a gate pass and a down pass that read
  * every kept row once per expert, and a per-token sum; bitwise reproducible), 4 = the
- * decode path in pairs (three to six tokens of a shape that paths 1 and 2 take: tokens
+ * decode path in pairs (three to six tokens of a shape that paths 1 and 2 take, three
+ * or four with more than 16 routed experts: tokens
  * 2i and 2i + 1 through the decode path, one call after the other, the last token of an
  * odd count alone; the tokens are independent, and two pairs that route to one expert
  * read its rows twice), 0 = the general path (router, up-projection, gather and combine

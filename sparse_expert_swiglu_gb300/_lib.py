@@ -417,7 +417,8 @@ def layer_path(layer: Layer, B: int) -> str:
     kernel), 'batched' (16 to 64 tokens, d <= 4096, at least 6 tokens per routed expert
     on average: router, up kernel, then per-expert kept-row lists and gate and down passes
     that read each kept row once per expert), 'decode_pairs' (three to six tokens of a
-    shape the decode path takes: two at a time through it) or
+    shape the decode path takes, three or four with more than 16 routed experts: two at
+    a time through it) or
     'general' (router, up, gather and combine kernels)."""
     r = int(lib().moe_layer_path(ctypes.byref(layer.c_struct()), B))
     if r < 0:

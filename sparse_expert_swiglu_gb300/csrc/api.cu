@@ -394,12 +394,15 @@ static bool use_decode_path(const moe_layer_t* layer, int B, const DeviceInfo& d
 // A few tokens more than the decode path takes run through it two at a time (the
 // tokens are independent: routing, experts and RMSNorm act per token); the experts two
 // pairs share are then read twice, and it still measured faster than the general path
-// up to kPairMaxB tokens (Mixtral-8x7B at 70 %, 4 / 5 / 6 tokens: 171 / 218 / 255 against
-// 216 / 251 / 277 us; at 8 tokens the general path's 329 us wins).
-constexpr int kPairMaxB = 6;
+// up to 6 tokens with at most 16 routed experts (Mixtral-8x7B at 70 %, 4 / 5 / 6 / 7
+// tokens: 171 / 218 / 255 / 304 against 216 / 251 / 277 / 308 us; 8 tokens: 340 against
+// 329) and up to 4 with more, where every call routes over all of them (DeepSeek-V2-Lite,
+// 0 / 50 / 90 %: 4 tokens 138 / 103 / 70 against 170 / 119 / 68 us; 7 tokens 252 / 190 /
+// 131 against 239 / 169 / 93).
 static bool use_decode_pairs(const moe_layer_t* layer, int B, const DeviceInfo& di) {
+  const int pair_max = layer->routed.E <= 16 ? 6 : 4;
   int su = 0, sr = 0, cap = 0, umax = 0;
-  return B > 2 && B <= kPairMaxB && !use_decode_path(layer, B, di, su, sr, cap, umax) &&
+  return B > 2 && B <= pair_max && !use_decode_path(layer, B, di, su, sr, cap, umax) &&
          use_decode_path(layer, 2, di, su, sr, cap, umax);
 }
 

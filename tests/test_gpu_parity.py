@@ -564,7 +564,8 @@ def test_layer_interleaved_gate_down(B):
 def test_layer_path_selection():
     """One or two tokens with 8/16/32/64 routed experts take a decode path: one kernel for
     one token up to d = 4096, else two kernels up to d = 6144; three or four such tokens
-    (up to six) go through it in pairs; other shapes take the general path."""
+    (up to six, or four with more than 16 routed experts) go through it in pairs; other
+    shapes take the general path."""
     def layer(d, f, E):
         de = synth.experts(E, d, f, 50)
         ex = ses.Experts.from_dense(de.w_up.cuda(), de.gate_t.cuda(), de.down.cuda(),
@@ -579,6 +580,9 @@ def test_layer_path_selection():
     assert ses.layer_path(small, 7) == "general"
     assert ses.layer_path(layer(6144, 256, 8), 4) == "decode_pairs"
     assert ses.layer_path(layer(1024, 256, 128), 3) == "general"
+    # with more than 16 routed experts only up to four tokens go in pairs
+    assert ses.layer_path(layer(1024, 256, 64), 4) == "decode_pairs"
+    assert ses.layer_path(layer(1024, 256, 64), 5) == "general"
     assert ses.layer_path(layer(1024, 256, 64), 1) == "decode_fused"
     assert ses.layer_path(layer(1024, 256, 128), 1) == "general"
     assert ses.layer_path(layer(4096, 256, 8), 1) == "decode_fused"
