@@ -8,16 +8,23 @@
 // Each CTA takes a contiguous range of units.  One producer thread streams the
 // units' packed strips (contiguous in memory) into a 4-stage shared-memory ring
 // with 1-D bulk copies (TMA).  Consumer warp w owns superblock sb = w % nsb of
-// M-tile slot w / nsb, keeps the B fragments (the group's tokens) of its superblock
-// in registers, and runs the INT2 dot products on the tensor cores (mma.sync
-// m16n8k16, fp16 in, fp32 accumulate).  Partial v of the superblocks are summed in
+// M-tile slot w / nsb, reads the B fragments (the group's tokens) of its superblock
+// from the group's x in shared memory as each k-step comes, and runs the INT2 dot
+// products on the tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate).  Partial v of the superblocks are summed in
 // a fixed order by one warp per M-tile, which also applies the threshold.
 #include "params.cuh"
 
 namespace sesg {
 
 constexpr int kUpMaxStages = 4;
-constexpr size_t kUpSmemBudget = 200 * 1024;
+constexpr size_t kUpSmemBudget = 220 * 1024;
+// compute warps per CTA (up to): with the B fragments read from shared memory, 16
+// warps (two M-tiles of 8 superblocks per step at d = 4096) hide the dependent mma and
+// code-extraction latencies that 8 warps left exposed; at most kUpMaxMpar M-tiles per
+// step, since one finalize warp sums and thresholds all of them
+constexpr int kUpWarps = 16;
+constexpr int kUpMaxMpar = 4;
+constexpr int kXPad = 8;  // halves after each token's x row (rows 16 bytes off the banks)
 
 struct UpLayout {
   int nsb, mpar, nwc, spp, stages;
@@ -31,7 +38,9 @@ __host__ __device__ inline UpLayout up_layout(int d, int max_tok) {
   UpLayout L;
   L.nsb = n_superblocks(d);
   if (L.nsb <= 8) {
-    L.mpar = 8 / L.nsb;
+    L.mpar = kUpWarps / L.nsb;
+    if (L.mpar > kUpMaxMpar) L.mpar = kUpMaxMpar;
+    if (L.mpar < 1) L.mpar = 1;
     L.nwc = L.mpar * L.nsb;
   } else {
     L.mpar = 1;
@@ -40,7 +49,7 @@ __host__ __device__ inline UpLayout up_layout(int d, int max_tok) {
   L.strip = (size_t)L.nsb * kBlkBytes;
   const size_t step = L.strip * L.mpar;
   L.spp = step >= 32768 ? 1 : (int)((32768 + step - 1) / step);
-  size_t fixed = 256 + (size_t)max_tok * d * 2 + (size_t)kMaxTok * (d / kGroup) * 4 +
+  size_t fixed = 256 + (size_t)max_tok * (d + kXPad) * 2 + (size_t)kMaxTok * (d / kGroup) * 4 +
                  (size_t)2 * L.nwc * 32 * 16 + (size_t)L.mpar * 16 * kMaxTok * 4 + 64;
   while (L.spp > 1 && fixed + 2 * step * L.spp > kUpSmemBudget) --L.spp;
   L.stage_bytes = step * L.spp;
@@ -55,7 +64,7 @@ __host__ __device__ inline UpLayout up_layout(int d, int max_tok) {
   L.off_stage = o;
   o += L.stage_bytes * L.stages;
   L.off_x = o;
-  o += (size_t)max_tok * d * 2;
+  o += (size_t)max_tok * (d + kXPad) * 2;
   o = (o + 15) & ~(size_t)15;
   L.off_xg = o;
   o += (size_t)kMaxTok * (d / kGroup) * 4;
@@ -68,10 +77,19 @@ __host__ __device__ inline UpLayout up_layout(int d, int max_tok) {
   return L;
 }
 
+// Where lane (gl, c) finds its B operand: token gl / G's x at the superblock's input
+// 16 ks + 2 c (and + 8) for k-step ks, used when the k-step's quantiser group class
+// gi % G is the lane's slot class gl % G and the token exists, else zero.
+struct BSrc {
+  const __half* row;  // the token's x at the superblock start + 2 c (a valid address)
+  int cls;            // gl % G
+  bool tok;           // token gl / G is one of the group's
+};
+
 // k-steps of quantiser group GI (compile time): 4 mma into the 4 accumulator chains.
-template <int GI>
-__device__ __forceinline__ void up_group(const uint4 (&w)[4], const uint32_t (&bf)[64],
-                                         float (&D)[4][4]) {
+template <int G, int GI>
+__device__ __forceinline__ void up_group(const uint4 (&w)[4], const BSrc& bs, float (&D)[4][4]) {
+  const bool on = bs.tok && bs.cls == GI % G;
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     uint32_t a[4];
@@ -79,25 +97,27 @@ __device__ __forceinline__ void up_group(const uint4 (&w)[4], const uint32_t (&b
     a[1] = code_pair<GI>(w[t].y);
     a[2] = code_pair<GI>(w[t].z);
     a[3] = code_pair<GI>(w[t].w);
-    mma_16816(D[t], a, bf[2 * (GI * 4 + t)], bf[2 * (GI * 4 + t) + 1]);
+    const __half* xr = bs.row + 16 * (GI * 4 + t);
+    const uint32_t b0 = on ? *reinterpret_cast<const uint32_t*>(xr) : 0u;
+    const uint32_t b1 = on ? *reinterpret_cast<const uint32_t*>(xr + 8) : 0u;
+    mma_16816(D[t], a, b0, b1);
   }
 }
 
 template <int T, int PH, int GAM>
-__device__ __forceinline__ void up_phase_groups(const uint4 (&w)[4],
-                                                const uint32_t (&bf)[64], float (&D)[4][4], int ng) {
+__device__ __forceinline__ void up_phase_groups(const uint4 (&w)[4], const BSrc& bs, float (&D)[4][4],
+                                                int ng) {
   constexpr int G = 8 / T;
   if constexpr (GAM < G) {
     constexpr int GI = PH * G + GAM;
-    if (GI < ng) up_group<GI>(w, bf, D);
-    up_phase_groups<T, PH, GAM + 1>(w, bf, D, ng);
+    if (GI < ng) up_group<G, GI>(w, bs, D);
+    up_phase_groups<T, PH, GAM + 1>(w, bs, D, ng);
   }
 }
 
 // Fold the accumulators of phase PH (G quantiser groups side by side) into v.
 template <int T, int PH>
-__device__ __forceinline__ void up_phase(const uint4 (&w)[4],
-                                         const uint32_t (&bf)[64], const uint8_t* __restrict__ szt,
+__device__ __forceinline__ void up_phase(const uint4 (&w)[4], const BSrc& bs, const uint8_t* __restrict__ szt,
                                          const float* __restrict__ xg, int sb, int ng, int ngrp,
                                          float (&vacc)[2][2]) {
   constexpr int G = 8 / T;
@@ -105,7 +125,7 @@ __device__ __forceinline__ void up_phase(const uint4 (&w)[4],
   float D[4][4];
 #pragma unroll
   for (int t = 0; t < 4; ++t) D[t][0] = D[t][1] = D[t][2] = D[t][3] = 0.f;
-  up_phase_groups<T, PH, 0>(w, bf, D, ng);
+  up_phase_groups<T, PH, 0>(w, bs, D, ng);
   const int gi_lane = (G >= 2) ? (2 * c) % G : 0;
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
@@ -126,13 +146,12 @@ __device__ __forceinline__ void up_phase(const uint4 (&w)[4],
 }
 
 template <int T, int PH>
-__device__ __forceinline__ void up_phases(const uint4 (&w)[4],
-                                          const uint32_t (&bf)[64], const uint8_t* __restrict__ szt,
+__device__ __forceinline__ void up_phases(const uint4 (&w)[4], const BSrc& bs, const uint8_t* __restrict__ szt,
                                           const float* __restrict__ xg, int sb, int ng, int ngrp,
                                           float (&vacc)[2][2]) {
   if constexpr (PH < T) {
-    up_phase<T, PH>(w, bf, szt, xg, sb, ng, ngrp, vacc);
-    up_phases<T, PH + 1>(w, bf, szt, xg, sb, ng, ngrp, vacc);
+    up_phase<T, PH>(w, bs, szt, xg, sb, ng, ngrp, vacc);
+    up_phases<T, PH + 1>(w, bs, szt, xg, sb, ng, ngrp, vacc);
   }
 }
 
@@ -146,17 +165,16 @@ __device__ __forceinline__ void up_phases(const uint4 (&w)[4],
 // and the per-group correction v += s * (A_g - z * X_g) (X_g = sum of x over the
 // group) is applied once per G groups.  Four accumulator chains (one per k-step of a
 // group) shorten the mma dependency chain.  Every group index is a compile-time
-// constant, so the codes, fragments and accumulators stay in registers.
+// constant, so the codes and accumulators stay in registers.
 template <int T>
-__device__ __forceinline__ void up_superblock(const uint8_t* __restrict__ blk,
-                                              const uint32_t (&bf)[64],
+__device__ __forceinline__ void up_superblock(const uint8_t* __restrict__ blk, const BSrc& bs,
                                               const float* __restrict__ xg, int sb, int ng,
                                               int ngrp, float (&vacc)[2][2]) {
   const int lane = threadIdx.x & 31;
   uint4 w[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) w[q] = reinterpret_cast<const uint4*>(blk)[q * 32 + lane];
-  up_phases<T, 0>(w, bf, blk + kBlkCodeBytes, xg, sb, ng, ngrp, vacc);
+  up_phases<T, 0>(w, bs, blk + kBlkCodeBytes, xg, sb, ng, ngrp, vacc);
 }
 
 // One warp, after the superblock partials are summed: per-token v of the M-tile's
@@ -232,27 +250,6 @@ __device__ __forceinline__ void up_finalize(const ExpertParams& p, const GroupDe
               (uint16_t)mb;
       }
     }
-  }
-}
-
-// B fragments of superblock sb for the current group: k-step ks of quantiser group
-// gi = ks / 4 feeds slot gl (token gl / G) only when gl % G == gi % G.
-__device__ __forceinline__ void build_bfrag_regs(const __half* __restrict__ xs, int d, int n_tok,
-                                                 int T, int sb, uint32_t (&bf)[64]) {
-  const int lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
-  const int G = 8 / T, tau = gl / G;
-#pragma unroll
-  for (int ks = 0; ks < 32; ++ks) {
-    const int gi = ks >> 2;
-    const int k = sb * kSuper + 16 * ks + 2 * c;
-    uint32_t b0 = 0, b1 = 0;
-    if ((gl % G) == (gi % G) && tau < n_tok && k < d) {
-      const __half* xr = xs + (size_t)tau * d + k;
-      b0 = *reinterpret_cast<const uint32_t*>(xr);
-      b1 = *reinterpret_cast<const uint32_t*>(xr + 8);
-    }
-    bf[2 * ks] = b0;
-    bf[2 * ks + 1] = b1;
   }
 }
 
@@ -361,7 +358,8 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
     const int ng = min(8, (d - sb * kSuper) / kGroup);
     int cur_g = -1, T = 1;
     float thr = 0.f;
-    uint32_t bf[64];
+    BSrc bs{xs, 0, false};
+    const int xstride = d + kXPad;
     // step position: jj within the stage, stage st (ring slot s, parity ph); the group g
     // of unit us and its first unit g_lo; all advanced without divisions
     int jj = 0, st = 0, s = 0, ph = 0, jpar = 0;
@@ -380,7 +378,7 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
         const int n_tok = s_gd.n_tok;
         for (int i = threadIdx.x; i < n_tok * (d / 8); i += nbar) {
           const int t = i / (d / 8), o = i % (d / 8);
-          reinterpret_cast<uint4*>(xs + (size_t)t * d)[o] =
+          reinterpret_cast<uint4*>(xs + (size_t)t * xstride)[o] =
               __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)s_gd.tok[t] * d) + o);
         }
         int el;
@@ -391,7 +389,7 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
           const int t = i / ngrp, grp = i % ngrp;
           float sum = 0.f;
           if (t < n_tok) {
-            const uint4* xr = reinterpret_cast<const uint4*>(xs + (size_t)t * d + grp * kGroup);
+            const uint4* xr = reinterpret_cast<const uint4*>(xs + (size_t)t * xstride + grp * kGroup);
 #pragma unroll
             for (int r = 0; r < kGroup / 8; ++r) {
               const uint4 v = xr[r];
@@ -407,7 +405,12 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
           xg[i] = sum;
         }
         T = n_tok <= 1 ? 1 : n_tok <= 2 ? 2 : n_tok <= 4 ? 4 : 8;
-        if (!fin) build_bfrag_regs(xs, d, n_tok, T, sb, bf);
+        {
+          const int Gc = 8 / T, gl = lane >> 2, tau = gl / Gc;
+          bs.tok = tau < n_tok;
+          bs.cls = gl % Gc;
+          bs.row = xs + (size_t)(bs.tok ? tau : 0) * xstride + sb * kSuper + 2 * (lane & 3);
+        }
         named_barrier(1, nbar);
         cur_g = g;
       }
@@ -422,10 +425,10 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
           const uint8_t* blk = stage + (size_t)s * L.stage_bytes +
                                ((size_t)jj * L.mpar + m_slot) * L.strip + (size_t)sb * kBlkBytes;
           switch (T) {
-            case 1: up_superblock<1>(blk, bf, xg, sb, ng, ngrp, vacc); break;
-            case 2: up_superblock<2>(blk, bf, xg, sb, ng, ngrp, vacc); break;
-            case 4: up_superblock<4>(blk, bf, xg, sb, ng, ngrp, vacc); break;
-            default: up_superblock<8>(blk, bf, xg, sb, ng, ngrp, vacc); break;
+            case 1: up_superblock<1>(blk, bs, xg, sb, ng, ngrp, vacc); break;
+            case 2: up_superblock<2>(blk, bs, xg, sb, ng, ngrp, vacc); break;
+            case 4: up_superblock<4>(blk, bs, xg, sb, ng, ngrp, vacc); break;
+            default: up_superblock<8>(blk, bs, xg, sb, ng, ngrp, vacc); break;
           }
         }
         vpart[((jpar & 1) * nwc + warp) * 32 + lane] =
@@ -485,7 +488,8 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
 size_t up_smem_bytes(int d, int max_tok) { return up_layout(d, max_tok).total; }
 int up_threads(int d) { return (up_layout(d, 1).nwc + 2) * 32; }
 
-// Register budget: 10 warps (d <= 4096), 14 warps (d <= 6144) or up to 18 warps per CTA.
+// Register budget: up to 10 warps, up to 14 (d <= 6144: one warp per superblock) or up to
+// 18 (d <= 4096: 16 compute warps; beyond 6144) warps per CTA.
 static const void* up_kernel_for(int d) {
   const int t = up_threads(d);
   return t <= 320 ? (const void*)up_kernel<320> : t <= 448 ? (const void*)up_kernel<448> : (const void*)up_kernel<576>;
