@@ -177,11 +177,13 @@ __device__ __forceinline__ bool bar_or(bool bad, int n) {
 
 // ---- gate: h for the kept rows of one expert and one group of 16 of its tokens ------
 // Warps 0 .. ncw - 1 (ncw = d / 256) own 256-input slices of d and hold the group's x
-// there as mma A fragments (16 tokens x 256 inputs = 64 registers); warp ncw's lane 0
-// streams whole gate rows (2d bytes, one bulk copy each) into a ring.  Per batch of 8
-// kept rows every warp forms D[16 tokens][8 rows] over its slice (the rows as B via
-// ldmatrix), the partials meet in shared memory and warp 0 turns their sum into
-// h = SiLU(.) * v * mask * w, stored at ht[expert][group][row][hi/lo][16 tokens].
+// there as mma A fragments (16 tokens x 256 inputs = 64 registers); warp ncw's lanes
+// stream whole gate rows (2d bytes, one bulk copy each, lane i the batch's row i) into a
+// ring.  Per batch of 8 kept rows every warp forms D[16 tokens][8 rows] over its slice
+// (the rows as B via ldmatrix), the partials meet in shared memory and the first 128
+// consumer threads turn their sums into h = SiLU(.) * v * mask * w, one (row, token)
+// each, stored at ht[expert][group][row][hi/lo][16 tokens].  (One warp forming all 128
+// took 2,300 cycles a batch and held up every stage release behind it.)
 constexpr int kGateST = 16;            // ring stages (one gate row each)
 constexpr int kGateWarps = 16;         // consumer warps, at most (d <= 4096)
 constexpr int kGateBatch = 8;          // kept rows per batch (the mma N)
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(Ba
       int e, g, r0, nr;
       tile_of(tile, e, g, r0, nr);
       const int T = p.seg_t[e], t0 = g * kBtGroupTok, Tg = min(kBtGroupTok, T - t0), K = p.seg_n[e];
-      named_barrier(1, nct);  // warp 0 is done with the previous tile's table
+      named_barrier(1, nct);  // the h of the previous tile's last batch is formed
       for (int i = tid; i < kBtTileRows * kBtGroupTok; i += nct) {
         const int rl = i / kBtGroupTok, tl = i % kBtGroupTok;
         float vmw = 0.f;
@@ -350,30 +352,26 @@ __global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(Ba
           failed = true;
           break;
         }
-        if (warp == 0) {
-          // lane: tokens gid, gid + 8 and rows 2 c4, 2 c4 + 1 of the batch
-          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int w = 0; w < ncw; ++w) {
-            const float4 v = *reinterpret_cast<const float4*>(rb + w * 128 + lane * 4);
-            sum.x += v.x;
-            sum.y += v.y;
-            sum.z += v.z;
-            sum.w += v.w;
-          }
-          const float dv[4] = {sum.x, sum.y, sum.z, sum.w};
+        // h of the batch's 128 (row, token) values, one per consumer thread (the first
+        // 128): value q is accumulator entry q & 3 of lane q >> 2, i.e. token
+        // (q >> 4) + 8 (q >> 1 & 1) and row 2 (q >> 2 & 3) + (q & 1); the warps' partials
+        // added in warp order
+        for (int q = tid; q < 128; q += nct) {
+          float sum = 0.f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int tl = gid + (i >= 2 ? 8 : 0), rl = b0 + 2 * c4 + (i & 1);
-            if (tl < Tg && rl < nr) {
-              const int r = r0 + rl;
-              const float vmw = s_vmw[rl][tl];
-              const float h = vmw != 0.f ? silu_f(dv[i]) * vmw : 0.f;
-              const __half hi = __float2half_rn(h);
-              const __half lo = __float2half_rn(h - __half2float(hi));
-              __half* dst = p.ht + bt_ht_index(e, g, f, r);
-              dst[tl] = hi;
-              dst[kBtGroupTok + tl] = lo;
-            }
+          for (int w = 0; w < kGateWarps; ++w)
+            if (w < ncw) sum += rb[w * 128 + q];
+          const int ql = q >> 2, i = q & 3;
+          const int tl = (ql >> 2) + (i >= 2 ? 8 : 0), rl = b0 + 2 * (ql & 3) + (i & 1);
+          if (tl < Tg && rl < nr) {
+            const int r = r0 + rl;
+            const float vmw = s_vmw[rl][tl];
+            const float h = vmw != 0.f ? silu_f(sum) * vmw : 0.f;
+            const __half hi = __float2half_rn(h);
+            const __half lo = __float2half_rn(h - __half2float(hi));
+            __half* dst = p.ht + bt_ht_index(e, g, f, r);
+            dst[tl] = hi;
+            dst[kBtGroupTok + tl] = lo;
           }
         }
         ++nbatch;
