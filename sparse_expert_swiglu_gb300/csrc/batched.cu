@@ -184,7 +184,11 @@ __device__ __forceinline__ bool bar_or(bool bad, int n) {
 // consumer threads turn their sums into h = SiLU(.) * v * mask * w, one (row, token)
 // each, stored at ht[expert][group][row][hi/lo][16 tokens].  (One warp forming all 128
 // took 2,300 cycles a batch and held up every stage release behind it.)
-constexpr int kGateST = 16;            // ring stages (one gate row each)
+// ring stages (one gate row each): 32 where they fit (d <= 2048), else 16.  Rows take
+// about 6 us from issue to arrival here (a cycle trace); 32 stages instead of 16 at
+// DeepSeek-V2-Lite's shape, and 24 at Mixtral's, changed the pass by under 1 %.
+constexpr int kGateSTMax = 32;
+__host__ __device__ __forceinline__ int gate_stages(int d) { return d <= 2048 ? 32 : 16; }
 constexpr int kGateWarps = 16;         // consumer warps, at most (d <= 4096)
 constexpr int kGateBatch = 8;          // kept rows per batch (the mma N)
 constexpr int kBtGroupTok = 16;        // tokens per group (the mma M)
@@ -205,13 +209,14 @@ __global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(Ba
   __shared__ float s_vmw[kBtTileRows][kBtGroupTok];
   const int d = p.d, f = p.f, ncw = d / 256, nct = ncw * 32;
   const size_t stage_b = (size_t)2 * d + 16;  // a gate row, padded against bank conflicts
+  const int ST = gate_stages(d);
   uint64_t* full = reinterpret_cast<uint64_t*>(bsm);
-  uint64_t* empty = full + kGateST;
-  float* red = reinterpret_cast<float*>(bsm + 2 * kGateST * 8);       // [2][ncw][128]
-  uint8_t* ring = bsm + 2 * kGateST * 8 + 2 * kGateWarps * 128 * 4;
+  uint64_t* empty = full + kGateSTMax;
+  float* red = reinterpret_cast<float*>(bsm + 2 * kGateSTMax * 8);       // [2][ncw][128]
+  uint8_t* ring = bsm + 2 * kGateSTMax * 8 + 2 * kGateWarps * 128 * 4;
   const int nseg = p.routed.E + p.n_shared, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kGateST; ++s) {
+    for (int s = 0; s < ST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], ncw);
     }
@@ -252,8 +257,8 @@ __global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(Ba
         const int cnt = min(kGateBatch, nr - rb);
         bool ok = !*reinterpret_cast<volatile int*>(&s_abort);
         if (ok && lane < cnt) {
-          const int q = issued + lane, st = q % kGateST;
-          if (q >= kGateST) ok = mbar_wait(&empty[st], ((q / kGateST) & 1) ^ 1);
+          const int q = issued + lane, st = q % ST;
+          if (q >= ST) ok = mbar_wait(&empty[st], ((q / ST) & 1) ^ 1);
           if (ok) {
             const int col = p.seg_col[(size_t)e * f + r0 + rb + lane];
             mbar_arrive_expect_tx(&full[st], (uint32_t)(2 * d));
@@ -309,8 +314,8 @@ __global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(Ba
         bool ok = !*reinterpret_cast<volatile int*>(&s_abort);
         for (int i = 0; i < nv && ok; ++i) {
           int sq = cs + i, pq = cph;
-          if (sq >= kGateST) {
-            sq -= kGateST;
+          if (sq >= ST) {
+            sq -= ST;
             pq ^= 1;
           }
           ok = mbar_wait(&full[sq], pq);
@@ -319,7 +324,7 @@ __global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(Ba
         // B: lanes 0-7 address kept row (lane & 7) (row 0 again past nv) at k, 8-15 at k + 8
         const int ri = (lane & 7) < nv ? (lane & 7) : 0;
         int sr = cs + ri;
-        if (sr >= kGateST) sr -= kGateST;
+        if (sr >= ST) sr -= ST;
         const uint32_t bbase = smem_addr(ring + (size_t)sr * stage_b) + (uint32_t)(256 * warp + ((lane >> 3) & 1) * 8) * 2u;
         float dacc[4] = {0.f, 0.f, 0.f, 0.f};
         if (ok) {
@@ -334,12 +339,12 @@ __global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(Ba
         if (lane == 0 && ok)
           for (int i = 0; i < nv; ++i) {
             int sq = cs + i;
-            if (sq >= kGateST) sq -= kGateST;
+            if (sq >= ST) sq -= ST;
             mbar_arrive(&empty[sq]);
           }
         cs += nv;
-        if (cs >= kGateST) {
-          cs -= kGateST;
+        if (cs >= ST) {
+          cs -= ST;
           cph ^= 1;
         }
         float* rb = red + (size_t)(nbatch & 1) * kGateWarps * 128;
@@ -627,7 +632,7 @@ __global__ void __launch_bounds__(kFinalThreads) batch_final_kernel(BatchParams 
 }  // namespace
 
 size_t batch_gate_smem(int d) {
-  return (size_t)2 * kGateST * 8 + (size_t)2 * kGateWarps * 128 * 4 + (size_t)kGateST * (2 * d + 16);
+  return (size_t)2 * kGateSTMax * 8 + (size_t)2 * kGateWarps * 128 * 4 + (size_t)gate_stages(d) * (2 * d + 16);
 }
 size_t batch_down_smem(int d) {
   const size_t W = bt_chunk(d);
