@@ -183,7 +183,9 @@ __device__ __forceinline__ bool bar_or(bool bad, int n) {
 // (the rows as B via ldmatrix), the partials meet in shared memory and the first 128
 // consumer threads turn their sums into h = SiLU(.) * v * mask * w, one (row, token)
 // each, stored at ht[expert][group][row][hi/lo][16 tokens].  (One warp forming all 128
-// took 2,300 cycles a batch and held up every stage release behind it.)
+// took 2,300 cycles a batch and held up every stage release behind it.)  Warp ncw + 1
+// builds each tile's table of v * mask * w, one tile ahead of the consumers, in a second
+// buffer.
 // ring stages (one gate row each): 32 where they fit (d <= 2048), else 16.  Rows take
 // about 6 us from issue to arrival here (a cycle trace); 32 stages instead of 16 at
 // DeepSeek-V2-Lite's shape, and 24 at Mixtral's, changed the pass by under 1 %.
@@ -201,12 +203,15 @@ __device__ __forceinline__ size_t bt_ht_index(int e, int g, int f, int r) {
   return ((((size_t)e * kBtMaxGroups + g) * f + r) * 2) * kBtGroupTok;
 }
 
-__global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(BatchParams p) {
+__global__ void __launch_bounds__((kGateWarps + 2) * 32, 1) batch_gate_kernel(BatchParams p) {
   extern __shared__ __align__(128) uint8_t bsm[];
   __shared__ int s_pre[kBtMaxSeg + 1];
   __shared__ int s_abort;
-  // the consumers' tile table: v * mask * w of each (kept row, group token)
-  __shared__ float s_vmw[kBtTileRows][kBtGroupTok];
+  // the tile tables: v * mask * w of each (kept row, group token); table k of this CTA
+  // in buffer k % 2, filled by the table warp (tbl_full) and released by the consumers
+  // (tbl_free) once the tile's last h is formed
+  __shared__ float s_vmw[2][kBtTileRows][kBtGroupTok];
+  __shared__ __align__(8) uint64_t tbl_full[2], tbl_free[2];
   const int d = p.d, f = p.f, ncw = d / 256, nct = ncw * 32;
   const size_t stage_b = (size_t)2 * d + 16;  // a gate row, padded against bank conflicts
   const int ST = gate_stages(d);
@@ -219,6 +224,10 @@ __global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(Ba
     for (int s = 0; s < ST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], ncw);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tbl_full[b], 1);
+      mbar_init(&tbl_free[b], 1);
     }
     fence_barrier_init();
     s_abort = 0;
@@ -272,28 +281,60 @@ __global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(Ba
         issued += cnt;
       }
     }
+  } else if (warp == ncw + 1) {
+    // ---- table warp: lane l fills token l % 16's column of rows 2 j + l / 16, in three
+    // rounds of independent loads (the rows' columns, their mask words, the kept v)
+    const int tl = lane & (kBtGroupTok - 1), rh = lane / kBtGroupTok;
+    int k = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+      const int b = k & 1;
+      if (k >= 2 && !__all_sync(0xffffffffu, mbar_wait(&tbl_free[b], ((k >> 1) - 1) & 1))) {
+        if (lane == 0) atomicExch(&s_abort, 1);
+        break;
+      }
+      if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&s_abort) != 0)) break;
+      int e, g, r0, nr;
+      tile_of(tile, e, g, r0, nr);
+      const int t0 = g * kBtGroupTok, Tg = min(kBtGroupTok, p.seg_t[e] - t0);
+      const bool tok = tl < Tg;
+      const int tk = tok ? p.seg_tok[e * kBtMaxTok + t0 + tl] : 0, sl = tok ? p.seg_slot[e * kBtMaxTok + t0 + tl] : 0;
+      const float tw = tok ? p.seg_w[e * kBtMaxTok + t0 + tl] : 0.f;
+      const size_t row = (size_t)tk * p.n_slots + sl;
+      const int* cols = p.seg_col + (size_t)e * f + r0;
+      int c[kBtTileRows / 2];
+#pragma unroll
+      for (int j = 0; j < kBtTileRows / 2; ++j) c[j] = (tok && 2 * j + rh < nr) ? cols[2 * j + rh] : -1;
+      uint32_t kept = 0u;
+#pragma unroll
+      for (int j = 0; j < kBtTileRows / 2; ++j)
+        if (c[j] >= 0 && ((p.mask[row * p.fw + (c[j] >> 5)] >> (c[j] & 31)) & 1u)) kept |= 1u << j;
+#pragma unroll
+      for (int j = 0; j < kBtTileRows / 2; ++j)
+        s_vmw[b][2 * j + rh][tl] = ((kept >> j) & 1u) ? p.v[row * f + c[j]] * tw : 0.f;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tbl_full[b]);
+    }
   } else {
     // ---- consumers
     const int gid = lane >> 2, c4 = lane & 3;
-    int cs = 0, cph = 0, nbatch = 0;
+    int cs = 0, cph = 0, nbatch = 0, k = 0;
     bool failed = false;
-    for (int tile = blockIdx.x; tile < ntiles && !failed; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < ntiles && !failed; tile += gridDim.x, ++k) {
       int e, g, r0, nr;
       tile_of(tile, e, g, r0, nr);
       const int T = p.seg_t[e], t0 = g * kBtGroupTok, Tg = min(kBtGroupTok, T - t0), K = p.seg_n[e];
       named_barrier(1, nct);  // the h of the previous tile's last batch is formed
-      for (int i = tid; i < kBtTileRows * kBtGroupTok; i += nct) {
-        const int rl = i / kBtGroupTok, tl = i % kBtGroupTok;
-        float vmw = 0.f;
-        if (rl < nr && tl < Tg) {
-          const int col = p.seg_col[(size_t)e * f + r0 + rl];
-          const int tk = p.seg_tok[e * kBtMaxTok + t0 + tl], sl = p.seg_slot[e * kBtMaxTok + t0 + tl];
-          const size_t row = (size_t)tk * p.n_slots + sl;
-          if ((p.mask[row * p.fw + (col >> 5)] >> (col & 31)) & 1u)
-            vmw = p.v[row * f + col] * p.seg_w[e * kBtMaxTok + t0 + tl];
+      if (tid == 0 && k > 0) mbar_arrive(&tbl_free[(k - 1) & 1]);
+      // this tile's table (one verdict for all consumer threads)
+      if (bar_or(!mbar_wait(&tbl_full[k & 1], (k >> 1) & 1), nct)) {
+        if (tid == 0) {
+          set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
         }
-        s_vmw[rl][tl] = vmw;
+        failed = true;
+        break;
       }
+      const float(*tab)[kBtGroupTok] = s_vmw[k & 1];
       // this warp's x slice of the group's tokens as A fragments (zero past Tg)
       uint32_t xa[16][4];
       {
@@ -370,7 +411,7 @@ __global__ void __launch_bounds__((kGateWarps + 1) * 32, 1) batch_gate_kernel(Ba
           const int tl = (ql >> 2) + (i >= 2 ? 8 : 0), rl = b0 + 2 * (ql & 3) + (i & 1);
           if (tl < Tg && rl < nr) {
             const int r = r0 + rl;
-            const float vmw = s_vmw[rl][tl];
+            const float vmw = tab[rl][tl];
             const float h = vmw != 0.f ? silu_f(sum) * vmw : 0.f;
             const __half hi = __float2half_rn(h);
             const __half lo = __float2half_rn(h - __half2float(hi));
@@ -652,7 +693,7 @@ cudaError_t launch_batched(const BatchParams& p, int P, cudaStream_t st) {
   const size_t gs = batch_gate_smem(p.d), ds = batch_down_smem(p.d);
   e = cudaFuncSetAttribute(batch_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gs);
   if (e != cudaSuccess) return e;
-  batch_gate_kernel<<<P, (p.d / 256 + 1) * 32, gs, st>>>(p);
+  batch_gate_kernel<<<P, (p.d / 256 + 2) * 32, gs, st>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(batch_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ds);
   if (e != cudaSuccess) return e;
