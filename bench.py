@@ -578,8 +578,27 @@ def run_reference(args, world, rank, local):
         experts[e] = dict(w_gate=de.gate_t[e].cpu().numpy().T, w_up_deq=wdeq,
                           w_down=de.down[e].cpu().numpy(), thr=float(np.float32(t)))
     del de
-    secs = time_oracle(xs, wr, experts, args.steps, args.warmup)
-    value = W["B"] * k * args.steps / secs
+    # a step is 1/n of a single-token layer decode: the oracle on the token, with both
+    # routed experts cut to one of n column slices of their intermediate dimension (the
+    # n slices together are the layer's expert work); n is chosen from one full decode so
+    # that the --steps run takes about two minutes
+    x0 = xs[0:1]
+    t0 = time.perf_counter()
+    orc.moe_layer(x0, wr, experts, k, True, rmsnorm_out=True)
+    t_full = time.perf_counter() - t0
+    n = max(1, min(64, math.ceil(args.steps * t_full / 120.0)))
+    cuts = np.array_split(np.arange(f), n)
+    sliced = [[None if ex is None else dict(w_gate=np.ascontiguousarray(ex["w_gate"][:, c]),
+                                            w_up_deq=np.ascontiguousarray(ex["w_up_deq"][:, c]),
+                                            w_down=np.ascontiguousarray(ex["w_down"][c, :]), thr=ex["thr"])
+               for ex in experts] for c in cuts]
+    for i in range(args.warmup):
+        orc.moe_layer(xs[i % xs_n:i % xs_n + 1], wr, sliced[i % n], k, True)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        orc.moe_layer(xs[i % xs_n:i % xs_n + 1], wr, sliced[i % n], k, True)
+    secs = time.perf_counter() - t0
+    value = W["B"] * k * args.steps / n / secs
     cores = oracle_threads()
     line = {
         "impl": "reference", "metric": METRIC.replace("70%", pct_label(args.sparsity)), "value": value,
@@ -588,9 +607,11 @@ def run_reference(args, world, rank, local):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(args.sparsity, max(1, args.copies), args.gpus),
         "cpu_baseline": {"value": value, "unit": "expert-tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{args.steps} single-token layer decodes over {xs_n} tokens of layer copy 0 "
-                                   f"(fp64 numpy oracle, {pct_label(args.sparsity)} thresholds from "
-                                   f"{W['calib_tokens']} calibration tokens)"},
+                         "sample": f"{args.steps} steps, each 1/{n} of a single-token layer decode (routing, then both "
+                                   f"routed experts on one of {n} column slices of f), over {xs_n} tokens of "
+                                   f"layer copy 0 (fp64 numpy oracle, {pct_label(args.sparsity)} thresholds from "
+                                   f"{W['calib_tokens']} calibration tokens; a full decode took "
+                                   f"{t_full * 1e3:.0f} ms)"},
         "e2e": {"value": value, "unit": "expert-tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
