@@ -381,3 +381,24 @@ def test_mutation_router_tie_break(monkeypatch):
     monkeypatch.setattr(orc, "route_topk", mutant)
     with pytest.raises(AssertionError):
         test_route_golden()
+
+
+def test_layer_additive_over_column_slices():
+    """Every kept intermediate column contributes its own term h_i W^down[i, :] to an
+    expert's output (steps 3 and 4 of Algorithm 1), so a layer's output (before the
+    RMSNorm) is the sum of the layers whose experts keep only one slice of the columns
+    each; the reference arm of the bench times one slice per step."""
+    rng = np.random.default_rng(21)
+    d, f, E, k = 128, 96, 4, 2
+    x = rng.standard_normal((3, d)).astype(np.float16)
+    wr = (rng.standard_normal((d, E)) * 0.1).astype(np.float16)
+    experts = [dict(w_gate=rng.standard_normal((d, f)) * 0.05, w_up_deq=rng.standard_normal((d, f)) * 0.05,
+                    w_down=rng.standard_normal((f, d)) * 0.05, thr=0.1) for _ in range(E)]
+    y_full, _ = orc.moe_layer(x, wr, experts, k, True)
+    total = np.zeros_like(y_full)
+    for c in np.array_split(np.arange(f), 5):
+        sl = [dict(w_gate=ex["w_gate"][:, c], w_up_deq=ex["w_up_deq"][:, c], w_down=ex["w_down"][c, :],
+                   thr=ex["thr"]) for ex in experts]
+        y, _ = orc.moe_layer(x, wr, sl, k, True)
+        total += y
+    np.testing.assert_allclose(total, y_full, rtol=0, atol=1e-14)
