@@ -446,9 +446,10 @@ __global__ void __launch_bounds__((kGateWarps + 2) * 32, 1) batch_gate_kernel(Ba
 
 // ---- down: one 2048-column chunk of d for one part (512 rows) of one (expert, group) --
 // Warps 0 .. ncw - 1 (ncw = W / 128, W = min(d, 2048)) own 128 columns of the chunk and
-// accumulate Y^T[128 columns][16 tokens] in registers; warp ncw's lane 0 streams batches
-// of 16 kept rows (each row's chunk, 2W bytes, one bulk copy) with their h (1 KB).  The
-// part's sums go to ypart[part][token][slot], added in order by the final kernel.
+// accumulate Y^T[128 columns][16 tokens] in registers; warp ncw streams batches of 16
+// kept rows (each row's chunk, 2W bytes, one bulk copy, lane i row i) with their h (1 KB,
+// lane 16).  The part's sums go to ypart[part][token][slot], added in order by the final
+// kernel.
 constexpr int kDownST = 3;
 constexpr int kDownRowsB = 16;   // kept rows per batch (the mma K)
 constexpr int kDownWarps = 16;

@@ -1285,10 +1285,10 @@ __global__ void __launch_bounds__(MAXT, 1) decode_gather_kernel(DecodeParams p) 
 
 // ---------------------------------------------------------------------------
 // One-kernel decode layer (d <= 4096).  The up kernel's routing and up phase, then, in
-// the same CTA, the gather of exactly the kept columns of this CTA's own units: the
-// producer lane streams a unit's kept rows as soon as its finalize warp has published
-// them (interleaved with the remaining strips, which keep priority), and the compute
-// warps turn from superblocks to rows when their units are done.  There is no grid-wide
+// the same CTA, the gather of exactly the kept columns of this CTA's own units: the row
+// producer warp streams a unit's kept rows as soon as its finalize warp has published
+// them, while the strip producer warp still streams the later units' strips, and the
+// compute warps turn from superblocks to rows when their units are done.  There is no grid-wide
 // step between the up projection and the gather: a CTA never waits for another one.
 // Each CTA adds its share of y into the fp32 accumulator, and the last one to finish
 // rounds y (after the RMSNorm of stacked layers), leaving the accumulator zeroed.
