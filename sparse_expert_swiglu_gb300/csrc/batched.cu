@@ -325,7 +325,7 @@ __global__ void __launch_bounds__((kGateWarps + 2) * 32, 1) batch_gate_kernel(Ba
       const int T = p.seg_t[e], t0 = g * kBtGroupTok, Tg = min(kBtGroupTok, T - t0), K = p.seg_n[e];
       named_barrier(1, nct);  // the h of the previous tile's last batch is formed
       if (tid == 0 && k > 0) mbar_arrive(&tbl_free[(k - 1) & 1]);
-      // this tile's table (one verdict for all consumer threads)
+      // this tile's table (one decision for all consumer threads)
       if (bar_or(!mbar_wait(&tbl_full[k & 1], (k >> 1) & 1), nct)) {
         if (tid == 0) {
           set_status(&p.ctrl->status, MOE_ERR_TIMEOUT);
