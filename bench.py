@@ -70,11 +70,10 @@ NCU_TRAFFIC = {
     # decode_gather_kernel: 147.50 MB (read + write) captured on layer copy 0 at 70% (the
     # 1-copy small case, 143.97 MB algorithmic), scaled to the 8-copy mean of 139.12 MB
     ("decode_gather_kernel", "345fe56b4667b2fa"): 147.50e6 * 139.12 / 143.97,
-    # decode_layer_kernel: 180.87 MB read + 2.98 MB written (dram__bytes_read.sum,
+    # decode_layer_kernel: 180.87 MB read + 3.10 MB written (dram__bytes_read.sum,
     # dram__bytes_write.sum) captured on layer copy 0 at 70% (the 1-copy case, 180.75 MB
-    # algorithmic), scaled to the 8-copy mean of 175.90 MB (sources re-keyed after a change
-    # to comments only)
-    ("decode_layer_kernel", "1279beb542d2f967"): (180873216 + 2975488) * 175.90 / 180.75,
+    # algorithmic), scaled to the 8-copy mean of 175.90 MB
+    ("decode_layer_kernel", "4b95660d2d5d96fb"): (180871936 + 3104768) * 175.90 / 180.75,
 }
 
 

@@ -1600,7 +1600,7 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
       // get h = 0
       for (int k = 0;; ++k) {
         const int hs = k & (kHB - 1);
-        if (vload(&m->abort) || !__all_sync(0xffffffffu, mbar_wait(&dotsb[hs], (k / kHB) & 1))) break;
+        if (!__all_sync(0xffffffffu, !vload(&m->abort) && mbar_wait(&dotsb[hs], (k / kHB) & 1))) break;
         const int nbw = vload(&nbs[hs]);
         const int nb = nbw & 0xff;
         if (lane < kDecRows * 2) {
@@ -1770,7 +1770,7 @@ __global__ void __launch_bounds__(kUpRegThreads, 1) decode_layer_kernel(DecodePa
           kn = __shfl_sync(0xffffffffu, kn, 0);
           if (kn - cons >= kDecRows) return kDecRows;
           if (ak) return kn - cons;
-          if (vload(&m->abort) || tries > (uint32_t)kDecMaxUnits * 16) return -1;
+          if (__any_sync(0xffffffffu, vload(&m->abort)) || tries > (uint32_t)kDecMaxUnits * 16) return -1;
           int sq = s0 + (kn - cons), pq = ph0;
           if (sq >= SR) {
             sq -= SR;
