@@ -382,6 +382,7 @@ __global__ void __launch_bounds__(MAXT, 1) gather_kernel(ExpertParams p) {
                                  (uint32_t)(kw + lhalf * 8) * 2u;
           // two accumulator chains (even and odd k-steps) halve the dependent mma latency
           float dd[4] = {0.f, 0.f, 0.f, 0.f}, de[4] = {0.f, 0.f, 0.f, 0.f};
+          ok = __all_sync(0xffffffffu, ok);  // the mma below is warp-wide: one decision for all lanes
           if (ok) {
             // B column gid = token gid (zero beyond the x rows held)
             const bool xon = gid < XR;
