@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(MAXT, 1) up_kernel(ExpertParams p) {
       const bool last = jj == spp - 1 || ue >= u1;
       bool ok = true;
       if (!fin) {
-        if (first) ok = mbar_wait(&full[s], ph);
+        if (first) ok = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));  // the mma below is warp-wide
         const bool active = us + m_slot < ue;
         float vacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
         if (active && ok) {
