@@ -72,8 +72,9 @@ NCU_TRAFFIC = {
     ("decode_gather_kernel", "345fe56b4667b2fa"): 147.50e6 * 139.12 / 143.97,
     # decode_layer_kernel: 180.87 MB read + 3.10 MB written (dram__bytes_read.sum,
     # dram__bytes_write.sum) captured on layer copy 0 at 70% (the 1-copy case, 180.75 MB
-    # algorithmic), scaled to the 8-copy mean of 175.90 MB
-    ("decode_layer_kernel", "4b95660d2d5d96fb"): (180871936 + 3104768) * 175.90 / 180.75,
+    # algorithmic), scaled to the 8-copy mean of 175.90 MB (re-keyed after two unused fields
+    # of the control block were renamed; the compiled kernel is unchanged)
+    ("decode_layer_kernel", "6652570ccd95b6ef"): (180871936 + 3104768) * 175.90 / 180.75,
 }
 
 

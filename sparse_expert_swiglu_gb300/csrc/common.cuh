@@ -85,9 +85,9 @@ struct Ctrl {
   int status;        // first device-side error, MOE_OK if none
   int route_done;    // last-CTA counter of the router
   int G;             // number of groups of the current call
-  int work;          // next unclaimed unit of the decode kernel
+  int reserved0;     // unused (keeps the block's layout)
   int N;             // total kept items of the current call (written by the gather kernel)
-  int work_done;     // decode CTAs that have claimed their last unit
+  int reserved1;     // unused
   int gdone;         // decode gather CTAs that have added their share of y
   int pad1;
 };
