@@ -274,10 +274,30 @@ def set_thresholds(layers, table, pct):
         layer.routed.thr.copy_(table[pct][r])
 
 
+def count_bytes(idx, words, d, f, E, k, B, up_bytes):
+    """Bytes one layer step must move, from its routing (idx [B][k]) and its masks (words
+    [B][k][ceil(f / 32)] uint32, bit c of word c / 32 = column c kept): per active expert
+    the packed up projection plus 4 d bytes per column kept for any of its tokens (gate row
+    + down row, read once), the router weight (2 d E), x in and y out (2 B d each).  Also
+    per kernel."""
+    words = np.asarray(words, dtype=np.uint32)
+    bits = ((words[..., :, None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(B, k, -1)[..., :f]
+    experts = sorted(set(np.asarray(idx).ravel().tolist()))
+    kept_cols, up_total = 0, 0
+    for e in experts:
+        rws, cls = np.nonzero(np.asarray(idx) == e)
+        union = np.any(bits[rws, cls].astype(bool), axis=0)
+        kept_cols += int(union.sum())
+        up_total += up_bytes
+    gather = 4 * d * kept_cols
+    return dict(up=up_total + 2 * B * d, gather=gather, route=2 * d * E + 2 * B * d,
+                total=up_total + gather + 2 * d * E + 2 * B * d * 2,
+                kept_frac=kept_cols / (f * len(experts)), pairs=B * k)
+
+
 def algorithmic_bytes(layers, xs, ws_list):
-    """Bytes a step must move at the current thresholds, from the realised masks:
-    per active expert the packed up projection plus 4 d bytes per kept column (gate
-    row + down row), the router weight, x in and y out.  Also per kernel."""
+    """count_bytes of every layer copy at the current thresholds, from the masks the
+    layer itself returns."""
     import sparse_expert_swiglu_gb300 as ses
     W = WORKLOAD
     d, f, E, k, B = W["d"], W["f"], W["E"], W["k"], W["B"]
@@ -285,20 +305,7 @@ def algorithmic_bytes(layers, xs, ws_list):
     rows = []
     for layer, x, ws in zip(layers, xs, ws_list):
         _, dbg = ses.layer_decode(x, layer, rmsnorm=True, ws=ws, debug=True)
-        idx = dbg["topk_idx"].cpu().numpy()
-        words = dbg["mask"].cpu().numpy().astype(np.uint32)
-        bits = ((words[..., :, None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(B, k, -1)[..., :f]
-        kept_cols, up_total = 0, 0
-        for e in sorted(set(idx.ravel().tolist())):
-            rws, cls = np.nonzero(idx == e)
-            union = np.any(bits[rws, cls].astype(bool), axis=0)
-            kept_cols += int(union.sum())
-            up_total += up_bytes
-        gather = 4 * d * kept_cols
-        rows.append(dict(up=up_total + 2 * B * d, gather=gather, route=2 * d * E + 2 * B * d,
-                         total=up_total + gather + 2 * d * E + 2 * B * d * 2,
-                         kept_frac=kept_cols / (f * len(set(idx.ravel().tolist()))),
-                         pairs=B * k))
+        rows.append(count_bytes(dbg["topk_idx"].cpu().numpy(), dbg["mask"].cpu().numpy(), d, f, E, k, B, up_bytes))
     return rows
 
 
